@@ -1,0 +1,292 @@
+/*
+ * Exact attention oracle: TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-threaded fp64 restatement of what the attention hot
+ * path computes.  Only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg may load this file's library; the product path never does.
+ * It shares no code, header or constant with the CUDA library.
+ *
+ * Definitions followed:
+ *   - Forward, O = softmax(scale * Q K^T [+ causal mask]) V per head:
+ *     SparkAttention (arXiv 2502.12784), Equation 1 and the masked decoder MHA
+ *     of Figure 1; the same formula restated in the CANN ops-transformer MHA
+ *     article, section 1 ("MHA 计算的瓦片化分解"), with scale = 1/sqrt(d_k).
+ *   - Saved row statistic LSE_q = m_q + ln(sum_k exp(s_qk - m_q)):
+ *     StreamKL summary (gist.science 2606.20005), Methodology 1 (LSE_t = m_t +
+ *     log l_t) and 2 (probabilities regenerated as P = exp(S - LSE)).
+ *   - Backward for the loss sum(O * dO): SparkAttention, Figure 9 / Equation 4
+ *     (dPsum term, dS = P o (dP - dPsum)); the equation body is not printed on
+ *     the page, so the exact gradient of the forward above is written out:
+ *       dV = P^T dO,  dP = dO V^T,  D_q = sum_k P_qk dP_qk,
+ *       dS = P o (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
+ *
+ * Conventions (the plainest readings where the pages are silent):
+ *   - tensors are contiguous row-major [B][H][N][d]; LSE and D are [B][H][Nq];
+ *   - causal masking is top-left aligned: query q sees keys k <= q;
+ *   - LSE is in natural-log units of the scaled scores;
+ *   - D is the softmax Jacobian term sum_k P_qk dP_qk (mathematically equal to
+ *     rowsum(dO o O)).
+ *
+ * No blocking, fusion or reordering beyond the definitions: each query row is
+ * evaluated on its own from its full score row.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdlib.h>
+#include <string.h>
+
+static int key_visible(long q, long k, int causal) { return !causal || k <= q; }
+
+static double dot(const double* a, const double* b, int d) {
+  double acc = 0.0;
+  for (int c = 0; c < d; ++c) acc += a[c] * b[c];
+  return acc;
+}
+
+/*
+ * Probabilities of one query row q of one head:
+ *   s_k = scale <Q_q, K_k> for visible keys, m = max_k s_k,
+ *   P_k = exp(s_k - m) / sum_j exp(s_j - m), masked keys get P_k = 0,
+ *   *lse = m + ln(sum_j exp(s_j - m)).
+ * Returns the number of visible keys (0 leaves P all zero and *lse = -inf).
+ */
+static long row_probs(const double* Qh, const double* Kh, long Nk, int d, long q,
+                      int causal, double scale, double* P, double* lse) {
+  const double* qrow = Qh + (size_t)q * d;
+  double m = -INFINITY;
+  long nvis = 0;
+  for (long k = 0; k < Nk; ++k) {
+    if (key_visible(q, k, causal)) {
+      P[k] = scale * dot(qrow, Kh + (size_t)k * d, d);
+      if (P[k] > m) m = P[k];
+      ++nvis;
+    } else {
+      P[k] = 0.0;
+    }
+  }
+  if (nvis == 0) {
+    *lse = -INFINITY;
+    return 0;
+  }
+  double z = 0.0;
+  for (long k = 0; k < Nk; ++k) {
+    if (key_visible(q, k, causal)) {
+      P[k] = exp(P[k] - m);
+      z += P[k];
+    }
+  }
+  for (long k = 0; k < Nk; ++k) P[k] /= z;
+  *lse = m + log(z);
+  return nvis;
+}
+
+/* dP_k = <dO_q, V_k> for every key; returns D_q = sum_k P_k dP_k. */
+static double row_dp(const double* dOh, const double* Vh, long Nk, int d, long q,
+                     const double* P, double* dP) {
+  const double* dorow = dOh + (size_t)q * d;
+  double D = 0.0;
+  for (long k = 0; k < Nk; ++k) {
+    dP[k] = dot(dorow, Vh + (size_t)k * d, d);
+    D += P[k] * dP[k];
+  }
+  return D;
+}
+
+/* Full forward: O [B][H][Nq][d], LSE [B][H][Nq]. Returns 0, or -1 on allocation failure. */
+int oracle_attn_fwd(const double* Q, const double* K, const double* V, double* O, double* LSE,
+                    int B, int H, long Nq, long Nk, int d, int causal, double scale) {
+  double* P = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  if (!P) return -1;
+  for (long bh = 0; bh < (long)B * H; ++bh) {
+    const double* Qh = Q + (size_t)bh * Nq * d;
+    const double* Kh = K + (size_t)bh * Nk * d;
+    const double* Vh = V + (size_t)bh * Nk * d;
+    for (long q = 0; q < Nq; ++q) {
+      double lse;
+      row_probs(Qh, Kh, Nk, d, q, causal, scale, P, &lse);
+      double* orow = O + ((size_t)bh * Nq + q) * d;
+      for (int c = 0; c < d; ++c) orow[c] = 0.0;
+      for (long k = 0; k < Nk; ++k) {
+        if (P[k] == 0.0) continue;
+        const double* vrow = Vh + (size_t)k * d;
+        for (int c = 0; c < d; ++c) orow[c] += P[k] * vrow[c];
+      }
+      LSE[(size_t)bh * Nq + q] = lse;
+    }
+  }
+  free(P);
+  return 0;
+}
+
+/*
+ * Full backward of L = sum(O o dO): dQ [B][H][Nq][d], dK, dV [B][H][Nk][d];
+ * Dout [B][H][Nq] (may be NULL) receives D_q = sum_k P_qk dP_qk.
+ */
+int oracle_attn_bwd(const double* Q, const double* K, const double* V, const double* dO,
+                    double* dQ, double* dK, double* dV, double* Dout,
+                    int B, int H, long Nq, long Nk, int d, int causal, double scale) {
+  double* P = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  double* dP = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  if (!P || !dP) {
+    free(P);
+    free(dP);
+    return -1;
+  }
+  for (long bh = 0; bh < (long)B * H; ++bh) {
+    const double* Qh = Q + (size_t)bh * Nq * d;
+    const double* Kh = K + (size_t)bh * Nk * d;
+    const double* Vh = V + (size_t)bh * Nk * d;
+    const double* dOh = dO + (size_t)bh * Nq * d;
+    double* dQh = dQ + (size_t)bh * Nq * d;
+    double* dKh = dK + (size_t)bh * Nk * d;
+    double* dVh = dV + (size_t)bh * Nk * d;
+    memset(dKh, 0, sizeof(double) * (size_t)Nk * d);
+    memset(dVh, 0, sizeof(double) * (size_t)Nk * d);
+    for (long q = 0; q < Nq; ++q) {
+      double lse;
+      row_probs(Qh, Kh, Nk, d, q, causal, scale, P, &lse);
+      double D = row_dp(dOh, Vh, Nk, d, q, P, dP);
+      if (Dout) Dout[(size_t)bh * Nq + q] = D;
+      double* dqrow = dQh + (size_t)q * d;
+      const double* qrow = Qh + (size_t)q * d;
+      const double* dorow = dOh + (size_t)q * d;
+      for (int c = 0; c < d; ++c) dqrow[c] = 0.0;
+      for (long k = 0; k < Nk; ++k) {
+        if (!key_visible(q, k, causal)) continue;
+        double dS = P[k] * (dP[k] - D);
+        const double* krow = Kh + (size_t)k * d;
+        double* dkrow = dKh + (size_t)k * d;
+        double* dvrow = dVh + (size_t)k * d;
+        for (int c = 0; c < d; ++c) {
+          dqrow[c] += scale * dS * krow[c];
+          dkrow[c] += scale * dS * qrow[c];
+          dvrow[c] += P[k] * dorow[c];
+        }
+      }
+    }
+  }
+  free(P);
+  free(dP);
+  return 0;
+}
+
+/*
+ * Forward restricted to chosen query rows.  rows[i] = bh * Nq + q.
+ * O_rows [nrows][d], lse_rows [nrows].  Same definition as oracle_attn_fwd.
+ */
+int oracle_attn_fwd_rows(const double* Q, const double* K, const double* V,
+                         int B, int H, long Nq, long Nk, int d, int causal, double scale,
+                         long nrows, const long* rows, double* O_rows, double* lse_rows) {
+  (void)B;
+  (void)H;
+  double* P = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  if (!P) return -1;
+  for (long i = 0; i < nrows; ++i) {
+    long bh = rows[i] / Nq, q = rows[i] % Nq;
+    const double* Qh = Q + (size_t)bh * Nq * d;
+    const double* Kh = K + (size_t)bh * Nk * d;
+    const double* Vh = V + (size_t)bh * Nk * d;
+    row_probs(Qh, Kh, Nk, d, q, causal, scale, P, &lse_rows[i]);
+    double* orow = O_rows + (size_t)i * d;
+    for (int c = 0; c < d; ++c) orow[c] = 0.0;
+    for (long k = 0; k < Nk; ++k) {
+      if (P[k] == 0.0) continue;
+      for (int c = 0; c < d; ++c) orow[c] += P[k] * Vh[(size_t)k * d + c];
+    }
+  }
+  free(P);
+  return 0;
+}
+
+/* dQ restricted to chosen query rows (rows[i] = bh * Nq + q); dQ_rows [nrows][d], D_rows [nrows] (nullable). */
+int oracle_attn_dq_rows(const double* Q, const double* K, const double* V, const double* dO,
+                        int B, int H, long Nq, long Nk, int d, int causal, double scale,
+                        long nrows, const long* rows, double* dQ_rows, double* D_rows) {
+  (void)B;
+  (void)H;
+  double* P = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  double* dP = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  if (!P || !dP) {
+    free(P);
+    free(dP);
+    return -1;
+  }
+  for (long i = 0; i < nrows; ++i) {
+    long bh = rows[i] / Nq, q = rows[i] % Nq;
+    const double* Qh = Q + (size_t)bh * Nq * d;
+    const double* Kh = K + (size_t)bh * Nk * d;
+    const double* Vh = V + (size_t)bh * Nk * d;
+    const double* dOh = dO + (size_t)bh * Nq * d;
+    double lse;
+    row_probs(Qh, Kh, Nk, d, q, causal, scale, P, &lse);
+    double D = row_dp(dOh, Vh, Nk, d, q, P, dP);
+    if (D_rows) D_rows[i] = D;
+    double* dqrow = dQ_rows + (size_t)i * d;
+    for (int c = 0; c < d; ++c) dqrow[c] = 0.0;
+    for (long k = 0; k < Nk; ++k) {
+      if (!key_visible(q, k, causal)) continue;
+      double dS = P[k] * (dP[k] - D);
+      for (int c = 0; c < d; ++c) dqrow[c] += scale * dS * Kh[(size_t)k * d + c];
+    }
+  }
+  free(P);
+  free(dP);
+  return 0;
+}
+
+/*
+ * dK and dV restricted to chosen key columns (cols[i] = bh * Nk + k);
+ * dK_cols, dV_cols [ncols][d].  Every query row that sees a chosen key is
+ * evaluated in full (its whole score row), exactly as in oracle_attn_bwd.
+ */
+int oracle_attn_dkdv_cols(const double* Q, const double* K, const double* V, const double* dO,
+                          int B, int H, long Nq, long Nk, int d, int causal, double scale,
+                          long ncols, const long* cols, double* dK_cols, double* dV_cols) {
+  double* P = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  double* dP = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  if (!P || !dP) {
+    free(P);
+    free(dP);
+    return -1;
+  }
+  memset(dK_cols, 0, sizeof(double) * (size_t)ncols * d);
+  memset(dV_cols, 0, sizeof(double) * (size_t)ncols * d);
+  for (long bh = 0; bh < (long)B * H; ++bh) {
+    /* smallest chosen key of this head: rows q < kmin see none of them when causal */
+    long kmin = -1;
+    for (long i = 0; i < ncols; ++i)
+      if (cols[i] / Nk == bh && (kmin < 0 || cols[i] % Nk < kmin)) kmin = cols[i] % Nk;
+    if (kmin < 0) continue;
+    const double* Qh = Q + (size_t)bh * Nq * d;
+    const double* Kh = K + (size_t)bh * Nk * d;
+    const double* Vh = V + (size_t)bh * Nk * d;
+    const double* dOh = dO + (size_t)bh * Nq * d;
+    for (long q = causal ? kmin : 0; q < Nq; ++q) {
+      double lse;
+      row_probs(Qh, Kh, Nk, d, q, causal, scale, P, &lse);
+      double D = row_dp(dOh, Vh, Nk, d, q, P, dP);
+      const double* qrow = Qh + (size_t)q * d;
+      const double* dorow = dOh + (size_t)q * d;
+      for (long i = 0; i < ncols; ++i) {
+        if (cols[i] / Nk != bh) continue;
+        long k = cols[i] % Nk;
+        if (!key_visible(q, k, causal)) continue;
+        double dS = P[k] * (dP[k] - D);
+        for (int c = 0; c < d; ++c) {
+          dK_cols[(size_t)i * d + c] += scale * dS * qrow[c];
+          dV_cols[(size_t)i * d + c] += P[k] * dorow[c];
+        }
+      }
+    }
+  }
+  free(P);
+  free(dP);
+  return 0;
+}
+
+/* The full probability matrix of one head, P [Nq][Nk] (small shapes; used by invariant checks). */
+int oracle_attn_probs(const double* Qh, const double* Kh, long Nq, long Nk, int d, int causal,
+                      double scale, double* P, double* lse) {
+  for (long q = 0; q < Nq; ++q) row_probs(Qh, Kh, Nk, d, q, causal, scale, P + (size_t)q * Nk, &lse[q]);
+  return 0;
+}
