@@ -1,0 +1,491 @@
+// Fused attention backward for sm_103a: three launches on one stream.
+//
+// 1. bwd_pre_kernel: D_q = rowsum(dO o O) in fp32 (SparkAttention Figure 9,
+//    "dPsum"), LSE converted to base 2 (padding rows get +inf so that their
+//    recomputed probabilities are exactly 0), and the fp32 dQ accumulator
+//    zeroed.
+// 2. bwd_main_kernel: one CTA per 128-row key/value block of one (batch,
+//    head) -- the backward pass is parallel over blocks of columns of the
+//    attention matrix ("Fast Transformer training with long sequences",
+//    backward parallelisation).  K_j, V_j stay resident; for every query tile
+//    i that sees them (causal: i >= j) it recomputes
+//        S^T = K_j Q_i^T,  P^T = exp2(S^T*scale*log2e - LSE2_i)
+//        dP^T = V_j dO_i^T, dS^T = P^T o (dP^T - D_i)
+//        dV_j += P^T dO_i,  dK_j += dS^T Q_i,  dQ_i += dS K_j
+//    (StreamKL summary, Methodology 2: P regenerated tile by tile from the
+//    stored LSE), accumulating dK_j, dV_j in TMEM and reducing dQ_i into the
+//    fp32 accumulator with vector atomics (SparkAttention: dQ is atomically
+//    added across thread blocks; StreamKL: atomics while the buffer fits in L2).
+// 3. bwd_dq_convert_kernel: dQ = scale * dQacc rounded to the input dtype.
+//
+// Main-kernel warp roles (448 threads):
+//   warps 0-3   dQ drain: TMEM dQ_i -> registers -> red.global.add.v4.f32
+//   warps 4-7   compute, query columns [0, 64) of each tile (thread = key row)
+//   warps 8-11  compute, query columns [64, 128)
+//   warp  12    TMA producer: K_j, V_j once; Q_i, dO_i through an NR-slot ring
+//   warp  13    MMA issuer (one thread) and TMEM owner
+// Tensor memory: X = [0,128) holds S^T then dP^T of the current tile,
+// Y = [128, 128+d) holds dQ_i, dV at [256, 256+d), dK at [384, 384+d).
+// Shared memory: K_j, V_j, P^T and dS^T (128 x 128, 16-bit), and the Q/dO ring.
+// Per tile the MMA issue order is S_{i+1}, dK_i, dV_i, dQ_i, dP_{i+1}, so the
+// exponentials of tile i+1 overlap the three gradient MMAs of tile i.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace exattn {
+namespace {
+
+constexpr int kBwdThreads = 448;
+constexpr uint32_t kChunkBytes = 128 * 128;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int NCH = D / 64;
+  static constexpr uint32_t TILE = kTileRows * D * 2;
+  static constexpr uint32_t PT = 128 * 128 * 2;  // P^T / dS^T tile
+  static constexpr int NR = (D == 64) ? 6 : 3;   // Q/dO ring slots
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = OFF_K + TILE;
+  static constexpr uint32_t OFF_P = OFF_V + TILE;
+  static constexpr uint32_t OFF_DS = OFF_P + PT;
+  static constexpr uint32_t OFF_RING = OFF_DS + PT;
+  static constexpr uint32_t OFF_BAR = OFF_RING + NR * TILE;
+  // kv_full, ring_full[NR], ring_empty[NR], s_full, s_used, dp_full, ds_ready, p_empty, ds_empty,
+  // dq_full, dq_empty, done, mma_done
+  static constexpr int NBAR = 1 + 2 * NR + 10;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t BYTES = OFF_MISC + 16;
+  static constexpr uint32_t SMEM_ALLOC = BYTES + 1024;
+};
+
+struct BwdBars {
+  uint32_t base;
+  int nr;
+  __device__ uint32_t kv_full() const { return base; }
+  __device__ uint32_t ring_full(int s) const { return base + 8 * (1 + s); }
+  __device__ uint32_t ring_empty(int s) const { return base + 8 * (1 + nr + s); }
+  __device__ uint32_t at(int k) const { return base + 8 * (1 + 2 * nr + k); }
+  __device__ uint32_t s_full() const { return at(0); }
+  __device__ uint32_t s_used() const { return at(1); }
+  __device__ uint32_t dp_full() const { return at(2); }
+  __device__ uint32_t ds_ready() const { return at(3); }
+  __device__ uint32_t p_empty() const { return at(4); }
+  __device__ uint32_t ds_empty() const { return at(5); }
+  __device__ uint32_t dq_full() const { return at(6); }
+  __device__ uint32_t dq_empty() const { return at(7); }
+  __device__ uint32_t done() const { return at(8); }
+  __device__ uint32_t mma_done() const { return at(9); }
+};
+
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __maxnreg__(144) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
+  using C = BwdCfg<D>;
+  constexpr int NR = C::NR;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw);
+  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sP = sbase + C::OFF_P, sDS = sbase + C::OFF_DS;
+  const uint32_t sRing = sbase + C::OFF_RING;
+  const BwdBars bars{sbase + C::OFF_BAR, NR};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_MISC + 4);
+  const WaitCtx wc{abort_flag, a.err_word, a.timeout_ns};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int jb = blockIdx.y;  // key block; causal work decreases with jb, so low jb are scheduled first
+  const int k0 = jb * kTileRows;
+  const int nq_tiles = (a.Nq + kTileRows - 1) / kTileRows;
+  const int i_start = CAUSAL ? jb : 0;
+  const int n = max(0, nq_tiles - i_start);  // query tiles this block visits
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0u;
+    mbar_init(bars.kv_full(), 1);
+    for (int s = 0; s < NR; ++s) {
+      mbar_init(bars.ring_full(s), 1);
+      mbar_init(bars.ring_empty(s), 1);
+    }
+    mbar_init(bars.s_full(), 1);
+    mbar_init(bars.s_used(), 256);
+    mbar_init(bars.dp_full(), 1);
+    mbar_init(bars.ds_ready(), 256);
+    mbar_init(bars.p_empty(), 1);
+    mbar_init(bars.ds_empty(), 1);
+    mbar_init(bars.dq_full(), 1);
+    mbar_init(bars.dq_empty(), 128);
+    mbar_init(bars.done(), 1);
+    mbar_init(bars.mma_done(), 1);
+    fence_mbar_init();
+  }
+  if (warp == 13) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tX = tmem, tY = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+
+  if (warp == 12) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n > 0) {
+      prefetch_tmap(&a.tm_q);
+      prefetch_tmap(&a.tm_do);
+      mbar_arrive_expect_tx(bars.kv_full(), 2 * C::TILE);
+      for (int c = 0; c < C::NCH; ++c) {
+        tma_load_3d(sK + c * kChunkBytes, &a.tm_k, c * 64, k0, bh, bars.kv_full());
+        tma_load_3d(sV + c * kChunkBytes, &a.tm_v, c * 64, k0, bh, bars.kv_full());
+      }
+      int issued = 0;
+      for (int L = 0; L < 2 * n; ++L) {
+        const int s = L % NR;
+        if (!mbar_wait(bars.ring_empty(s), ((L / NR) & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(bars.ring_full(s), C::TILE);
+        const CUtensorMap* map = (L & 1) ? &a.tm_do : &a.tm_q;
+        const int q_row = (i_start + (L >> 1)) * kTileRows;
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(sRing + s * C::TILE + c * kChunkBytes, map, c * 64, q_row, bh, bars.ring_full(s));
+        ++issued;
+      }
+      if (*abort_flag) {
+        for (int L = max(0, issued - NR); L < issued; ++L) mbar_drain(bars.ring_full(L % NR), (L / NR) & 1, a.timeout_ns);
+        mbar_drain(bars.kv_full(), 0, a.timeout_ns);
+      }
+    }
+  } else if (warp == 13) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idS = idesc_f16(128, 128, BF16, false, false);   // K-major x K-major
+      constexpr uint32_t idG = idesc_f16(128, D, BF16, false, true);      // dV, dK: A K-major, B MN-major
+      constexpr uint32_t idQ = idesc_f16(128, D, BF16, true, true);       // dQ: A = dS MN-major, B = K MN-major
+      auto slot_of = [](int L) { return L % NR; };
+      auto phase_of = [](int L) { return static_cast<uint32_t>((L / NR) & 1); };
+
+      // S^T_i = K Q_i^T into X
+      auto issue_S = [&](int it) -> bool {
+        const int L = 2 * it;
+        if (!mbar_wait(bars.ring_full(slot_of(L)), phase_of(L), wc)) return false;
+        tc_fence_after();
+        const uint32_t sq = sRing + slot_of(L) * C::TILE;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
+          mma_ss(tX, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sq + off, 16, 1024), idS, k > 0);
+        }
+        mma_commit(bars.s_full());
+        return true;
+      };
+      // dP^T_i = V dO_i^T into X (after the compute warps have read S^T_i)
+      auto issue_dP = [&](int it) -> bool {
+        const int L = 2 * it + 1;
+        if (!mbar_wait(bars.ring_full(slot_of(L)), phase_of(L), wc)) return false;
+        if (!mbar_wait(bars.s_used(), it & 1, wc)) return false;
+        tc_fence_after();
+        const uint32_t sdo = sRing + slot_of(L) * C::TILE;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
+          mma_ss(tX, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024), idS, k > 0);
+        }
+        mma_commit(bars.dp_full());
+        return true;
+      };
+
+      bool ok = mbar_wait(bars.kv_full(), 0, wc);
+      if (ok) ok = issue_S(0);
+      if (ok) ok = issue_dP(0);
+      for (int it = 0; ok && it < n; ++it) {
+        if (!(ok = mbar_wait(bars.ds_ready(), it & 1, wc))) break;
+        tc_fence_after();
+        if (it + 1 < n && !(ok = issue_S(it + 1))) break;
+        const uint32_t sq = sRing + slot_of(2 * it) * C::TILE;
+        const uint32_t sdo = sRing + slot_of(2 * it + 1) * C::TILE;
+        // dK += dS^T Q_i   (A: dS^T [key][query] K-major; B: Q_i [query][d] MN-major)
+#pragma unroll
+        for (int k = 0; k < 128 / 16; ++k) {
+          const uint32_t aoff = (k >> 2) * kChunkBytes + (k & 3) * 32;
+          mma_ss(tdK, sdesc_sw128(sDS + aoff, 16, 1024), sdesc_sw128(sq + k * 2048, kChunkBytes, 1024), idG,
+                 (it > 0 || k > 0));
+        }
+        mma_commit(bars.ring_empty(slot_of(2 * it)));
+        // dV += P^T dO_i
+#pragma unroll
+        for (int k = 0; k < 128 / 16; ++k) {
+          const uint32_t aoff = (k >> 2) * kChunkBytes + (k & 3) * 32;
+          mma_ss(tdV, sdesc_sw128(sP + aoff, 16, 1024), sdesc_sw128(sdo + k * 2048, kChunkBytes, 1024), idG,
+                 (it > 0 || k > 0));
+        }
+        mma_commit(bars.p_empty());
+        mma_commit(bars.ring_empty(slot_of(2 * it + 1)));
+        // dQ_i = dS K  (A: dS [query][key] read MN-major from the dS^T tile; B: K [key][d] MN-major)
+        if (it > 0 && !(ok = mbar_wait(bars.dq_empty(), (it - 1) & 1, wc))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 128 / 16; ++k)
+          mma_ss(tY, sdesc_sw128(sDS + k * 2048, kChunkBytes, 1024), sdesc_sw128(sK + k * 2048, kChunkBytes, 1024),
+                 idQ, k > 0);
+        mma_commit(bars.dq_full());
+        mma_commit(bars.ds_empty());
+        if (it + 1 < n && !(ok = issue_dP(it + 1))) break;
+      }
+      if (ok) mma_commit(bars.done());
+      mma_commit(bars.mma_done());
+      mbar_drain(bars.mma_done(), 0, a.timeout_ns);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ dQ drain
+    const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
+    const int r = warp * 32 + lane;  // query row inside the tile
+    for (int it = 0; it < n; ++it) {
+      if (!mbar_wait_warp(bars.dq_full(), it & 1, wc)) break;
+      tc_fence_after();
+      uint32_t v[D / 32][32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tY + lane_bits + c * 32, v[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) reg_fence32(v[c]);
+      tc_fence_before();
+      mbar_arrive(bars.dq_empty());
+      const size_t row = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows + r;
+      float* dst = a.dq_acc + row * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          red_add_v4(dst + c * 32 + u * 4, __uint_as_float(v[c][4 * u]), __uint_as_float(v[c][4 * u + 1]),
+                     __uint_as_float(v[c][4 * u + 2]), __uint_as_float(v[c][4 * u + 3]));
+    }
+  } else {
+    // ------------------------------------------------------------ compute
+    const int h = (warp - 4) >> 2;       // query half: columns [64h, 64h + 64)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;   // key row inside the block = TMEM lane
+    const int kv = k0 + r;
+    const bool kv_valid = kv < a.Nk;
+    const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
+    const float c_log2 = a.scale * 1.4426950408889634f;
+    const uint32_t p_row = sP + h * kChunkBytes, ds_row = sDS + h * kChunkBytes;
+    bool ok = true;
+    for (int it = 0; it < n; ++it) {
+      const int qb = (i_start + it) * kTileRows + h * 64;  // first query column of this half
+      const float* lse2 = a.lse2 + static_cast<size_t>(bh) * a.Nq_pad + qb;
+      const float* dsum = a.dsum + static_cast<size_t>(bh) * a.Nq_pad + qb;
+      if (!(ok = mbar_wait_warp(bars.s_full(), it & 1, wc))) break;
+      tc_fence_after();
+      uint32_t s[2][32];
+      tmem_ld32(tX + lane_bits + h * 64, s[0]);
+      tmem_ld32(tX + lane_bits + h * 64 + 32, s[1]);
+      tmem_wait_ld();
+      reg_fence32(s[0]);
+      reg_fence32(s[1]);
+      tc_fence_before();
+      mbar_arrive(bars.s_used());
+
+      // P^T = exp2(S^T * scale*log2e - LSE2); masked entries are exactly 0.
+      const bool diag = CAUSAL && (i_start + it == jb);
+      float p[64];
+#pragma unroll
+      for (int c = 0; c < 64; c += 4) {
+        const float4 l4 = __ldg(reinterpret_cast<const float4*>(lse2 + c));
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int col = c + e;
+          float x = ex2_approx(fmaf(__uint_as_float(s[col >> 5][col & 31]), c_log2, -lv[e]));
+          if (!kv_valid || (diag && qb + col < kv)) x = 0.f;
+          p[col] = x;
+        }
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(p[2 * i], p[2 * i + 1]);
+      if (it > 0 && !(ok = mbar_wait_warp(bars.p_empty(), (it - 1) & 1, wc))) break;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        st_shared_v4(p_row + sw128_offset(r, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+
+      if (!(ok = mbar_wait_warp(bars.dp_full(), it & 1, wc))) break;
+      tc_fence_after();
+      tmem_ld32(tX + lane_bits + h * 64, s[0]);
+      tmem_ld32(tX + lane_bits + h * 64 + 32, s[1]);
+      tmem_wait_ld();
+      reg_fence32(s[0]);
+      reg_fence32(s[1]);
+      // dS^T = P^T o (dP^T - D)
+#pragma unroll
+      for (int c = 0; c < 64; c += 4) {
+        const float4 d4 = __ldg(reinterpret_cast<const float4*>(dsum + c));
+        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int col = c + e;
+          p[col] = p[col] * (__uint_as_float(s[col >> 5][col & 31]) - dv[e]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(p[2 * i], p[2 * i + 1]);
+      if (it > 0 && !(ok = mbar_wait_warp(bars.ds_empty(), (it - 1) & 1, wc))) break;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        st_shared_v4(ds_row + sw128_offset(r, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bars.ds_ready());
+    }
+
+    // ------------------------------------------------------------ epilogue
+    // warps 4-7 write dV (staged in the V tile), warps 8-11 write dK * scale (staged in the K tile).
+    if (ok && n > 0) ok = mbar_wait_warp(bars.done(), 0, wc);
+    const uint32_t stage = h ? sK : sV;
+    const uint32_t tacc = (h ? tdK : tdV) + lane_bits;
+    const float mul = h ? a.scale : 1.0f;
+    if (ok) {
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < C::NCH; ++ch) {
+        uint32_t o[2][32];
+        if (n > 0) {
+          tmem_ld32(tacc + ch * 64, o[0]);
+          tmem_ld32(tacc + ch * 64 + 32, o[1]);
+          tmem_wait_ld();
+          reg_fence32(o[0]);
+          reg_fence32(o[1]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[0][i] = o[1][i] = 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int hh = u >> 2, b = (u & 3) * 8;
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack2<BF16>(__uint_as_float(o[hh][b + 2 * e]) * mul, __uint_as_float(o[hh][b + 2 * e + 1]) * mul);
+          st_shared_v4(stage + ch * kChunkBytes + sw128_offset(r, u), w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1 + h, 128);
+    if (ok && r == 0 && !*abort_flag) {
+      const CUtensorMap* map = h ? &a.tm_dk : &a.tm_dv;
+      for (int ch = 0; ch < C::NCH; ++ch) tma_store_3d(map, stage + ch * kChunkBytes, ch * 64, k0, bh);
+      tma_store_commit();
+      tma_store_wait_all();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 13) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// D = rowsum(dO o O), LSE2 = LSE * log2(e) (+inf on padding rows), dQacc = 0.
+// TPR threads per row, 8 elements (16 bytes) per thread.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ BwdArgs a) {
+  constexpr int TPR = D / 8;
+  constexpr int RPB = 256 / TPR;
+  const size_t row = static_cast<size_t>(blockIdx.x) * RPB + threadIdx.x / TPR;
+  const int sub = threadIdx.x % TPR;
+  const size_t total = static_cast<size_t>(a.bh_count) * a.Nq_pad;
+  const bool in_range = row < total;  // no early return: the whole warp takes part in the shuffles below
+  const int bh = in_range ? static_cast<int>(row / a.Nq_pad) : 0;
+  const int q = in_range ? static_cast<int>(row % a.Nq_pad) : a.Nq;
+  float acc = 0.f;
+  if (in_range && q < a.Nq) {
+    const size_t src = (static_cast<size_t>(bh) * a.Nq + q) * D + sub * 8;
+    const uint4 ov = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.o) + src));
+    const uint4 dv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dout) + src));
+    const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(unpack_lo<BF16>(ow[e]), unpack_lo<BF16>(dw[e]), acc);
+      acc = fmaf(unpack_hi<BF16>(ow[e]), unpack_hi<BF16>(dw[e]), acc);
+    }
+  }
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (!in_range) return;
+  float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D + sub * 8);
+  z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+  z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (sub == 0) {
+    if (q < a.Nq) {
+      a.lse2[row] = a.lse[static_cast<size_t>(bh) * a.Nq + q] * 1.4426950408889634f;
+      a.dsum[row] = acc;
+    } else {
+      a.lse2[row] = INFINITY;
+      a.dsum[row] = 0.f;
+    }
+  }
+}
+
+// dQ = scale * dQacc, rounded to the input dtype; 8 elements per thread.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const __grid_constant__ BwdArgs a) {
+  const size_t e = (static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x) * 8;
+  const size_t total = static_cast<size_t>(a.bh_count) * a.Nq * D;
+  if (e >= total) return;
+  const size_t row = e / D;
+  const int col = static_cast<int>(e % D);
+  const size_t bh = row / a.Nq, q = row % a.Nq;
+  const float4* src = reinterpret_cast<const float4*>(a.dq_acc + (bh * a.Nq_pad + q) * D + col);
+  const float4 x = src[0], y = src[1];
+  const float s = a.scale;
+  uint4 out;
+  out.x = pack2<BF16>(x.x * s, x.y * s);
+  out.y = pack2<BF16>(x.z * s, x.w * s);
+  out.z = pack2<BF16>(y.x * s, y.y * s);
+  out.w = pack2<BF16>(y.z * s, y.w * s);
+  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + e) = out;
+}
+
+template <int D, bool CAUSAL, bool BF16>
+cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  {
+    constexpr int RPB = 256 / (D / 8);
+    const size_t rows = static_cast<size_t>(a.bh_count) * a.Nq_pad;
+    bwd_pre_kernel<D, BF16><<<static_cast<unsigned>((rows + RPB - 1) / RPB), 256, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    auto kern = bwd_main_kernel<D, CAUSAL, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.bh_count, (a.Nk + kTileRows - 1) / kTileRows, 1);
+    kern<<<grid, kBwdThreads, C::SMEM_ALLOC, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const size_t total = static_cast<size_t>(a.bh_count) * a.Nq * D / 8;
+    bwd_dq_convert_kernel<D, BF16><<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(a);
+    return cudaGetLastError();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+  if (a.d == 64) {
+    if (a.causal) return a.bf16 ? launch_bwd_t<64, true, true>(a, stream) : launch_bwd_t<64, true, false>(a, stream);
+    return a.bf16 ? launch_bwd_t<64, false, true>(a, stream) : launch_bwd_t<64, false, false>(a, stream);
+  }
+  if (a.causal) return a.bf16 ? launch_bwd_t<128, true, true>(a, stream) : launch_bwd_t<128, true, false>(a, stream);
+  return a.bf16 ? launch_bwd_t<128, false, true>(a, stream) : launch_bwd_t<128, false, false>(a, stream);
+}
+
+}  // namespace exattn

@@ -1,0 +1,355 @@
+// Fused attention forward for sm_103a.
+//
+// One CTA owns 256 query rows of one (batch, head): two 128-row query tiles
+// Q0, Q1 that share every K/V tile it streams (SparkAttention, Figure 6: Q
+// read once, K/V streamed, O written once; parallel over batch x heads x
+// query-row blocks as in "Fast Transformer training with long sequences").
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax warpgroup for query tile 0 (thread = query row)
+//   warps 4-7  softmax warpgroup for query tile 1
+//   warp  8    TMA producer: Q once, then K_j / V_j into NS-deep rings
+//   warp  9    MMA issuer (one thread) and TMEM owner
+//
+// Tensor memory (512 columns x 128 lanes x 32 bit):
+//   [  0,128) S0 = Q0 K_j^T fp32; P0 (16-bit, packed in pairs) overwrites its first 64 columns
+//   [128,256) S1 / P1
+//   [256,256+d) O0 accumulator, [384,384+d) O1 accumulator
+//
+// Per key tile j and query tile t the MMA warp issues S_t = Q_t K_j^T, the
+// softmax warpgroup turns S_t into P_t = exp2(S_t*scale*log2e - m) with the
+// online running max m and running sum l (rescaling O_t in TMEM only when the
+// max grows by more than 2^8 -- the final O/l is exact either way), writes P_t
+// back into TMEM, and the MMA warp issues O_t += P_t V_j with P_t read from
+// TMEM.  Issue order S0[0] S1[0] | PV0[j] S0[j+1] PV1[j] S1[j+1] | ... keeps
+// the tensor pipe busy on one tile while the other tile's softmax runs.
+// Causal: key tiles past a query tile's diagonal are skipped entirely and only
+// the diagonal (or ragged last) tile is masked.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace exattn {
+namespace {
+
+constexpr int kFwdThreads = 320;
+constexpr uint32_t kChunkBytes = 128 * 128;  // 128 rows x 128 bytes
+
+template <int D>
+struct FwdCfg {
+  static constexpr int NCH = D / 64;                      // 128-byte chunks per row
+  static constexpr uint32_t TILE = kTileRows * D * 2;     // one 128-row 16-bit tile
+  static constexpr int NS = (D == 64) ? 4 : 2;            // K and V ring depth
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE;
+  static constexpr uint32_t OFF_V = OFF_K + NS * TILE;
+  static constexpr uint32_t OFF_BAR = OFF_V + NS * TILE;
+  // barriers: q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[2], p_full[2], o_full[2], mma_done
+  static constexpr int NBAR = 1 + 4 * NS + 7;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (4 B) + abort flag (4 B)
+  static constexpr uint32_t BYTES = OFF_MISC + 16;
+  static constexpr uint32_t SMEM_ALLOC = BYTES + 1024;      // slack for 1024-byte alignment
+};
+
+struct FwdBars {
+  uint32_t base;
+  int ns;
+  __device__ uint32_t q_full() const { return base; }
+  __device__ uint32_t k_full(int s) const { return base + 8 * (1 + s); }
+  __device__ uint32_t k_empty(int s) const { return base + 8 * (1 + ns + s); }
+  __device__ uint32_t v_full(int s) const { return base + 8 * (1 + 2 * ns + s); }
+  __device__ uint32_t v_empty(int s) const { return base + 8 * (1 + 3 * ns + s); }
+  __device__ uint32_t s_full(int t) const { return base + 8 * (1 + 4 * ns + t); }
+  __device__ uint32_t p_full(int t) const { return base + 8 * (3 + 4 * ns + t); }
+  __device__ uint32_t o_full(int t) const { return base + 8 * (5 + 4 * ns + t); }
+  __device__ uint32_t mma_done() const { return base + 8 * (7 + 4 * ns); }
+};
+
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __maxnreg__(200) fwd_kernel(const __grid_constant__ FwdArgs a) {
+  using C = FwdCfg<D>;
+  constexpr int NS = C::NS;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw);
+  const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+  const FwdBars bars{sbase + C::OFF_BAR, NS};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_MISC + 4);
+  const WaitCtx wc{abort_flag, a.err_word, a.timeout_ns};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int qb = gridDim.y - 1 - blockIdx.y;  // heaviest (causal) query blocks are scheduled first
+  const int q0 = qb * (kFwdSubTiles * kTileRows);
+  const int nkv = (a.Nk + kTileRows - 1) / kTileRows;
+  // key tiles visited by query tile 0 / 1 (causal: up to and including the diagonal tile)
+  const int ntile0 = CAUSAL ? min(nkv, q0 / kTileRows + 1) : nkv;
+  const int ntile1 = CAUSAL ? min(nkv, q0 / kTileRows + 2) : nkv;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0u;
+    mbar_init(bars.q_full(), 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bars.k_full(s), 1);
+      mbar_init(bars.k_empty(s), 1);
+      mbar_init(bars.v_full(s), 1);
+      mbar_init(bars.v_empty(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bars.s_full(t), 1);
+      mbar_init(bars.p_full(t), kTileRows);
+      mbar_init(bars.o_full(t), 1);
+    }
+    mbar_init(bars.mma_done(), 1);
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&a.tm_q);
+      prefetch_tmap(&a.tm_k);
+      prefetch_tmap(&a.tm_v);
+      mbar_arrive_expect_tx(bars.q_full(), 2 * C::TILE);
+      for (int t = 0; t < 2; ++t)
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(sQ + t * C::TILE + c * kChunkBytes, &a.tm_q, c * 64, q0 + t * kTileRows, bh, bars.q_full());
+      int issued_k = 0, issued_v = 0;
+      for (int j = 0; j < ntile1; ++j) {
+        const int s = j % NS;
+        const uint32_t ph = (j / NS) & 1;
+        if (!mbar_wait(bars.k_empty(s), ph ^ 1, wc)) break;
+        mbar_arrive_expect_tx(bars.k_full(s), C::TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(sK + s * C::TILE + c * kChunkBytes, &a.tm_k, c * 64, j * kTileRows, bh, bars.k_full(s));
+        ++issued_k;
+        if (!mbar_wait(bars.v_empty(s), ph ^ 1, wc)) break;
+        mbar_arrive_expect_tx(bars.v_full(s), C::TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(sV + s * C::TILE + c * kChunkBytes, &a.tm_v, c * 64, j * kTileRows, bh, bars.v_full(s));
+        ++issued_v;
+      }
+      // On abort, every load this thread issued must land before the CTA exits.
+      if (*abort_flag) {
+        for (int j = max(0, issued_k - NS); j < issued_k; ++j) mbar_drain(bars.k_full(j % NS), (j / NS) & 1, a.timeout_ns);
+        for (int j = max(0, issued_v - NS); j < issued_v; ++j) mbar_drain(bars.v_full(j % NS), (j / NS) & 1, a.timeout_ns);
+        mbar_drain(bars.q_full(), 0, a.timeout_ns);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_f16(128, 128, BF16, false, false);
+      constexpr uint32_t idPV = idesc_f16(128, D, BF16, false, true);
+      bool ok = mbar_wait(bars.q_full(), 0, wc);
+
+      auto issue_S = [&](int t, int j) -> bool {
+        const int s = j % NS;
+        if (!mbar_wait(bars.k_full(s), (j / NS) & 1, wc)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
+          const uint64_t ad = sdesc_sw128(sQ + t * C::TILE + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sK + s * C::TILE + off, 16, 1024);
+          mma_ss(tmem + t * 128, ad, bd, idS, k > 0 ? 1u : 0u);
+        }
+        mma_commit(bars.s_full(t));
+        return true;
+      };
+      auto issue_PV = [&](int t, int j) -> bool {
+        const int s = j % NS;
+        if (!mbar_wait(bars.v_full(s), (j / NS) & 1, wc)) return false;
+        if (!mbar_wait(bars.p_full(t), j & 1, wc)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kTileRows / 16; ++k) {
+          const uint64_t bd = sdesc_sw128(sV + s * C::TILE + k * 2048, kChunkBytes, 1024);
+          mma_ts(tmem + 256 + t * 128, tmem + t * 128 + k * 8, bd, idPV, (j > 0 || k > 0) ? 1u : 0u);
+        }
+        return true;
+      };
+
+      if (ok) ok = issue_S(0, 0);
+      if (ok) ok = issue_S(1, 0);
+      if (ok) mma_commit(bars.k_empty(0));
+      for (int j = 0; ok && j < ntile1; ++j) {
+        if (j < ntile0) {
+          if (!(ok = issue_PV(0, j))) break;
+          if (j == ntile0 - 1) mma_commit(bars.o_full(0));
+          if (j + 1 < ntile0 && !(ok = issue_S(0, j + 1))) break;
+        }
+        if (!(ok = issue_PV(1, j))) break;
+        mma_commit(bars.v_empty(j % NS));
+        if (j == ntile1 - 1) mma_commit(bars.o_full(1));
+        if (j + 1 < ntile1) {
+          if (!(ok = issue_S(1, j + 1))) break;
+          mma_commit(bars.k_empty((j + 1) % NS));
+        }
+      }
+      // Every MMA issued above completes before TMEM can be released.
+      mma_commit(bars.mma_done());
+      mbar_drain(bars.mma_done(), 0, a.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;                  // query tile of this warpgroup
+    const int quarter = warp & 3;             // TMEM lane quarter this warp may access
+    const int r = quarter * 32 + lane;        // row inside the tile = TMEM lane
+    const int row = q0 + t * kTileRows + r;   // query index inside the head
+    const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + t * 128 + lane_bits;
+    const uint32_t tO = tmem + 256 + t * 128 + lane_bits;
+    const float c_log2 = a.scale * 1.4426950408889634f;  // scale * log2(e)
+    const int n = t ? ntile1 : ntile0;
+    float m = -INFINITY;  // running max of the scaled scores, base-2 units
+    float l = 0.f;        // running sum of exp2(score - m)
+    bool ok = true;
+
+    for (int j = 0; j < n; ++j) {
+      if (!(ok = mbar_wait_warp(bars.s_full(t), j & 1, wc))) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
+
+      const bool need_mask = ((j + 1) * kTileRows > a.Nk) || (CAUSAL && j * kTileRows + kTileRows - 1 > q0 + t * kTileRows);
+      if (need_mask) {
+        const int lim = (CAUSAL ? min(a.Nk, row + 1) : a.Nk) - j * kTileRows;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+      const float m_new = fmaxf(m, mx * c_log2);
+      if (j == 0) {
+        m = m_new;
+      } else {
+        const bool need = m_new > m + 8.0f;
+        if (__any_sync(0xffffffffu, need)) {
+          // O_t is complete for key tile j-1: its last MMA was issued before S_t[j].
+          const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_wait_ld();
+            reg_fence32(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + c * 32, o);
+          }
+          tmem_wait_st();
+          l *= alpha;
+          if (need) m = m_new;
+        }
+      }
+      const float ms = (m == -INFINITY) ? 0.f : m;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // columns [64h, 64h+64) -> packed columns [32h, 32h+32)
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = 2 * h + (i >> 4), e = (i & 15) * 2;
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), c_log2, -ms));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), c_log2, -ms));
+          l += p0 + p1;
+          pk[i] = pack2<BF16>(p0, p1);
+        }
+        tmem_st32(tS + h * 32, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bars.p_full(t));
+    }
+
+    // ------------------------------------------------------------ epilogue
+    if (ok) ok = mbar_wait_warp(bars.o_full(t), 0, wc);
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+      if (row < a.Nq) a.lse[static_cast<size_t>(bh) * a.Nq + row] = (m + __log2f(l)) * 0.6931471805599453f;
+      const uint32_t stage = sQ + t * C::TILE;  // Q_t is dead: all of its MMAs completed before o_full
+#pragma unroll
+      for (int ch = 0; ch < C::NCH; ++ch) {
+        uint32_t o[2][32];
+        tmem_ld32(tO + ch * 64, o[0]);
+        tmem_ld32(tO + ch * 64 + 32, o[1]);
+        tmem_wait_ld();
+        reg_fence32(o[0]);
+        reg_fence32(o[1]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int h = u >> 2, b = (u & 3) * 8;
+          const uint32_t w0 = pack2<BF16>(__uint_as_float(o[h][b + 0]) * inv_l, __uint_as_float(o[h][b + 1]) * inv_l);
+          const uint32_t w1 = pack2<BF16>(__uint_as_float(o[h][b + 2]) * inv_l, __uint_as_float(o[h][b + 3]) * inv_l);
+          const uint32_t w2 = pack2<BF16>(__uint_as_float(o[h][b + 4]) * inv_l, __uint_as_float(o[h][b + 5]) * inv_l);
+          const uint32_t w3 = pack2<BF16>(__uint_as_float(o[h][b + 6]) * inv_l, __uint_as_float(o[h][b + 7]) * inv_l);
+          st_shared_v4(stage + ch * kChunkBytes + sw128_offset(r, u), w0, w1, w2, w3);
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1 + t, 128);
+    if (ok && r == 0 && q0 + t * kTileRows < a.Nq && !*abort_flag) {
+      for (int ch = 0; ch < C::NCH; ++ch)
+        tma_store_3d(&a.tm_o, sQ + t * C::TILE + ch * kChunkBytes, ch * 64, q0 + t * kTileRows, bh);
+      tma_store_commit();
+      tma_store_wait_all();
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL, bool BF16>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = fwd_kernel<D, CAUSAL, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  const int nqb = (a.Nq + kFwdSubTiles * kTileRows - 1) / (kFwdSubTiles * kTileRows);
+  dim3 grid(a.bh_count, nqb, 1);
+  kern<<<grid, kFwdThreads, C::SMEM_ALLOC, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+  if (a.d == 64) {
+    if (a.causal) return a.bf16 ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, true, false>(a, stream);
+    return a.bf16 ? launch_fwd_t<64, false, true>(a, stream) : launch_fwd_t<64, false, false>(a, stream);
+  }
+  if (a.causal) return a.bf16 ? launch_fwd_t<128, true, true>(a, stream) : launch_fwd_t<128, true, false>(a, stream);
+  return a.bf16 ? launch_fwd_t<128, false, true>(a, stream) : launch_fwd_t<128, false, false>(a, stream);
+}
+
+}  // namespace exattn

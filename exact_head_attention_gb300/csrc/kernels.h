@@ -1,0 +1,45 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public header.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace exattn {
+
+constexpr int kTileRows = 128;   // query rows per MMA tile (tcgen05 M) and key rows per K/V tile
+constexpr int kFwdSubTiles = 2;  // query tiles per forward CTA (256 rows)
+
+struct FwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 3-D maps {d, N, B*H}, box {64, 128, 1}, 128-byte swizzle
+  float* lse;                          // [B*H][Nq]
+  uint32_t* err_word;
+  int bh_count, Nq, Nk, d;
+  bool causal, bf16;
+  float scale;
+  uint64_t timeout_ns;
+};
+
+struct BwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv;
+  const void* o;       // [B*H][Nq][d] 16-bit
+  const void* dout;    // [B*H][Nq][d] 16-bit
+  const float* lse;    // [B*H][Nq]
+  void* dq;            // [B*H][Nq][d] 16-bit
+  float* dq_acc;       // [B*H][Nq_pad][d] fp32 workspace
+  float* lse2;         // [B*H][Nq_pad] fp32 workspace: LSE * log2(e), +inf on padding rows
+  float* dsum;         // [B*H][Nq_pad] fp32 workspace: rowsum(dO o O), 0 on padding rows
+  uint32_t* err_word;
+  int bh_count, Nq, Nq_pad, Nk, d;
+  bool causal, bf16;
+  float scale;
+  uint64_t timeout_ns;
+};
+
+// Each returns cudaSuccess or the launch error.
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+
+}  // namespace exattn

@@ -1,0 +1,87 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI
+and compare with the fp64 CPU oracle on the same seeded inputs.
+
+Tolerances (fixed by the method's numeric contract):
+  forward O  max-abs  <= 1e-2 (bf16) / 2e-3 (fp16)
+  LSE        max-abs  <= 1e-3
+  dQ, dK, dV relative L2 <= 2e-2
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from exact_head_attention_gb300 import exattn, workloads
+
+O_TOL = {"bf16": 1e-2, "fp16": 2e-3}
+LSE_TOL = 1e-3
+GRAD_TOL = 2e-2
+
+
+def run_gpu(w: workloads.Workload, x: dict, backward: bool = True):
+    """Forward (+ backward) on cuda through the C ABI; results copied back to CPU fp32."""
+    dev = torch.device("cuda")
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o, lse = exattn.forward(q, k, v, w.causal, w.scale)
+    out = {"o": o, "lse": lse}
+    if backward:
+        do = x["do"].to(dev)
+        dq, dk, dv = exattn.backward(q, k, v, o, do, lse, w.causal, w.scale)
+        out.update(dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    status = exattn.check_device_error()
+    assert status == 0, f"device error word: {exattn.STATUS_NAMES.get(status)}"
+    return {key: t.float().cpu().numpy() for key, t in out.items()}
+
+
+def rel_l2(a, b) -> float:
+    return float(np.linalg.norm(np.asarray(a, np.float64) - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def check_fwd(w, got_o, got_lse, ref_o, ref_lse, what=""):
+    err_o = float(np.abs(got_o - ref_o).max()) if ref_o.size else 0.0
+    err_l = float(np.abs(got_lse - ref_lse).max()) if ref_lse.size else 0.0
+    assert np.isfinite(got_o).all() and np.isfinite(got_lse).all(), f"{what}: non-finite output"
+    assert err_o <= O_TOL[w.dtype], f"{what}: O max-abs {err_o:.3e} > {O_TOL[w.dtype]}"
+    assert err_l <= LSE_TOL, f"{what}: LSE max-abs {err_l:.3e} > {LSE_TOL}"
+    return err_o, err_l
+
+
+def check_grads(got: dict, ref: dict, what=""):
+    errs = {}
+    for name in ("dq", "dk", "dv"):
+        if name not in ref:
+            continue
+        assert np.isfinite(got[name]).all(), f"{what}: non-finite {name}"
+        errs[name] = rel_l2(got[name], ref[name])
+        assert errs[name] <= GRAD_TOL, f"{what}: {name} rel-L2 {errs[name]:.3e} > {GRAD_TOL}"
+    return errs
+
+
+def oracle_heads(w, x, heads, backward=True):
+    """Full oracle on a subset of (b, h) heads; returns arrays [len(heads), N, d]."""
+    sel = lambda t: torch.stack([t[b, h] for b, h in heads])[None]  # noqa: E731  -> [1, nh, N, d]
+    q, k, v = sel(x["q"]), sel(x["k"]), sel(x["v"])
+    o, lse = oracle.attn_fwd(q, k, v, w.causal, w.scale)
+    ref = {"o": o[0], "lse": lse[0]}
+    if backward:
+        dq, dk, dv, _ = oracle.attn_bwd(q, k, v, sel(x["do"]), w.causal, w.scale)
+        ref.update(dq=dq[0], dk=dk[0], dv=dv[0])
+    return ref
+
+
+def pick_heads(w, n=2):
+    all_heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    if len(all_heads) <= n:
+        return all_heads
+    return [all_heads[0], all_heads[-1]][:n]
+
+
+def sample_rows(N: int, n: int, seed: int) -> np.ndarray:
+    """First, last and random rows in between (sorted, unique)."""
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 2, 127, 128, N // 2, N - 2, N - 1]
+    rows = set(r for r in fixed if 0 <= r < N)
+    rows.update(rng.integers(0, N, size=max(0, n - len(rows))).tolist())
+    return np.array(sorted(rows), dtype=np.int64)

@@ -1,0 +1,87 @@
+"""C-ABI boundary checks that need no GPU: the library loads, exports every
+function include/exattn.h declares, and rejects bad arguments before touching
+the device (fake, never-dereferenced pointers are used)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_head_attention_gb300 import build, exattn
+    build.build()
+    return exattn.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "exattn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert {"attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    from exact_head_attention_gb300 import exattn
+    for code in range(8):
+        assert exattn.status_string(code)
+    assert exattn.status_string(99) == "unknown status"
+
+
+def test_workspace_size(lib):
+    from exact_head_attention_gb300 import exattn
+    # fp32 dQ accumulator over 128-row padded queries + two fp32 row vectors, each 256-byte aligned
+    assert exattn.workspace_size(1, 12, 8192, 128) == 12 * 8192 * 128 * 4 + 2 * 12 * 8192 * 4
+    rows = 2 * 3 * 256
+    assert exattn.workspace_size(2, 3, 129, 64) == rows * 64 * 4 + 2 * ((rows * 4 + 255) // 256 * 256)
+    for bad in ((0, 1, 1, 64), (1, 0, 1, 64), (1, 1, 0, 64), (1, 1, 1, 96)):
+        assert exattn.workspace_size(*bad) == 0
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation happens first
+
+
+def _fwd(lib, B=1, H=1, Nq=128, Nk=128, d=64, causal=0, scale=0.125, dtype=0, ptrs=None):
+    p = ptrs or [FAKE] * 5
+    return lib.attn_fwd(*[ctypes.c_void_p(x) if x is not None else None for x in p],
+                        B, H, Nq, Nk, d, causal, scale, dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), 1), (dict(H=-1), 1), (dict(Nq=0), 1), (dict(Nk=0), 1),
+    (dict(scale=0.0), 1), (dict(scale=-1.0), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(dtype=7), 1), (dict(d=96), 2), (dict(d=256), 2), (dict(Nq=65536 * 256), 1),
+    (dict(ptrs=[FAKE, None, FAKE, FAKE, FAKE]), 1),
+    (dict(ptrs=[FAKE, FAKE, FAKE + 8, FAKE, FAKE]), 3),
+    (dict(ptrs=[FAKE, FAKE, FAKE, FAKE, FAKE + 4]), 3),
+])
+def test_fwd_rejects_bad_arguments(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+
+
+def _bwd(lib, ws=FAKE, ws_bytes=None, ptrs=None, d=64, **kw):
+    B, H, Nq, Nk = kw.get("B", 1), kw.get("H", 1), kw.get("Nq", 128), kw.get("Nk", 128)
+    need = lib.attn_bwd_workspace_size(B, H, Nq, d)
+    p = ptrs or [FAKE] * 9
+    return lib.attn_bwd(*[ctypes.c_void_p(x) if x is not None else None for x in p],
+                        B, H, Nq, Nk, d, 0, 0.125, 0, ctypes.c_void_p(ws) if ws else None,
+                        need if ws_bytes is None else ws_bytes, None)
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    assert _bwd(lib, B=0) == 1
+    assert _bwd(lib, d=80) == 2
+    assert _bwd(lib, ptrs=[FAKE] * 8 + [None]) == 1
+    assert _bwd(lib, ws=None) == 6
+    assert _bwd(lib, ws_bytes=100) == 6
+    assert _bwd(lib, ptrs=[FAKE] * 6 + [FAKE + 2] + [FAKE] * 2) == 3
+    assert _bwd(lib, ws=FAKE + 16) == 3  # workspace must be 256-byte aligned

@@ -1,0 +1,171 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Small and ragged shapes are compared element by element over every output;
+the mid-size workloads on a subset of heads with the full oracle; the
+long-sequence workloads at full size on sampled query rows (O, LSE, dQ) and
+key rows (dK, dV) that the oracle evaluates one by one, plus gradient
+invariants that hold at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_head_attention_gb300 import workloads
+
+from parity import (check_fwd, check_grads, oracle_heads, pick_heads, rel_l2, run_gpu, sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+W = workloads.WORKLOADS
+
+# (B, H, Nq, Nk, d, dtype, causal): one tile, several tiles, ragged tails, Nq != Nk both ways, degenerate sizes
+SMALL = [
+    (1, 2, 128, 128, 64, "fp16", False),
+    (1, 2, 128, 128, 64, "fp16", True),
+    (1, 1, 1, 1, 64, "bf16", False),
+    (1, 1, 1, 1, 128, "bf16", True),
+    (1, 1, 7, 7, 64, "bf16", True),
+    (1, 2, 100, 100, 128, "bf16", True),
+    (2, 1, 129, 257, 64, "bf16", False),
+    (1, 1, 257, 129, 128, "fp16", True),
+    (1, 1, 257, 129, 64, "bf16", False),
+    (1, 2, 1000, 1000, 64, "bf16", True),
+    (1, 1, 300, 700, 128, "bf16", False),
+    (1, 1, 700, 300, 64, "fp16", True),
+    (1, 1, 513, 513, 128, "bf16", True),
+    (3, 2, 384, 384, 128, "fp16", False),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "B{}H{}q{}k{}d{}{}{}".format(*s[:6], "c" if s[6] else ""))
+def test_small_full_parity(shape):
+    B, H, Nq, Nk, d, dt, causal = shape
+    w = workloads.custom(B, H, Nq, Nk, d, dt, causal)
+    x = workloads.make_inputs(w)
+    got = run_gpu(w, x)
+    o, lse = oracle.attn_fwd(x["q"], x["k"], x["v"], causal, w.scale)
+    check_fwd(w, got["o"], got["lse"], o, lse, w.name)
+    dq, dk, dv, _ = oracle.attn_bwd(x["q"], x["k"], x["v"], x["do"], causal, w.scale)
+    check_grads(got, {"dq": dq, "dk": dk, "dv": dv}, w.name)
+
+
+@pytest.mark.parametrize("name", ["tiny_fp16"])
+def test_tiny_workload_full(name):
+    w = W[name]
+    x = workloads.make_inputs(w)
+    got = run_gpu(w, x)
+    o, lse = oracle.attn_fwd(x["q"], x["k"], x["v"], w.causal, w.scale)
+    check_fwd(w, got["o"], got["lse"], o, lse, name)
+    dq, dk, dv, _ = oracle.attn_bwd(x["q"], x["k"], x["v"], x["do"], w.causal, w.scale)
+    check_grads(got, {"dq": dq, "dk": dk, "dv": dv}, name)
+
+
+@pytest.mark.parametrize("name", ["self1k_bf16", "self1k_causal_bf16", "dec_self512_fp16", "dec_cross512x1024_fp16"])
+def test_midsize_workloads_on_head_subset(name):
+    w = W[name]
+    x = workloads.make_inputs(w)
+    got = run_gpu(w, x)
+    heads = pick_heads(w, 2)
+    ref = oracle_heads(w, x, heads)
+    sel = lambda a: np.stack([a[b, h] for b, h in heads])  # noqa: E731
+    check_fwd(w, sel(got["o"]), sel(got["lse"]), ref["o"], ref["lse"], name)
+    check_grads({k: sel(got[k]) for k in ("dq", "dk", "dv")}, ref, name)
+    _check_invariants(w, x, got, name)
+
+
+def _check_invariants(w, x, got, what):
+    """Per head: sum_k dK_k = 0 (rows of dS sum to 0) and sum_k dV_k = sum_q dO_q (rows of P sum to 1).
+
+    Both hold at any size; the bound is relative to the head's ||dK||_F and ||sum_q dO_q||."""
+    dk = got["dk"].astype(np.float64)
+    dk_sum = np.linalg.norm(dk.sum(axis=2), axis=-1)
+    dk_norm = np.linalg.norm(dk, axis=(2, 3))
+    assert (dk_sum <= 2e-2 * dk_norm + 1e-6).all(), f"{what}: sum_k dK_k != 0 ({(dk_sum / dk_norm).max():.2e})"
+    dv_sum = got["dv"].astype(np.float64).sum(axis=2)
+    do_sum = x["do"].double().sum(dim=2).numpy()
+    err = np.linalg.norm(dv_sum - do_sum, axis=-1) / np.maximum(np.linalg.norm(do_sum, axis=-1), 1e-30)
+    assert (err <= 2e-2).all(), f"{what}: sum_k dV_k != sum_q dO_q ({err.max():.2e})"
+
+
+def _sampled_check(w, x, got, n_rows, heads, seed):
+    N = w.Nq
+    for (b, h) in heads:
+        bh = b * w.H + h
+        rows = sample_rows(N, n_rows, seed + bh)
+        flat = bh * N + rows
+        o_r, lse_r = oracle.attn_fwd_rows(x["q"], x["k"], x["v"], w.causal, w.scale, flat)
+        check_fwd(w, got["o"][b, h, rows], got["lse"][b, h, rows], o_r, lse_r, f"{w.name} head {bh}")
+        dq_r, _ = oracle.attn_dq_rows(x["q"], x["k"], x["v"], x["do"], w.causal, w.scale, flat)
+        check_grads({"dq": got["dq"][b, h, rows]}, {"dq": dq_r}, f"{w.name} head {bh} dQ rows")
+        # key rows near the end: few query rows see them under the causal mask, so the oracle is cheap
+        cols = np.array(sorted({w.Nk - 1, w.Nk - 2, w.Nk - 64, w.Nk - 129, w.Nk - 200}), dtype=np.int64)
+        dk_c, dv_c = oracle.attn_dkdv_cols(x["q"], x["k"], x["v"], x["do"], w.causal, w.scale, bh * w.Nk + cols)
+        check_grads({"dk": got["dk"][b, h, cols], "dv": got["dv"][b, h, cols]}, {"dk": dk_c, "dv": dv_c},
+                    f"{w.name} head {bh} dK/dV rows")
+
+
+@pytest.mark.parametrize("name", ["long8k_causal_bf16", "ctx32k_d64_causal_bf16", "ctx32k_d128_causal_bf16"])
+def test_long_workloads_full_size_sampled(name):
+    w = W[name]
+    x = workloads.make_inputs(w)
+    got = run_gpu(w, x)
+    heads = [(0, 0), (w.B - 1, w.H - 1)]
+    _sampled_check(w, x, got, 48 if w.Nq > 10000 else 96, heads, seed=w.index)
+    _check_invariants(w, x, got, name)
+
+
+def test_outputs_written_everywhere():
+    """Outputs pre-filled with NaN must be fully overwritten (ragged shapes included)."""
+    from exact_head_attention_gb300 import exattn
+    w = workloads.custom(2, 3, 333, 271, 128, "bf16", True)
+    x = workloads.make_inputs(w)
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((w.B, w.H, w.Nq), float("nan"), device=dev)
+    assert exattn.fwd_raw(q, k, v, o, lse, w.causal, w.scale) == 0
+    dq, dk, dv = (torch.full_like(t, float("nan")) for t in (q, k, v))
+    ws = torch.full((exattn.workspace_size(w.B, w.H, w.Nq, w.d),), 0xFF, dtype=torch.uint8, device=dev)
+    assert exattn.bwd_raw(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, ws) == 0
+    torch.cuda.synchronize()
+    for t in (o, lse, dq, dk, dv):
+        assert torch.isfinite(t).all()
+
+
+def test_guard_bytes_untouched():
+    """Writes stay inside the outputs: sentinel bytes around each output are unchanged."""
+    from exact_head_attention_gb300 import exattn
+    w = workloads.custom(1, 2, 200, 150, 64, "fp16", False)
+    x = workloads.make_inputs(w)
+    dev = torch.device("cuda")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    pad = 4096
+
+    def guarded(like):
+        n = like.numel()
+        buf = torch.full((n + 2 * pad,), 12345.0, dtype=like.dtype, device=dev)
+        return buf, buf[pad:pad + n].view(like.shape)
+
+    ob, o = guarded(q)
+    lb, lse = guarded(torch.empty((w.B, w.H, w.Nq), dtype=torch.float32))
+    assert exattn.fwd_raw(q, k, v, o, lse, w.causal, w.scale) == 0
+    qb, dq = guarded(q)
+    kb, dk = guarded(k)
+    vb, dv = guarded(v)
+    ws = torch.empty(exattn.workspace_size(w.B, w.H, w.Nq, w.d), dtype=torch.uint8, device=dev)
+    assert exattn.bwd_raw(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, ws) == 0
+    torch.cuda.synchronize()
+    for buf in (ob, lb, qb, kb, vb):
+        assert (buf[:pad] == 12345.0).all() and (buf[-pad:] == 12345.0).all()
+
+
+def test_repeatable_forward_and_dkdv():
+    """Forward and dK/dV are bitwise repeatable; dQ (fp32 atomics) agrees within rounding."""
+    w = workloads.custom(1, 4, 1024, 1024, 128, "bf16", True)
+    x = workloads.make_inputs(w)
+    a = run_gpu(w, x)
+    b = run_gpu(w, x)
+    for key in ("o", "lse", "dk", "dv"):
+        assert np.array_equal(a[key], b[key]), key
+    assert rel_l2(a["dq"], b["dq"]) < 1e-3
