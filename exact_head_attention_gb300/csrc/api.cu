@@ -2,6 +2,7 @@
 // TMA tensor-map encoding, the per-device error word and kernel dispatch.
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -28,6 +29,18 @@ struct DeviceState {
 };
 
 std::mutex g_mutex;
+thread_local char g_last_error[256] = "";
+
+// Records a failing CUDA runtime call for attn_last_error and returns ATTN_ERR_CUDA.
+attn_status cuda_fail(const char* what, cudaError_t e) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+  return ATTN_ERR_CUDA;
+}
+
+attn_status driver_fail(const char* what, int code) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: CUresult %d", what, code);
+  return ATTN_ERR_CUDA;
+}
 DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -51,27 +64,28 @@ bool checked_mode() {
 // Per-device one-time set-up: capability check, error-word address, encoder.
 attn_status device_state(DeviceState** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceState& st = g_dev[dev];
   if (!st.ready) {
     int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail("cudaDeviceGetAttribute", e);
     st.supported = (major == 10 && minor == 3);
     if (st.supported) {
       void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return ATTN_ERR_CUDA;
+      if ((e = cudaGetSymbolAddress(&p, g_error_word)) != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
       st.err_word = static_cast<uint32_t*>(p);
-      if (cudaMemset(st.err_word, 0, sizeof(uint32_t)) != cudaSuccess) return ATTN_ERR_CUDA;
+      if ((e = cudaMemset(st.err_word, 0, sizeof(uint32_t))) != cudaSuccess) return cuda_fail("cudaMemset", e);
       if (!g_encode) {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || !fn)
-          return ATTN_ERR_CUDA;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess) return cuda_fail("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", e);
+        if (q != cudaDriverEntryPointSuccess || !fn) return driver_fail("cuTensorMapEncodeTiled lookup", q);
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
       }
     }
@@ -85,7 +99,7 @@ attn_status device_state(DeviceState** out) {
 // 3-D map over a contiguous [BH][N][d] 16-bit tensor; box = 64 columns x 128 rows x 1,
 // 128-byte swizzle (matches the kernels' shared-memory operand layout); rows
 // past N read as zero and are dropped on store.
-bool encode_map(CUtensorMap* map, const void* ptr, bool bf16, int bh, int n, int d) {
+CUresult encode_map(CUtensorMap* map, const void* ptr, bool bf16, int bh, int n, int d) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(n) * d * 2};
   const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTileRows), 1};
@@ -94,7 +108,7 @@ bool encode_map(CUtensorMap* map, const void* ptr, bool bf16, int bh, int n, int
                               const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return r;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -116,7 +130,7 @@ int padded_rows(int Nq) { return (Nq + kTileRows - 1) / kTileRows * kTileRows; }
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 attn_status finish(cudaError_t e, cudaStream_t stream) {
-  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_fail("kernel launch", e);
   if (checked_mode()) return attn_check_device_error(stream);
   return ATTN_OK;
 }
@@ -139,9 +153,10 @@ extern "C" attn_status attn_fwd(const void* Q, const void* K, const void* V, voi
   std::memset(&a, 0, sizeof(a));
   const bool bf16 = dtype == ATTN_BF16;
   const int bh = B * H;
-  if (!encode_map(&a.tm_q, Q, bf16, bh, Nq, d) || !encode_map(&a.tm_k, K, bf16, bh, Nk, d) ||
-      !encode_map(&a.tm_v, V, bf16, bh, Nk, d) || !encode_map(&a.tm_o, O, bf16, bh, Nq, d))
-    return ATTN_ERR_CUDA;
+  CUresult r;
+  if ((r = encode_map(&a.tm_q, Q, bf16, bh, Nq, d)) != CUDA_SUCCESS || (r = encode_map(&a.tm_k, K, bf16, bh, Nk, d)) != CUDA_SUCCESS ||
+      (r = encode_map(&a.tm_v, V, bf16, bh, Nk, d)) != CUDA_SUCCESS || (r = encode_map(&a.tm_o, O, bf16, bh, Nq, d)) != CUDA_SUCCESS)
+    return driver_fail("cuTensorMapEncodeTiled", r);
   a.lse = LSE;
   a.err_word = ds->err_word;
   a.bh_count = bh;
@@ -179,10 +194,11 @@ extern "C" attn_status attn_bwd(const void* Q, const void* K, const void* V, con
   std::memset(&a, 0, sizeof(a));
   const bool bf16 = dtype == ATTN_BF16;
   const int bh = B * H;
-  if (!encode_map(&a.tm_q, Q, bf16, bh, Nq, d) || !encode_map(&a.tm_k, K, bf16, bh, Nk, d) ||
-      !encode_map(&a.tm_v, V, bf16, bh, Nk, d) || !encode_map(&a.tm_do, dO, bf16, bh, Nq, d) ||
-      !encode_map(&a.tm_dk, dK, bf16, bh, Nk, d) || !encode_map(&a.tm_dv, dV, bf16, bh, Nk, d))
-    return ATTN_ERR_CUDA;
+  CUresult r;
+  if ((r = encode_map(&a.tm_q, Q, bf16, bh, Nq, d)) != CUDA_SUCCESS || (r = encode_map(&a.tm_k, K, bf16, bh, Nk, d)) != CUDA_SUCCESS ||
+      (r = encode_map(&a.tm_v, V, bf16, bh, Nk, d)) != CUDA_SUCCESS || (r = encode_map(&a.tm_do, dO, bf16, bh, Nq, d)) != CUDA_SUCCESS ||
+      (r = encode_map(&a.tm_dk, dK, bf16, bh, Nk, d)) != CUDA_SUCCESS || (r = encode_map(&a.tm_dv, dV, bf16, bh, Nk, d)) != CUDA_SUCCESS)
+    return driver_fail("cuTensorMapEncodeTiled", r);
   const int nq_pad = padded_rows(Nq);
   const size_t rows = static_cast<size_t>(bh) * nq_pad;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -225,13 +241,19 @@ extern "C" attn_status attn_check_device_error(void* stream) {
   DeviceState* ds = nullptr;
   attn_status st = device_state(&ds);
   if (st != ATTN_OK) return st;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
   uint32_t code = 0;
-  if (cudaMemcpy(&code, ds->err_word, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if ((e = cudaMemcpy(&code, ds->err_word, sizeof(code), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail("cudaMemcpy(error word)", e);
   if (code != 0) {
     const uint32_t zero = 0;
-    if (cudaMemcpy(ds->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+    if ((e = cudaMemcpy(ds->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail("cudaMemcpy(error word)", e);
+    std::snprintf(g_last_error, sizeof(g_last_error), "device error word %u (a bounded wait expired)", code);
     return ATTN_ERR_TIMEOUT;
   }
   return ATTN_OK;
 }
+
+extern "C" const char* attn_last_error(void) { return g_last_error; }

@@ -18,12 +18,12 @@
 //    added across thread blocks; StreamKL: atomics while the buffer fits in L2).
 // 3. bwd_dq_convert_kernel: dQ = scale * dQacc rounded to the input dtype.
 //
-// Main-kernel warp roles (448 threads):
-//   warps 0-3   dQ drain: TMEM dQ_i -> registers -> red.global.add.v4.f32
-//   warps 4-7   compute, query columns [0, 64) of each tile (thread = key row)
-//   warps 8-11  compute, query columns [64, 128)
-//   warp  12    TMA producer: K_j, V_j once; Q_i, dO_i through an NR-slot ring
-//   warp  13    MMA issuer (one thread) and TMEM owner
+// Main-kernel warp roles (320 threads):
+//   warps 0-3   compute, query columns [0, 64) of each tile (thread = key row),
+//               and dQ columns [0, d/2) of the drain (TMEM dQ_i -> red.global.add.v4.f32)
+//   warps 4-7   compute, query columns [64, 128), dQ columns [d/2, d)
+//   warp  8     TMA producer: K_j, V_j once; Q_i, dO_i through an NR-slot ring
+//   warp  9     MMA issuer (one thread) and TMEM owner
 // Tensor memory: X = [0,128) holds S^T then dP^T of the current tile,
 // Y = [128, 128+d) holds dQ_i, dV at [256, 256+d), dK at [384, 384+d).
 // Shared memory: K_j, V_j, P^T and dS^T (128 x 128, 16-bit), and the Q/dO ring.
@@ -38,7 +38,7 @@
 namespace exattn {
 namespace {
 
-constexpr int kBwdThreads = 448;
+constexpr int kBwdThreads = 320;
 constexpr uint32_t kChunkBytes = 128 * 128;
 
 template <int D>
@@ -81,7 +81,7 @@ struct BwdBars {
 };
 
 template <int D, bool CAUSAL, bool BF16>
-__global__ void __maxnreg__(144) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
   using C = BwdCfg<D>;
   constexpr int NR = C::NR;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -117,12 +117,12 @@ __global__ void __maxnreg__(144) bwd_main_kernel(const __grid_constant__ BwdArgs
     mbar_init(bars.p_empty(), 1);
     mbar_init(bars.ds_empty(), 1);
     mbar_init(bars.dq_full(), 1);
-    mbar_init(bars.dq_empty(), 128);
+    mbar_init(bars.dq_empty(), 256);
     mbar_init(bars.done(), 1);
     mbar_init(bars.mma_done(), 1);
     fence_mbar_init();
   }
-  if (warp == 13) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -132,7 +132,7 @@ __global__ void __maxnreg__(144) bwd_main_kernel(const __grid_constant__ BwdArgs
   const uint32_t tmem = *tmem_slot;
   const uint32_t tX = tmem, tY = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
 
-  if (warp == 12) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n > 0) {
       prefetch_tmap(&a.tm_q);
@@ -158,7 +158,7 @@ __global__ void __maxnreg__(144) bwd_main_kernel(const __grid_constant__ BwdArgs
         mbar_drain(bars.kv_full(), 0, a.timeout_ns);
       }
     }
-  } else if (warp == 13) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n > 0) {
       constexpr uint32_t idS = idesc_f16(128, 128, BF16, false, false);   // K-major x K-major
@@ -238,41 +238,42 @@ __global__ void __maxnreg__(144) bwd_main_kernel(const __grid_constant__ BwdArgs
       mma_commit(bars.mma_done());
       mbar_drain(bars.mma_done(), 0, a.timeout_ns);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ dQ drain
-    const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
-    const int r = warp * 32 + lane;  // query row inside the tile
-    for (int it = 0; it < n; ++it) {
-      if (!mbar_wait_warp(bars.dq_full(), it & 1, wc)) break;
-      tc_fence_after();
-      uint32_t v[D / 32][32];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(tY + lane_bits + c * 32, v[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) reg_fence32(v[c]);
-      tc_fence_before();
-      mbar_arrive(bars.dq_empty());
-      const size_t row = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows + r;
-      float* dst = a.dq_acc + row * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          red_add_v4(dst + c * 32 + u * 4, __uint_as_float(v[c][4 * u]), __uint_as_float(v[c][4 * u + 1]),
-                     __uint_as_float(v[c][4 * u + 2]), __uint_as_float(v[c][4 * u + 3]));
-    }
   } else {
     // ------------------------------------------------------------ compute
-    const int h = (warp - 4) >> 2;       // query half: columns [64h, 64h + 64)
+    const int h = warp >> 2;             // query half: columns [64h, 64h + 64); dQ columns [h*d/2, (h+1)*d/2)
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;   // key row inside the block = TMEM lane
+    const int r = quarter * 32 + lane;   // TMEM lane: key row of S^T/dP^T, query row of dQ_i
     const int kv = k0 + r;
     const bool kv_valid = kv < a.Nk;
     const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
     const float c_log2 = a.scale * 1.4426950408889634f;
     const uint32_t p_row = sP + h * kChunkBytes, ds_row = sDS + h * kChunkBytes;
     bool ok = true;
+
+    // dQ_i (TMEM Y, lane = query row) -> fp32 vector atomics into the accumulator; the TMEM
+    // columns are released as soon as they are in registers.
+    auto drain_dq = [&](int it) -> bool {
+      if (!mbar_wait_warp(bars.dq_full(), it & 1, wc)) return false;
+      tc_fence_after();
+      uint32_t v[D / 64][32];
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) tmem_ld32(tY + lane_bits + h * (D / 2) + c * 32, v[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) reg_fence32(v[c]);
+      tc_fence_before();
+      mbar_arrive(bars.dq_empty());
+      const size_t row = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows + r;
+      float* dst = a.dq_acc + row * D + h * (D / 2);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          red_add_v4(dst + c * 32 + u * 4, __uint_as_float(v[c][4 * u]), __uint_as_float(v[c][4 * u + 1]),
+                     __uint_as_float(v[c][4 * u + 2]), __uint_as_float(v[c][4 * u + 3]));
+      return true;
+    };
+
     for (int it = 0; it < n; ++it) {
       const int qb = (i_start + it) * kTileRows + h * 64;  // first query column of this half
       const float* lse2 = a.lse2 + static_cast<size_t>(bh) * a.Nq_pad + qb;
@@ -311,6 +312,9 @@ __global__ void __maxnreg__(144) bwd_main_kernel(const __grid_constant__ BwdArgs
       for (int u = 0; u < 8; ++u)
         st_shared_v4(p_row + sw128_offset(r, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
 
+      // dQ of the previous tile is ready while this tile's dP^T is still being computed.
+      if (it > 0 && !(ok = drain_dq(it - 1))) break;
+
       if (!(ok = mbar_wait_warp(bars.dp_full(), it & 1, wc))) break;
       tc_fence_after();
       tmem_ld32(tX + lane_bits + h * 64, s[0]);
@@ -340,8 +344,10 @@ __global__ void __maxnreg__(144) bwd_main_kernel(const __grid_constant__ BwdArgs
       mbar_arrive(bars.ds_ready());
     }
 
+    if (ok && n > 0) ok = drain_dq(n - 1);
+
     // ------------------------------------------------------------ epilogue
-    // warps 4-7 write dV (staged in the V tile), warps 8-11 write dK * scale (staged in the K tile).
+    // warps 0-3 write dV (staged in the V tile), warps 4-7 write dK * scale (staged in the K tile).
     if (ok && n > 0) ok = mbar_wait_warp(bars.done(), 0, wc);
     const uint32_t stage = h ? sK : sV;
     const uint32_t tacc = (h ? tdK : tdV) + lane_bits;
@@ -384,7 +390,7 @@ __global__ void __maxnreg__(144) bwd_main_kernel(const __grid_constant__ BwdArgs
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 13) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

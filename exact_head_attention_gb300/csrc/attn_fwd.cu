@@ -68,7 +68,7 @@ struct FwdBars {
 };
 
 template <int D, bool CAUSAL, bool BF16>
-__global__ void __maxnreg__(200) fwd_kernel(const __grid_constant__ FwdArgs a) {
+__global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdArgs a) {
   using C = FwdCfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -221,27 +221,25 @@ __global__ void __maxnreg__(200) fwd_kernel(const __grid_constant__ FwdArgs a) {
     for (int j = 0; j < n; ++j) {
       if (!(ok = mbar_wait_warp(bars.s_full(t), j & 1, wc))) break;
       tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
-
+      // Columns at or past `lim` are masked (ragged last key tile, causal diagonal tile).
       const bool need_mask = ((j + 1) * kTileRows > a.Nk) || (CAUSAL && j * kTileRows + kTileRows - 1 > q0 + t * kTileRows);
-      if (need_mask) {
-        const int lim = (CAUSAL ? min(a.Nk, row + 1) : a.Nk) - j * kTileRows;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
-      }
+      const int lim = need_mask ? (CAUSAL ? min(a.Nk, row + 1) : a.Nk) - j * kTileRows : kTileRows;
+      // Pass 1: row max over the 128 scores (read from TMEM 64 columns at a time).
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sr[2][32];
+        tmem_ld32(tS + hh * 64, sr[0]);
+        tmem_ld32(tS + hh * 64 + 32, sr[1]);
+        tmem_wait_ld();
+        reg_fence32(sr[0]);
+        reg_fence32(sr[1]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (hh * 64 + c * 32 + i < lim) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+      }
       const float m_new = fmaxf(m, mx * c_log2);
       if (j == 0) {
         m = m_new;
@@ -266,14 +264,25 @@ __global__ void __maxnreg__(200) fwd_kernel(const __grid_constant__ FwdArgs a) {
         }
       }
       const float ms = (m == -INFINITY) ? 0.f : m;
+      // Pass 2: P = exp2(s * scale*log2e - m), packed to 16-bit pairs; scores [64h, 64h+64) become
+      // packed columns [32h, 32h+32), which the MMA reads as the A operand.  Every score of a half is
+      // loaded before its packed result is written over the first half of the S columns.
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {  // columns [64h, 64h+64) -> packed columns [32h, 32h+32)
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sr[2][32];
+        tmem_ld32(tS + h * 64, sr[0]);
+        tmem_ld32(tS + h * 64 + 32, sr[1]);
+        tmem_wait_ld();
+        reg_fence32(sr[0]);
+        reg_fence32(sr[1]);
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int c = 2 * h + (i >> 4), e = (i & 15) * 2;
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), c_log2, -ms));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), c_log2, -ms));
+          const int col = h * 64 + 2 * i;
+          const float s0 = col < lim ? __uint_as_float(sr[i >> 4][(2 * i) & 31]) : -INFINITY;
+          const float s1 = col + 1 < lim ? __uint_as_float(sr[i >> 4][(2 * i + 1) & 31]) : -INFINITY;
+          const float p0 = ex2_approx(fmaf(s0, c_log2, -ms));
+          const float p1 = ex2_approx(fmaf(s1, c_log2, -ms));
           l += p0 + p1;
           pk[i] = pack2<BF16>(p0, p1);
         }

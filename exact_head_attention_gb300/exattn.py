@@ -27,7 +27,14 @@ _lib = None
 class AttnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
+        detail = last_error()
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({status_string(status)})"
+                         + (f": {detail}" if detail else ""))
+
+
+def last_error() -> str:
+    """The library's description of its most recent failure on this thread ("" if none)."""
+    return load().attn_last_error().decode()
 
 
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -49,6 +56,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_check_device_error.argtypes = [vp]
             lib.attn_check_device_error.restype = i
+            lib.attn_last_error.argtypes = []
+            lib.attn_last_error.restype = ctypes.c_char_p
             _lib = lib
     return _lib
 

@@ -98,6 +98,13 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
 const char* attn_status_string(attn_status status);
 
 /*
+ * Describes, on the calling host thread, the most recent failure inside this
+ * library (which CUDA call failed and its error string); "" if none.  The
+ * pointer stays valid until the thread's next call into the library.
+ */
+const char* attn_last_error(void);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns ATTN_ERR_TIMEOUT if a kernel's bounded wait expired since the
  * last check, ATTN_ERR_CUDA if synchronisation failed, else ATTN_OK.
