@@ -1,0 +1,377 @@
+#!/usr/bin/env python3
+"""Throughput benchmark: exact fused attention, forward + backward, on GB300.
+
+One step = attn_fwd, then the backward's three C-ABI steps (attn_bwd_preprocess,
+attn_bwd_kv_blocks, attn_bwd_dq_convert -- together exactly attn_bwd) over one
+batch of the synthetic workload.  The default workload is the long-sequence,
+small-batch attention layer: B=1, H=12, Nq=Nk=8192, d=128, bf16, causal.
+
+FLOPs per step follow the metric's convention: forward 4*B*H*Nq*Nk*d, backward
+2.5x that, both halved when causal.
+
+Timing: W untimed warm-up steps, then K timed steps; between timed steps a
+256 MiB buffer is written (L2 flush) outside the timed events; every launch is
+bracketed by CUDA events on the launching stream; ms_per_step is the mean of
+the per-step device times, max over ranks.  With N > 1 (torchrun) every rank
+runs an independent replica of the workload (no collective on the data path).
+
+--impl reference times the CPU oracle (the plain fp64 definition) on the host
+cores instead, on bounded samples of the same workload.
+
+Prints ONE JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd+bwd TFLOPS (causal-adjusted) and % of GB300 BF16 tensor peak"
+FALLBACK_BF16_TFLOPS = 1900.0
+FLUSH_BYTES = 256 << 20
+
+
+def step_flops(w) -> tuple[float, float]:
+    f = 4.0 * w.B * w.H * w.Nq * w.Nk * w.d
+    if w.causal:
+        f /= 2
+    return f, 2.5 * f
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {"bf16_tflops": float(d["bf16_tflops"]), "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+                "source": "fallback"}
+
+
+def config_dict(w, extra=None) -> dict:
+    c = {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
+         "dtype": w.dtype, "sigma_qk": w.sigma_qk, "flops_per_step": sum(step_flops(w))}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) of SM clocks and throttle reasons for one GPU."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if uuid:
+            cmd.insert(1, f"--id={uuid}")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+
+    def summary(self, t0: float, t1: float) -> dict | None:
+        if self.proc is None:
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts + frac, float(parts[1]), float(parts[2]), parts[5:9]))
+            except Exception:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.25]
+        if not inside:  # timed region shorter than the sampling period: nearest samples
+            inside = sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:2]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ------------------------------------------------------------------ oracle timing
+
+def _oracle_step(x, w, n: int) -> float:
+    """The oracle's forward + backward on head (0, 0) restricted to the first n queries and keys."""
+    import oracle
+    q = x["q"][:1, :1, :n]
+    k = x["k"][:1, :1, :n]
+    v = x["v"][:1, :1, :n]
+    do = x["do"][:1, :1, :n]
+    t = time.perf_counter()
+    oracle.attn_fwd(q, k, v, w.causal, w.scale)
+    oracle.attn_bwd(q, k, v, do, w.causal, w.scale)
+    return time.perf_counter() - t
+
+
+def _sample_flops(w, n: int) -> float:
+    f = 4.0 * n * n * w.d * (0.5 if w.causal else 1.0)
+    return 3.5 * f
+
+
+def _pick_n(x, w, budget_s: float) -> int:
+    import oracle
+    oracle.build()
+    n0 = min(256, w.Nq, w.Nk)
+    t0 = max(_oracle_step(x, w, n0), 1e-4)
+    n = int(n0 * math.sqrt(budget_s / t0))
+    n = max(64, min(n, w.Nq, w.Nk))
+    return n - n % 64 if n >= 128 else n
+
+
+def cpu_baseline(x, w, budget_s: float = 15.0) -> dict:
+    n = _pick_n(x, w, budget_s)
+    dt = _oracle_step(x, w, n)
+    return {"value": _sample_flops(w, n) / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"fp64 oracle forward+backward of head (b=0,h=0), first {n} queries and keys, "
+                      f"{'causal' if w.causal else 'non-causal'}, d={w.d}; {dt:.1f} s on 1 thread "
+                      f"(host has {len(os.sched_getaffinity(0))} cores available)",
+            "seconds": dt}
+
+
+def run_reference(args, w) -> None:
+    from exact_head_attention_gb300 import workloads
+    x = workloads.make_inputs(w)
+    budget = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    n = _pick_n(x, w, budget)
+    for _ in range(args.warmup):
+        _oracle_step(x, w, n)
+    times = [_oracle_step(x, w, n) for _ in range(args.steps)]
+    mean = statistics.mean(times)
+    value = _sample_flops(w, n) / mean / 1e12
+    sample = (f"per step: fp64 oracle forward+backward of head (b=0,h=0), first {n} queries and keys "
+              f"(of {w.Nq}), 1 thread")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w, {"sample_n": n}),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------ main
+
+def traffic_from_profile(kernel_key: str) -> float | None:
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        d = json.load(open(path))[kernel_key]
+    except Exception:
+        return None
+    if d.get("source_sha") != kernel_source_sha():
+        return None
+    return float(d["dram_bytes_per_launch"])
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("attn_fwd.cu", "attn_bwd.cu", "ptx.cuh", "kernels.h"):
+        h.update(open(os.path.join(ROOT, "exact_head_attention_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from exact_head_attention_gb300 import workloads
+    w = workloads.WORKLOADS[args.workload or workloads.HEADLINE]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w)
+        return
+
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    from exact_head_attention_gb300 import build as _build
+    from exact_head_attention_gb300 import exattn
+    _build.build()
+    exattn.load()
+
+    x = workloads.make_inputs(w)
+    cpu = cpu_baseline(x, w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+
+    stream = torch.cuda.current_stream()
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(exattn.workspace_size(w.B, w.H, w.Nq, w.d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def launch(ev=None):
+        st = [exattn.fwd_raw(q, k, v, o, lse, w.causal, w.scale)]
+        if ev:
+            ev[1].record(stream)
+        for i, name in enumerate(exattn.BWD_STEPS):
+            st.append(exattn.bwd_raw(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, ws, step=name))
+            if ev:
+                ev[2 + i].record(stream)
+        if any(st):
+            raise RuntimeError(f"C-ABI status {st}: {exattn.last_error()}")
+
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    if exattn.check_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    props = torch.cuda.get_device_properties(dev)
+    sampler = ClockSampler(getattr(props, "uuid", None) and f"GPU-{props.uuid}")
+    for _ in range(args.warmup):  # keep the GPU loaded while the sampler starts
+        launch()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record(stream)
+        launch(evs[i])
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    if exattn.check_device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+    per = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)] for i in range(args.steps)]
+    step_ms = [sum(p) for p in per]
+    ms_per_step = statistics.mean(step_ms)
+    kern_ms = {name: statistics.mean(p[j] for p in per)
+               for j, name in enumerate(("fwd", "bwd_preprocess", "bwd_kv_blocks", "bwd_dq_convert"))}
+    if dist:
+        t = torch.tensor([ms_per_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+
+    # end to end through the C ABI: pinned host inputs -> device -> fwd + bwd -> host outputs
+    hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "do"))
+    ho, hdq, hdk, hdv = (torch.empty_like(t, device="cpu").pin_memory() for t in (q, q, k, v))
+    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        s1 = exattn.fwd_raw(q, k, v, o, lse, w.causal, w.scale)
+        s2 = exattn.bwd_raw(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, ws)
+        for hd, dd in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+            hd.copy_(dd, non_blocking=True)
+        if s1 or s2:
+            raise RuntimeError(exattn.last_error())
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ms = []
+    for i in range(args.e2e_steps):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e_ms.append(a.elapsed_time(b))
+    sampler.stop()
+    e2e_ms = statistics.mean(e_ms) if e_ms else float("nan")
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    fwd_f, bwd_f = step_flops(w)
+    flops = fwd_f + bwd_f
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    pk = peaks()
+    dominant = "bwd_kv_blocks"
+    achieved = bwd_f / (kern_ms[dominant] * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "fp16",
+        "data": "synthetic: seeded normal Q,K (sigma %.2g), V, dO (sigma 1)" % w.sigma_qk,
+        "config": config_dict(w, {"parallelism": "replicas" if world > 1 else "single GPU",
+                                  "l2": "256 MiB flush write between timed steps, outside the CUDA events"}),
+        "pct_of_peak": 100.0 * (flops / (ms_per_step * 1e-3) / 1e12) / pk["bf16_tflops"],
+        "peak_tflops": pk["bf16_tflops"], "peak_source": pk["source"],
+        "kernels_ms": kern_ms,
+        "fwd_tflops": fwd_f / (kern_ms["fwd"] * 1e-3) / 1e12,
+        "bwd_tflops": bwd_f / (sum(kern_ms[n] for n in ("bwd_preprocess", "bwd_kv_blocks", "bwd_dq_convert")) * 1e-3) / 1e12,
+        "roofline": {"kernel": "bwd_main_kernel (attn_bwd_kv_blocks)", "bound": "tensor", "achieved": achieved,
+                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                     "traffic": traffic_from_profile(f"{dominant}:{w.name}"),
+                     "peak_kind": f"bf16 dense burst ({pk['source']})"},
+        "cpu_baseline": ({k_: v_ for k_, v_ in cpu.items() if k_ != "seconds"} if cpu else None),
+        "e2e": ({"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms} if e_ms else None),
+        "gpu_launches": 4 * args.steps,
+        "clocks": sampler.summary(t_wall0, t_wall1),
+        "wall_s_timed_region": t_wall1 - t_wall0,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -177,10 +177,11 @@ extern "C" size_t attn_bwd_workspace_size(int B, int H, int Nq, int d) {
   return align256(rows * d * sizeof(float)) + 2 * align256(rows * sizeof(float));
 }
 
-extern "C" attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                                const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk, int d,
-                                int causal, float scale, attn_dtype dtype, void* workspace, size_t workspace_bytes,
-                                void* stream) {
+namespace {
+
+attn_status bwd_steps(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                      void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                      attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream, int steps) {
   attn_status st = check_common(B, H, Nq, Nk, d, scale, dtype);
   if (st != ATTN_OK) return st;
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
@@ -220,7 +221,41 @@ extern "C" attn_status attn_bwd(const void* Q, const void* K, const void* V, con
   a.scale = scale;
   a.timeout_ns = wait_timeout_ns();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return finish(launch_bwd(a, s), s);
+  return finish(launch_bwd(a, steps, s), s);
+}
+
+}  // namespace
+
+extern "C" attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                                const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk, int d,
+                                int causal, float scale, attn_dtype dtype, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  return bwd_steps(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
+                   workspace_bytes, stream, kBwdAll);
+}
+
+extern "C" attn_status attn_bwd_preprocess(const void* Q, const void* K, const void* V, const void* O,
+                                           const void* dO, const float* LSE, void* dQ, void* dK, void* dV, int B,
+                                           int H, int Nq, int Nk, int d, int causal, float scale, attn_dtype dtype,
+                                           void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_steps(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
+                   workspace_bytes, stream, kBwdPre);
+}
+
+extern "C" attn_status attn_bwd_kv_blocks(const void* Q, const void* K, const void* V, const void* O,
+                                          const void* dO, const float* LSE, void* dQ, void* dK, void* dV, int B,
+                                          int H, int Nq, int Nk, int d, int causal, float scale, attn_dtype dtype,
+                                          void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_steps(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
+                   workspace_bytes, stream, kBwdMain);
+}
+
+extern "C" attn_status attn_bwd_dq_convert(const void* Q, const void* K, const void* V, const void* O,
+                                           const void* dO, const float* LSE, void* dQ, void* dK, void* dV, int B,
+                                           int H, int Nq, int Nk, int d, int causal, float scale, attn_dtype dtype,
+                                           void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_steps(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
+                   workspace_bytes, stream, kBwdConvert);
 }
 
 extern "C" const char* attn_status_string(attn_status status) {
@@ -250,6 +285,10 @@ extern "C" attn_status attn_check_device_error(void* stream) {
     const uint32_t zero = 0;
     if ((e = cudaMemcpy(ds->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess)
       return cuda_fail("cudaMemcpy(error word)", e);
+    if (code == 8) {
+      std::snprintf(g_last_error, sizeof(g_last_error), "device error word 8: dynamic shared memory not 1024-byte aligned");
+      return ATTN_ERR_CUDA;
+    }
     std::snprintf(g_last_error, sizeof(g_last_error), "device error word %u (a bounded wait expired)", code);
     return ATTN_ERR_TIMEOUT;
   }

@@ -52,13 +52,19 @@ struct BwdCfg {
   static constexpr uint32_t OFF_P = OFF_V + TILE;
   static constexpr uint32_t OFF_DS = OFF_P + PT;
   static constexpr uint32_t OFF_RING = OFF_DS + PT;
-  static constexpr uint32_t OFF_BAR = OFF_RING + NR * TILE;
+  // two slots of the query tile's row vectors: 128 base-2 LSE then 128 D values (fp32)
+  static constexpr uint32_t OFF_ROWV = OFF_RING + NR * TILE;
+  static constexpr uint32_t ROWV_BYTES = 2 * 128 * 4;
+  static constexpr uint32_t OFF_BAR = OFF_ROWV + 2 * ROWV_BYTES;
   // kv_full, ring_full[NR], ring_empty[NR], s_full, s_used, dp_full, ds_ready, p_empty, ds_empty,
-  // dq_full, dq_empty, done, mma_done
-  static constexpr int NBAR = 1 + 2 * NR + 10;
+  // dq_full, dq_empty, done, mma_done, rowv_full[2], rowv_empty[2]
+  static constexpr int NBAR = 1 + 2 * NR + 14;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16;
-  static constexpr uint32_t SMEM_ALLOC = BYTES + 1024;
+  // The operand tiles need 1024-byte alignment; the dynamic shared memory base is checked at entry
+  // instead of padding (the d = 128 layout leaves no room for 1 KB of slack).
+  static constexpr uint32_t SMEM_ALLOC = BYTES;
+  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
 
 struct BwdBars {
@@ -78,6 +84,8 @@ struct BwdBars {
   __device__ uint32_t dq_empty() const { return at(7); }
   __device__ uint32_t done() const { return at(8); }
   __device__ uint32_t mma_done() const { return at(9); }
+  __device__ uint32_t rowv_full(int s) const { return at(10 + s); }
+  __device__ uint32_t rowv_empty(int s) const { return at(12 + s); }
 };
 
 template <int D, bool CAUSAL, bool BF16>
@@ -85,11 +93,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   using C = BwdCfg<D>;
   constexpr int NR = C::NR;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sbase = (raw + 1023u) & ~1023u;
-  uint8_t* gbase = smem_raw + (sbase - raw);
+  const uint32_t sbase = smem_u32(smem_raw);
+  if (!smem_base_aligned(sbase, a.err_word)) return;
+  uint8_t* gbase = smem_raw;
   const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sP = sbase + C::OFF_P, sDS = sbase + C::OFF_DS;
   const uint32_t sRing = sbase + C::OFF_RING;
+  const uint32_t sRowv = sbase + C::OFF_ROWV;
   const BwdBars bars{sbase + C::OFF_BAR, NR};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_MISC + 4);
@@ -120,6 +129,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     mbar_init(bars.dq_empty(), 256);
     mbar_init(bars.done(), 1);
     mbar_init(bars.mma_done(), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bars.rowv_full(s), 1);
+      mbar_init(bars.rowv_empty(s), 256);
+    }
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -142,9 +155,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         tma_load_3d(sK + c * kChunkBytes, &a.tm_k, c * 64, k0, bh, bars.kv_full());
         tma_load_3d(sV + c * kChunkBytes, &a.tm_v, c * 64, k0, bh, bars.kv_full());
       }
-      int issued = 0;
+      int issued = 0, issued_rowv = 0;
       for (int L = 0; L < 2 * n; ++L) {
         const int s = L % NR;
+        if ((L & 1) == 0) {
+          // LSE2 and D of query tile it = L/2 into row-vector slot it % 2
+          const int it = L >> 1, rs = it & 1;
+          if (!mbar_wait(bars.rowv_empty(rs), ((it >> 1) & 1) ^ 1, wc)) break;
+          mbar_arrive_expect_tx(bars.rowv_full(rs), C::ROWV_BYTES);
+          const size_t off = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows;
+          bulk_load(sRowv + rs * C::ROWV_BYTES, a.lse2 + off, 512, bars.rowv_full(rs));
+          bulk_load(sRowv + rs * C::ROWV_BYTES + 512, a.dsum + off, 512, bars.rowv_full(rs));
+          ++issued_rowv;
+        }
         if (!mbar_wait(bars.ring_empty(s), ((L / NR) & 1) ^ 1, wc)) break;
         mbar_arrive_expect_tx(bars.ring_full(s), C::TILE);
         const CUtensorMap* map = (L & 1) ? &a.tm_do : &a.tm_q;
@@ -155,6 +178,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       }
       if (*abort_flag) {
         for (int L = max(0, issued - NR); L < issued; ++L) mbar_drain(bars.ring_full(L % NR), (L / NR) & 1, a.timeout_ns);
+        for (int it = max(0, issued_rowv - 2); it < issued_rowv; ++it)
+          mbar_drain(bars.rowv_full(it & 1), (it >> 1) & 1, a.timeout_ns);
         mbar_drain(bars.kv_full(), 0, a.timeout_ns);
       }
     }
@@ -164,6 +189,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       constexpr uint32_t idS = idesc_f16(128, 128, BF16, false, false);   // K-major x K-major
       constexpr uint32_t idG = idesc_f16(128, D, BF16, false, true);      // dV, dK: A K-major, B MN-major
       constexpr uint32_t idQ = idesc_f16(128, D, BF16, true, true);       // dQ: A = dS MN-major, B = K MN-major
+      constexpr uint32_t idQT = idesc_f16(D, 128, BF16, true, true);      // dQ^T: A = K^T MN-major, B = dS^T MN-major
       auto slot_of = [](int L) { return L % NR; };
       auto phase_of = [](int L) { return static_cast<uint32_t>((L / NR) & 1); };
 
@@ -223,13 +249,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         }
         mma_commit(bars.p_empty());
         mma_commit(bars.ring_empty(slot_of(2 * it + 1)));
-        // dQ_i = dS K  (A: dS [query][key] read MN-major from the dS^T tile; B: K [key][d] MN-major)
         if (it > 0 && !(ok = mbar_wait(bars.dq_empty(), (it - 1) & 1, wc))) break;
         tc_fence_after();
+        if constexpr (D == 128) {
+          // dQ_i^T = K^T dS^T  (A: K^T [d][key] read MN-major from the K tile; B: dS^T [query][key] read
+          // MN-major from the dS^T tile).  TMEM lane = d, so each warp's reduction covers whole rows.
 #pragma unroll
-        for (int k = 0; k < 128 / 16; ++k)
-          mma_ss(tY, sdesc_sw128(sDS + k * 2048, kChunkBytes, 1024), sdesc_sw128(sK + k * 2048, kChunkBytes, 1024),
-                 idQ, k > 0);
+          for (int k = 0; k < 128 / 16; ++k)
+            mma_ss(tY, sdesc_sw128(sK + k * 2048, kChunkBytes, 1024), sdesc_sw128(sDS + k * 2048, kChunkBytes, 1024),
+                   idQT, k > 0);
+        } else {
+          // dQ_i = dS K  (A: dS [query][key] read MN-major from the dS^T tile; B: K [key][d] MN-major)
+#pragma unroll
+          for (int k = 0; k < 128 / 16; ++k)
+            mma_ss(tY, sdesc_sw128(sDS + k * 2048, kChunkBytes, 1024), sdesc_sw128(sK + k * 2048, kChunkBytes, 1024),
+                   idQ, k > 0);
+        }
         mma_commit(bars.dq_full());
         mma_commit(bars.ds_empty());
         if (it + 1 < n && !(ok = issue_dP(it + 1))) break;
@@ -255,6 +290,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     auto drain_dq = [&](int it) -> bool {
       if (!mbar_wait_warp(bars.dq_full(), it & 1, wc)) return false;
       tc_fence_after();
+      if constexpr (D == 128) {
+        // dQ_i^T: lane = d, column = query row.  This warpgroup reduces query rows [64h, 64h + 64); for
+        // each row a warp's 32 scalar reductions cover 32 consecutive floats (one 128-byte line).
+        uint32_t v[2][32];
+        tmem_ld32(tY + lane_bits + h * 64, v[0]);
+        tmem_ld32(tY + lane_bits + h * 64 + 32, v[1]);
+        tmem_wait_ld();
+        reg_fence32(v[0]);
+        reg_fence32(v[1]);
+        tc_fence_before();
+        mbar_arrive(bars.dq_empty());
+        const size_t row0 = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows + h * 64;
+        float* dst = a.dq_acc + row0 * D + r;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) red_add_f32(dst + static_cast<size_t>(c) * D, __uint_as_float(v[c >> 5][c & 31]));
+        return true;
+      }
       uint32_t v[D / 64][32];
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) tmem_ld32(tY + lane_bits + h * (D / 2) + c * 32, v[c]);
@@ -274,10 +326,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       return true;
     };
 
+    const bool ragged_kv = k0 + kTileRows > a.Nk;  // block-uniform
     for (int it = 0; it < n; ++it) {
       const int qb = (i_start + it) * kTileRows + h * 64;  // first query column of this half
-      const float* lse2 = a.lse2 + static_cast<size_t>(bh) * a.Nq_pad + qb;
-      const float* dsum = a.dsum + static_cast<size_t>(bh) * a.Nq_pad + qb;
+      const int rs = it & 1;                                // row-vector slot of this query tile
+      const float* rowv = reinterpret_cast<const float*>(gbase + C::OFF_ROWV + rs * C::ROWV_BYTES);
+      const float* lse2 = rowv + h * 64;
+      const float* dsum = rowv + 128 + h * 64;
       if (!(ok = mbar_wait_warp(bars.s_full(), it & 1, wc))) break;
       tc_fence_after();
       uint32_t s[2][32];
@@ -288,21 +343,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       reg_fence32(s[1]);
       tc_fence_before();
       mbar_arrive(bars.s_used());
+      if (!(ok = mbar_wait_warp(bars.rowv_full(rs), (it >> 1) & 1, wc))) break;
 
-      // P^T = exp2(S^T * scale*log2e - LSE2); masked entries are exactly 0.
+      // P^T = exp2(S^T * scale*log2e - LSE2); masked entries are exactly 0.  Only the causal
+      // diagonal tile and a ragged last key block need the mask: columns below `lo` are zeroed.
       const bool diag = CAUSAL && (i_start + it == jb);
       float p[64];
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
-        const float4 l4 = __ldg(reinterpret_cast<const float4*>(lse2 + c));
+        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
         const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int col = c + e;
-          float x = ex2_approx(fmaf(__uint_as_float(s[col >> 5][col & 31]), c_log2, -lv[e]));
-          if (!kv_valid || (diag && qb + col < kv)) x = 0.f;
-          p[col] = x;
+          p[col] = ex2_approx(fmaf(__uint_as_float(s[col >> 5][col & 31]), c_log2, -lv[e]));
         }
+      }
+      if (diag || ragged_kv) {
+        const int lo = !kv_valid ? 64 : (diag ? kv - qb : 0);
+#pragma unroll
+        for (int col = 0; col < 64; ++col)
+          if (col < lo) p[col] = 0.f;
       }
       uint32_t pk[32];
 #pragma unroll
@@ -325,7 +386,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       // dS^T = P^T o (dP^T - D)
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
-        const float4 d4 = __ldg(reinterpret_cast<const float4*>(dsum + c));
+        const float4 d4 = *reinterpret_cast<const float4*>(dsum + c);
         const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -333,6 +394,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
           p[col] = p[col] * (__uint_as_float(s[col >> 5][col & 31]) - dv[e]);
         }
       }
+      mbar_arrive(bars.rowv_empty(rs));
 #pragma unroll
       for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(p[2 * i], p[2 * i + 1]);
       if (it > 0 && !(ok = mbar_wait_warp(bars.ds_empty(), (it - 1) & 1, wc))) break;
@@ -457,17 +519,18 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const __grid_consta
   *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + e) = out;
 }
 
+// steps: bit 0 = preprocess, bit 1 = main, bit 2 = dQ conversion (launched in that order).
 template <int D, bool CAUSAL, bool BF16>
-cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_bwd_t(const BwdArgs& a, int steps, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  {
+  if (steps & kBwdPre) {
     constexpr int RPB = 256 / (D / 8);
     const size_t rows = static_cast<size_t>(a.bh_count) * a.Nq_pad;
     bwd_pre_kernel<D, BF16><<<static_cast<unsigned>((rows + RPB - 1) / RPB), 256, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  {
+  if (steps & kBwdMain) {
     auto kern = bwd_main_kernel<D, CAUSAL, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
@@ -476,22 +539,25 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  {
+  if (steps & kBwdConvert) {
     const size_t total = static_cast<size_t>(a.bh_count) * a.Nq * D / 8;
     bwd_dq_convert_kernel<D, BF16><<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(a);
     return cudaGetLastError();
   }
+  return cudaSuccess;
 }
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_bwd(const BwdArgs& a, int steps, cudaStream_t stream) {
   if (a.d == 64) {
-    if (a.causal) return a.bf16 ? launch_bwd_t<64, true, true>(a, stream) : launch_bwd_t<64, true, false>(a, stream);
-    return a.bf16 ? launch_bwd_t<64, false, true>(a, stream) : launch_bwd_t<64, false, false>(a, stream);
+    if (a.causal)
+      return a.bf16 ? launch_bwd_t<64, true, true>(a, steps, stream) : launch_bwd_t<64, true, false>(a, steps, stream);
+    return a.bf16 ? launch_bwd_t<64, false, true>(a, steps, stream) : launch_bwd_t<64, false, false>(a, steps, stream);
   }
-  if (a.causal) return a.bf16 ? launch_bwd_t<128, true, true>(a, stream) : launch_bwd_t<128, true, false>(a, stream);
-  return a.bf16 ? launch_bwd_t<128, false, true>(a, stream) : launch_bwd_t<128, false, false>(a, stream);
+  if (a.causal)
+    return a.bf16 ? launch_bwd_t<128, true, true>(a, steps, stream) : launch_bwd_t<128, true, false>(a, steps, stream);
+  return a.bf16 ? launch_bwd_t<128, false, true>(a, steps, stream) : launch_bwd_t<128, false, false>(a, steps, stream);
 }
 
 }  // namespace exattn

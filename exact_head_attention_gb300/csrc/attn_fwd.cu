@@ -67,6 +67,72 @@ struct FwdBars {
   __device__ uint32_t mma_done() const { return base + 8 * (7 + 4 * ns); }
 };
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Max of this thread's 128 scores in TMEM (read 64 columns at a time); with MASKED, columns at or
+// past `lim` are ignored.
+template <bool MASKED>
+__device__ __forceinline__ float tile_row_max(uint32_t tS, int lim) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    uint32_t sr[2][32];
+    tmem_ld32(tS + hh * 64, sr[0]);
+    tmem_ld32(tS + hh * 64 + 32, sr[1]);
+    tmem_wait_ld();
+    reg_fence32(sr[0]);
+    reg_fence32(sr[1]);
+#pragma unroll
+    for (int i = 0; i < 64; i += 2) {
+      float a = __uint_as_float(sr[i >> 5][i & 31]), b = __uint_as_float(sr[i >> 5][(i + 1) & 31]);
+      if constexpr (MASKED) {
+        if (hh * 64 + i >= lim) a = -INFINITY;
+        if (hh * 64 + i + 1 >= lim) b = -INFINITY;
+      }
+      mx = max3(mx, a, b);
+    }
+  }
+  return mx;
+}
+
+// P = exp2(s * c_log2 - ms) for this thread's 128 scores, packed into 16-bit pairs: scores
+// [64h, 64h + 64) become packed columns [32h, 32h + 32), the A operand of the P V MMA.  Every
+// score of a half is loaded before its packed result overwrites the first half of the S columns.
+// Returns the sum of the (fp32) probabilities.
+template <bool MASKED, bool BF16>
+__device__ __forceinline__ float tile_exp_pack(uint32_t tS, int lim, float c_log2, float ms) {
+  float l = 0.f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t sr[2][32];
+    tmem_ld32(tS + h * 64, sr[0]);
+    tmem_ld32(tS + h * 64 + 32, sr[1]);
+    tmem_wait_ld();
+    reg_fence32(sr[0]);
+    reg_fence32(sr[1]);
+    uint32_t pk[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float s0 = __uint_as_float(sr[i >> 4][(2 * i) & 31]);
+      float s1 = __uint_as_float(sr[i >> 4][(2 * i + 1) & 31]);
+      if constexpr (MASKED) {
+        if (h * 64 + 2 * i >= lim) s0 = -INFINITY;
+        if (h * 64 + 2 * i + 1 >= lim) s1 = -INFINITY;
+      }
+      const float p0 = ex2_approx(fmaf(s0, c_log2, -ms));
+      const float p1 = ex2_approx(fmaf(s1, c_log2, -ms));
+      l += p0 + p1;
+      pk[i] = pack2<BF16>(p0, p1);
+    }
+    tmem_st32(tS + h * 32, pk);
+  }
+  return l;
+}
+
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdArgs a) {
   using C = FwdCfg<D>;
@@ -224,22 +290,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       // Columns at or past `lim` are masked (ragged last key tile, causal diagonal tile).
       const bool need_mask = ((j + 1) * kTileRows > a.Nk) || (CAUSAL && j * kTileRows + kTileRows - 1 > q0 + t * kTileRows);
       const int lim = need_mask ? (CAUSAL ? min(a.Nk, row + 1) : a.Nk) - j * kTileRows : kTileRows;
-      // Pass 1: row max over the 128 scores (read from TMEM 64 columns at a time).
-      float mx = -INFINITY;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t sr[2][32];
-        tmem_ld32(tS + hh * 64, sr[0]);
-        tmem_ld32(tS + hh * 64 + 32, sr[1]);
-        tmem_wait_ld();
-        reg_fence32(sr[0]);
-        reg_fence32(sr[1]);
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (hh * 64 + c * 32 + i < lim) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
-      }
+      // Pass 1: row max over the 128 scores.
+      const float mx = need_mask ? tile_row_max<true>(tS, lim) : tile_row_max<false>(tS, lim);
       const float m_new = fmaxf(m, mx * c_log2);
       if (j == 0) {
         m = m_new;
@@ -264,30 +316,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         }
       }
       const float ms = (m == -INFINITY) ? 0.f : m;
-      // Pass 2: P = exp2(s * scale*log2e - m), packed to 16-bit pairs; scores [64h, 64h+64) become
-      // packed columns [32h, 32h+32), which the MMA reads as the A operand.  Every score of a half is
-      // loaded before its packed result is written over the first half of the S columns.
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t sr[2][32];
-        tmem_ld32(tS + h * 64, sr[0]);
-        tmem_ld32(tS + h * 64 + 32, sr[1]);
-        tmem_wait_ld();
-        reg_fence32(sr[0]);
-        reg_fence32(sr[1]);
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int col = h * 64 + 2 * i;
-          const float s0 = col < lim ? __uint_as_float(sr[i >> 4][(2 * i) & 31]) : -INFINITY;
-          const float s1 = col + 1 < lim ? __uint_as_float(sr[i >> 4][(2 * i + 1) & 31]) : -INFINITY;
-          const float p0 = ex2_approx(fmaf(s0, c_log2, -ms));
-          const float p1 = ex2_approx(fmaf(s1, c_log2, -ms));
-          l += p0 + p1;
-          pk[i] = pack2<BF16>(p0, p1);
-        }
-        tmem_st32(tS + h * 32, pk);
-      }
+      // Pass 2: P = exp2(s * scale*log2e - m), written back into TMEM as the PV MMA's A operand.
+      l += need_mask ? tile_exp_pack<true, BF16>(tS, lim, c_log2, ms) : tile_exp_pack<false, BF16>(tS, lim, c_log2, ms);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bars.p_full(t));

@@ -38,8 +38,11 @@ struct BwdArgs {
   uint64_t timeout_ns;
 };
 
+// Backward steps (bit mask for launch_bwd).
+constexpr int kBwdPre = 1, kBwdMain = 2, kBwdConvert = 4, kBwdAll = 7;
+
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
-cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdArgs& a, int steps, cudaStream_t stream);
 
 }  // namespace exattn

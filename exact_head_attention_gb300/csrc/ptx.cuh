@@ -69,6 +69,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Error codes a kernel records in the device error word.
 enum : uint32_t { kErrNone = 0, kErrTimeout = 5, kErrSmemAlign = 8 };
 
+// Dynamic shared memory must start 1024-byte aligned for kernels that request
+// no alignment slack; checked once at kernel entry (uniform across the CTA).
+__device__ __forceinline__ bool smem_base_aligned(uint32_t raw, uint32_t* err_word) {
+  if ((raw & 1023u) == 0u) return true;
+  if (threadIdx.x == 0) atomicCAS(err_word, 0u, kErrSmemAlign);
+  return false;
+}
+
 // Shared state of one CTA's bounded waits.  `abort_flag` points into shared
 // memory; once any thread gives up, every other wait in the CTA returns false
 // at its next check so that all roles reach the teardown.
@@ -126,6 +134,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
+}
+
+// Contiguous global -> shared copy (both 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
 }
 
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
@@ -305,6 +320,10 @@ __device__ __forceinline__ float unpack_hi(uint32_t v) {
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ void red_add_f32(float* gaddr, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gaddr), "f"(a) : "memory");
 }
 
 __device__ __forceinline__ void red_add_v4(float* gaddr, float a, float b, float c, float d) {

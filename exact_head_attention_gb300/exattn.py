@@ -19,6 +19,8 @@ ATTN_OK = 0
 STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_MISALIGNED",
                 4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_TIMEOUT", 6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_NOT_IMPLEMENTED"}
 ATTN_BF16, ATTN_FP16 = 0, 1
+# attn_bwd is these three C-ABI calls in this order
+BWD_STEPS = ("attn_bwd_preprocess", "attn_bwd_kv_blocks", "attn_bwd_dq_convert")
 
 _lock = threading.Lock()
 _lib = None
@@ -50,8 +52,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_fwd.restype = i
             lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
             lib.attn_bwd_workspace_size.restype = sz
-            lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
-            lib.attn_bwd.restype = i
+            for name in ("attn_bwd",) + BWD_STEPS:
+                fn = getattr(lib, name)
+                fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
+                fn.restype = i
             lib.attn_status_string.argtypes = [i]
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_check_device_error.argtypes = [vp]
@@ -120,13 +124,15 @@ def workspace_size(B: int, H: int, Nq: int, d: int) -> int:
     return int(load().attn_bwd_workspace_size(B, H, Nq, d))
 
 
-def bwd_raw(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, workspace, stream=None) -> int:
+def bwd_raw(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, workspace, stream=None,
+            step: str = "attn_bwd") -> int:
+    """Calls attn_bwd (or one of BWD_STEPS) on caller-provided tensors; returns the status code."""
     B, H, Nq, Nk, d = _dims(q, k)
     ws_ptr = None if workspace is None else ctypes.c_void_p(workspace.data_ptr())
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    return load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-                           B, H, Nq, Nk, d, int(bool(causal)), float(scale), _dtype_code(q), ws_ptr, ws_bytes,
-                           _stream(stream))
+    fn = getattr(load(), step)
+    return fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+              B, H, Nq, Nk, d, int(bool(causal)), float(scale), _dtype_code(q), ws_ptr, ws_bytes, _stream(stream))
 
 
 def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None, workspace=None, stream=None):

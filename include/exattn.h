@@ -94,6 +94,34 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
                      int B, int H, int Nq, int Nk, int d, int causal, float scale,
                      attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * The three steps attn_bwd launches, callable one at a time (same arguments
+ * and validation as attn_bwd; attn_bwd is exactly these three in this order on
+ * `stream`, sharing `workspace`):
+ *   attn_bwd_preprocess  D = rowsum(dO o O) and the base-2 LSE into the
+ *                        workspace; zeroes the workspace's fp32 dQ accumulator
+ *                        (SparkAttention Figure 9, the dPsum term).
+ *   attn_bwd_kv_blocks   the fused pass over key/value blocks: writes dK and
+ *                        dV and adds every block's dQ contribution into the
+ *                        accumulator ("Fast Transformer training with long
+ *                        sequences", backward parallelisation over columns).
+ *   attn_bwd_dq_convert  dQ = scale * accumulator, rounded to the dtype.
+ * Each step reads what the previous one left in `workspace`; calling them out
+ * of order gives undefined results (no fault).
+ */
+attn_status attn_bwd_preprocess(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                                const float* LSE, void* dQ, void* dK, void* dV,
+                                int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                                attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+attn_status attn_bwd_kv_blocks(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                               const float* LSE, void* dQ, void* dK, void* dV,
+                               int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                               attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+attn_status attn_bwd_dq_convert(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                                const float* LSE, void* dQ, void* dK, void* dV,
+                                int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                                attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Static description of a status code. */
 const char* attn_status_string(attn_status status);
 
