@@ -14,21 +14,28 @@
 //        dV_j += P^T dO_i,  dK_j += dS^T Q_i,  dQ_i += dS K_j
 //    (StreamKL summary, Methodology 2: P regenerated tile by tile from the
 //    stored LSE), accumulating dK_j, dV_j in TMEM and reducing dQ_i into the
-//    fp32 accumulator with vector atomics (SparkAttention: dQ is atomically
-//    added across thread blocks; StreamKL: atomics while the buffer fits in L2).
+//    fp32 accumulator with atomics (SparkAttention: dQ is atomically added
+//    across thread blocks; StreamKL: atomics while the buffer fits in L2).
 // 3. bwd_dq_convert_kernel: dQ = scale * dQacc rounded to the input dtype.
 //
 // Main-kernel warp roles (320 threads):
 //   warps 0-3   compute, query columns [0, 64) of each tile (thread = key row),
-//               and dQ columns [0, d/2) of the drain (TMEM dQ_i -> red.global.add.v4.f32)
-//   warps 4-7   compute, query columns [64, 128), dQ columns [d/2, d)
-//   warp  8     TMA producer: K_j, V_j once; Q_i, dO_i through an NR-slot ring
+//               and query rows [0, 64) of the dQ drain
+//   warps 4-7   compute, query columns [64, 128), dQ query rows [64, 128)
+//   warp  8     TMA producer: K_j, V_j once; Q_i, dO_i through an NR-slot ring,
+//               LSE2_i and D_i through a 2-slot ring
 //   warp  9     MMA issuer (one thread) and TMEM owner
-// Tensor memory: X = [0,128) holds S^T then dP^T of the current tile,
-// Y = [128, 128+d) holds dQ_i, dV at [256, 256+d), dK at [384, 384+d).
-// Shared memory: K_j, V_j, P^T and dS^T (128 x 128, 16-bit), and the Q/dO ring.
-// Per tile the MMA issue order is S_{i+1}, dK_i, dV_i, dQ_i, dP_{i+1}, so the
-// exponentials of tile i+1 overlap the three gradient MMAs of tile i.
+// Tensor memory (512 columns):
+//   X  = [0,128)    S^T_i, then dP^T_i; then each compute warpgroup h packs its
+//                   P^T half into [64h, 64h+32) and its dS^T half into
+//                   [64h+32, 64h+64) -- the A operands of the dV and dK MMAs
+//   Y  = [128,256)  dQ_i (d = 64: lane = query row) or dQ_i^T (d = 128: lane = d)
+//   dV = [256,256+d), dK = [384,384+d)
+// Shared memory: K_j, V_j, dS^T (the dQ MMA's operand), the Q/dO ring.
+// Per tile i the MMA issue order is dV_i, dK_i, S_{i+1}, dQ_i, dP_{i+1}: the
+// exponentials of tile i+1 overlap dQ_i and dP_{i+1}, and the dQ_i reduction
+// (issued by the compute warps after they hand over tile i+1) overlaps the
+// next tile's MMAs.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -45,24 +52,23 @@ template <int D>
 struct BwdCfg {
   static constexpr int NCH = D / 64;
   static constexpr uint32_t TILE = kTileRows * D * 2;
-  static constexpr uint32_t PT = 128 * 128 * 2;  // P^T / dS^T tile
+  static constexpr uint32_t PT = 128 * 128 * 2;  // dS^T tile
   static constexpr int NR = (D == 64) ? 6 : 3;   // Q/dO ring slots
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + TILE;
-  static constexpr uint32_t OFF_P = OFF_V + TILE;
-  static constexpr uint32_t OFF_DS = OFF_P + PT;
+  static constexpr uint32_t OFF_DS = OFF_V + TILE;
   static constexpr uint32_t OFF_RING = OFF_DS + PT;
   // two slots of the query tile's row vectors: 128 base-2 LSE then 128 D values (fp32)
   static constexpr uint32_t OFF_ROWV = OFF_RING + NR * TILE;
   static constexpr uint32_t ROWV_BYTES = 2 * 128 * 4;
   static constexpr uint32_t OFF_BAR = OFF_ROWV + 2 * ROWV_BYTES;
-  // kv_full, ring_full[NR], ring_empty[NR], s_full, s_used, dp_full, ds_ready, p_empty, ds_empty,
+  // kv_full, ring_full[NR], ring_empty[NR], s_full, s_used, dp_full, ds_ready, ds_empty,
   // dq_full, dq_empty, done, mma_done, rowv_full[2], rowv_empty[2]
-  static constexpr int NBAR = 1 + 2 * NR + 14;
+  static constexpr int NBAR = 1 + 2 * NR + 13;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   // The operand tiles need 1024-byte alignment; the dynamic shared memory base is checked at entry
-  // instead of padding (the d = 128 layout leaves no room for 1 KB of slack).
+  // instead of padding.
   static constexpr uint32_t SMEM_ALLOC = BYTES;
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
@@ -78,15 +84,18 @@ struct BwdBars {
   __device__ uint32_t s_used() const { return at(1); }
   __device__ uint32_t dp_full() const { return at(2); }
   __device__ uint32_t ds_ready() const { return at(3); }
-  __device__ uint32_t p_empty() const { return at(4); }
-  __device__ uint32_t ds_empty() const { return at(5); }
-  __device__ uint32_t dq_full() const { return at(6); }
-  __device__ uint32_t dq_empty() const { return at(7); }
-  __device__ uint32_t done() const { return at(8); }
-  __device__ uint32_t mma_done() const { return at(9); }
-  __device__ uint32_t rowv_full(int s) const { return at(10 + s); }
-  __device__ uint32_t rowv_empty(int s) const { return at(12 + s); }
+  __device__ uint32_t ds_empty() const { return at(4); }
+  __device__ uint32_t dq_full() const { return at(5); }
+  __device__ uint32_t dq_empty() const { return at(6); }
+  __device__ uint32_t done() const { return at(7); }
+  __device__ uint32_t mma_done() const { return at(8); }
+  __device__ uint32_t rowv_full(int s) const { return at(9 + s); }
+  __device__ uint32_t rowv_empty(int s) const { return at(11 + s); }
 };
+
+// TMEM column of K step k (16 query columns) of the packed P^T (off = 0) or dS^T (off = 32) operand:
+// query columns [0, 64) sit in [off, off + 32), query columns [64, 128) in [64 + off, 64 + off + 32).
+__device__ __forceinline__ uint32_t packed_col(int k, int off) { return (k < 4 ? k * 8 : 64 + (k - 4) * 8) + off; }
 
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
@@ -96,7 +105,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   const uint32_t sbase = smem_u32(smem_raw);
   if (!smem_base_aligned(sbase, a.err_word)) return;
   uint8_t* gbase = smem_raw;
-  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sP = sbase + C::OFF_P, sDS = sbase + C::OFF_DS;
+  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
   const uint32_t sRing = sbase + C::OFF_RING;
   const uint32_t sRowv = sbase + C::OFF_ROWV;
   const BwdBars bars{sbase + C::OFF_BAR, NR};
@@ -123,7 +132,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     mbar_init(bars.s_used(), 256);
     mbar_init(bars.dp_full(), 1);
     mbar_init(bars.ds_ready(), 256);
-    mbar_init(bars.p_empty(), 1);
     mbar_init(bars.ds_empty(), 1);
     mbar_init(bars.dq_full(), 1);
     mbar_init(bars.dq_empty(), 256);
@@ -187,7 +195,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n > 0) {
       constexpr uint32_t idS = idesc_f16(128, 128, BF16, false, false);   // K-major x K-major
-      constexpr uint32_t idG = idesc_f16(128, D, BF16, false, true);      // dV, dK: A K-major, B MN-major
+      constexpr uint32_t idG = idesc_f16(128, D, BF16, false, true);      // dV, dK: A (TMEM) K-major, B MN-major
       constexpr uint32_t idQ = idesc_f16(128, D, BF16, true, true);       // dQ: A = dS MN-major, B = K MN-major
       constexpr uint32_t idQT = idesc_f16(D, 128, BF16, true, true);      // dQ^T: A = K^T MN-major, B = dS^T MN-major
       auto slot_of = [](int L) { return L % NR; };
@@ -229,26 +237,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       for (int it = 0; ok && it < n; ++it) {
         if (!(ok = mbar_wait(bars.ds_ready(), it & 1, wc))) break;
         tc_fence_after();
-        if (it + 1 < n && !(ok = issue_S(it + 1))) break;
         const uint32_t sq = sRing + slot_of(2 * it) * C::TILE;
         const uint32_t sdo = sRing + slot_of(2 * it + 1) * C::TILE;
-        // dK += dS^T Q_i   (A: dS^T [key][query] K-major; B: Q_i [query][d] MN-major)
+        // dV += P^T dO_i   (A: P^T packed in TMEM X; B: dO_i [query][d] MN-major)
 #pragma unroll
-        for (int k = 0; k < 128 / 16; ++k) {
-          const uint32_t aoff = (k >> 2) * kChunkBytes + (k & 3) * 32;
-          mma_ss(tdK, sdesc_sw128(sDS + aoff, 16, 1024), sdesc_sw128(sq + k * 2048, kChunkBytes, 1024), idG,
-                 (it > 0 || k > 0));
-        }
-        mma_commit(bars.ring_empty(slot_of(2 * it)));
-        // dV += P^T dO_i
-#pragma unroll
-        for (int k = 0; k < 128 / 16; ++k) {
-          const uint32_t aoff = (k >> 2) * kChunkBytes + (k & 3) * 32;
-          mma_ss(tdV, sdesc_sw128(sP + aoff, 16, 1024), sdesc_sw128(sdo + k * 2048, kChunkBytes, 1024), idG,
-                 (it > 0 || k > 0));
-        }
-        mma_commit(bars.p_empty());
+        for (int k = 0; k < 128 / 16; ++k)
+          mma_ts(tdV, tX + packed_col(k, 0), sdesc_sw128(sdo + k * 2048, kChunkBytes, 1024), idG, (it > 0 || k > 0));
         mma_commit(bars.ring_empty(slot_of(2 * it + 1)));
+        // dK += dS^T Q_i   (A: dS^T packed in TMEM X; B: Q_i [query][d] MN-major)
+#pragma unroll
+        for (int k = 0; k < 128 / 16; ++k)
+          mma_ts(tdK, tX + packed_col(k, 32), sdesc_sw128(sq + k * 2048, kChunkBytes, 1024), idG, (it > 0 || k > 0));
+        mma_commit(bars.ring_empty(slot_of(2 * it)));
+        // S^T_{i+1} overwrites X after dV_i, dK_i have read it (MMAs of one thread run in order).
+        if (it + 1 < n && !(ok = issue_S(it + 1))) break;
         if (it > 0 && !(ok = mbar_wait(bars.dq_empty(), (it - 1) & 1, wc))) break;
         tc_fence_after();
         if constexpr (D == 128) {
@@ -275,18 +277,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     }
   } else {
     // ------------------------------------------------------------ compute
-    const int h = warp >> 2;             // query half: columns [64h, 64h + 64); dQ columns [h*d/2, (h+1)*d/2)
+    const int h = warp >> 2;             // query half: columns [64h, 64h + 64)
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;   // TMEM lane: key row of S^T/dP^T, query row of dQ_i
+    const int r = quarter * 32 + lane;   // TMEM lane: key row of S^T/dP^T; d (d = 128) or query row of dQ
     const int kv = k0 + r;
     const bool kv_valid = kv < a.Nk;
     const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
     const float c_log2 = a.scale * 1.4426950408889634f;
-    const uint32_t p_row = sP + h * kChunkBytes, ds_row = sDS + h * kChunkBytes;
+    const uint32_t ds_row = sDS + h * kChunkBytes;
     bool ok = true;
 
-    // dQ_i (TMEM Y, lane = query row) -> fp32 vector atomics into the accumulator; the TMEM
-    // columns are released as soon as they are in registers.
+    // dQ_i from TMEM Y -> fp32 reductions into the accumulator; Y is released as soon as the
+    // values are in registers.
     auto drain_dq = [&](int it) -> bool {
       if (!mbar_wait_warp(bars.dq_full(), it & 1, wc)) return false;
       tc_fence_after();
@@ -305,24 +307,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         float* dst = a.dq_acc + row0 * D + r;
 #pragma unroll
         for (int c = 0; c < 64; ++c) red_add_f32(dst + static_cast<size_t>(c) * D, __uint_as_float(v[c >> 5][c & 31]));
-        return true;
-      }
-      uint32_t v[D / 64][32];
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) tmem_ld32(tY + lane_bits + h * (D / 2) + c * 32, v[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) reg_fence32(v[c]);
-      tc_fence_before();
-      mbar_arrive(bars.dq_empty());
-      const size_t row = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows + r;
-      float* dst = a.dq_acc + row * D + h * (D / 2);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
+      } else {
+        // dQ_i: lane = query row; this warpgroup reduces d columns [32h, 32h + 32).
+        uint32_t v[32];
+        tmem_ld32(tY + lane_bits + h * 32, v);
+        tmem_wait_ld();
+        reg_fence32(v);
+        tc_fence_before();
+        mbar_arrive(bars.dq_empty());
+        const size_t row = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows + r;
+        float* dst = a.dq_acc + row * D + h * 32;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          red_add_v4(dst + c * 32 + u * 4, __uint_as_float(v[c][4 * u]), __uint_as_float(v[c][4 * u + 1]),
-                     __uint_as_float(v[c][4 * u + 2]), __uint_as_float(v[c][4 * u + 3]));
+          red_add_v4(dst + u * 4, __uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]), __uint_as_float(v[4 * u + 2]),
+                     __uint_as_float(v[4 * u + 3]));
+      }
       return true;
     };
 
@@ -365,16 +364,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         for (int col = 0; col < 64; ++col)
           if (col < lo) p[col] = 0.f;
       }
-      uint32_t pk[32];
+      // P^T rounded to 16 bits: the dV MMA's operand, and the P used in dS below (so that dV and dK
+      // see the same probabilities).
+      uint32_t pp[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(p[2 * i], p[2 * i + 1]);
-      if (it > 0 && !(ok = mbar_wait_warp(bars.p_empty(), (it - 1) & 1, wc))) break;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        st_shared_v4(p_row + sw128_offset(r, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-
-      // dQ of the previous tile is ready while this tile's dP^T is still being computed.
-      if (it > 0 && !(ok = drain_dq(it - 1))) break;
+      for (int i = 0; i < 32; ++i) pp[i] = pack2<BF16>(p[2 * i], p[2 * i + 1]);
 
       if (!(ok = mbar_wait_warp(bars.dp_full(), it & 1, wc))) break;
       tc_fence_after();
@@ -383,29 +377,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       tmem_wait_ld();
       reg_fence32(s[0]);
       reg_fence32(s[1]);
-      // dS^T = P^T o (dP^T - D)
+      // P^T into this half's first 32 columns of X: its dP^T values are in registers now.
+      tmem_st32(tX + lane_bits + h * 64, pp);
+      // dS^T = P^T o (dP^T - D), into the half's next 32 columns of X and into the shared dS^T tile.
+      uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
         const float4 d4 = *reinterpret_cast<const float4*>(dsum + c);
         const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+        float ds[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int col = c + e;
-          p[col] = p[col] * (__uint_as_float(s[col >> 5][col & 31]) - dv[e]);
+          const float pv = (col & 1) ? unpack_hi<BF16>(pp[col >> 1]) : unpack_lo<BF16>(pp[col >> 1]);
+          ds[e] = pv * (__uint_as_float(s[col >> 5][col & 31]) - dv[e]);
         }
+        pk[c >> 1] = pack2<BF16>(ds[0], ds[1]);
+        pk[(c >> 1) + 1] = pack2<BF16>(ds[2], ds[3]);
       }
       mbar_arrive(bars.rowv_empty(rs));
-#pragma unroll
-      for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(p[2 * i], p[2 * i + 1]);
+      tmem_st32(tX + lane_bits + h * 64 + 32, pk);
       if (it > 0 && !(ok = mbar_wait_warp(bars.ds_empty(), (it - 1) & 1, wc))) break;
 #pragma unroll
       for (int u = 0; u < 8; ++u)
         st_shared_v4(ds_row + sw128_offset(r, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bars.ds_ready());
-    }
 
+      // The previous tile's dQ has been ready since before this tile's dP^T.
+      if (it > 0 && !(ok = drain_dq(it - 1))) break;
+    }
     if (ok && n > 0) ok = drain_dq(n - 1);
 
     // ------------------------------------------------------------ epilogue
