@@ -53,7 +53,9 @@ struct BwdCfg {
   static constexpr int NCH = D / 64;
   static constexpr uint32_t TILE = kTileRows * D * 2;
   static constexpr uint32_t PT = 128 * 128 * 2;  // dS^T tile
-  static constexpr int NR = (D == 64) ? 6 : 3;   // Q/dO ring slots
+  // Q/dO ring slots: with 4, the loads of tile i+1 reuse the slots tile i-1 released, a whole
+  // tile ahead of their use.
+  static constexpr int NR = (D == 64) ? 6 : 4;
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + TILE;
   static constexpr uint32_t OFF_DS = OFF_V + TILE;
@@ -62,9 +64,9 @@ struct BwdCfg {
   static constexpr uint32_t OFF_ROWV = OFF_RING + NR * TILE;
   static constexpr uint32_t ROWV_BYTES = 2 * 128 * 4;
   static constexpr uint32_t OFF_BAR = OFF_ROWV + 2 * ROWV_BYTES;
-  // kv_full, ring_full[NR], ring_empty[NR], s_full, s_used, dp_full, ds_ready, ds_empty,
-  // dq_full, dq_empty, done, mma_done, rowv_full[2], rowv_empty[2]
-  static constexpr int NBAR = 1 + 2 * NR + 13;
+  // kv_full, ring_full[NR], ring_empty[NR], s_full, s_used, dp_full, pd_ready, ds_empty,
+  // dq_full, dq_empty, done, mma_done, rowv_full[2], rowv_empty[2], dss_ready
+  static constexpr int NBAR = 1 + 2 * NR + 14;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   // The operand tiles need 1024-byte alignment; the dynamic shared memory base is checked at entry
@@ -83,7 +85,8 @@ struct BwdBars {
   __device__ uint32_t s_full() const { return at(0); }
   __device__ uint32_t s_used() const { return at(1); }
   __device__ uint32_t dp_full() const { return at(2); }
-  __device__ uint32_t ds_ready() const { return at(3); }
+  __device__ uint32_t pd_ready() const { return at(3); }   // P^T, dS^T packed in TMEM X
+  __device__ uint32_t dss_ready() const { return at(13); } // dS^T in shared memory
   __device__ uint32_t ds_empty() const { return at(4); }
   __device__ uint32_t dq_full() const { return at(5); }
   __device__ uint32_t dq_empty() const { return at(6); }
@@ -131,7 +134,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     mbar_init(bars.s_full(), 1);
     mbar_init(bars.s_used(), 256);
     mbar_init(bars.dp_full(), 1);
-    mbar_init(bars.ds_ready(), 256);
+    mbar_init(bars.pd_ready(), 256);
+    mbar_init(bars.dss_ready(), 256);
     mbar_init(bars.ds_empty(), 1);
     mbar_init(bars.dq_full(), 1);
     mbar_init(bars.dq_empty(), 256);
@@ -235,7 +239,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       if (ok) ok = issue_S(0);
       if (ok) ok = issue_dP(0);
       for (int it = 0; ok && it < n; ++it) {
-        if (!(ok = mbar_wait(bars.ds_ready(), it & 1, wc))) break;
+        if (!(ok = mbar_wait(bars.pd_ready(), it & 1, wc))) break;
         tc_fence_after();
         const uint32_t sq = sRing + slot_of(2 * it) * C::TILE;
         const uint32_t sdo = sRing + slot_of(2 * it + 1) * C::TILE;
@@ -252,6 +256,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         // S^T_{i+1} overwrites X after dV_i, dK_i have read it (MMAs of one thread run in order).
         if (it + 1 < n && !(ok = issue_S(it + 1))) break;
         if (it > 0 && !(ok = mbar_wait(bars.dq_empty(), (it - 1) & 1, wc))) break;
+        if (!(ok = mbar_wait(bars.dss_ready(), it & 1, wc))) break;
         tc_fence_after();
         if constexpr (D == 128) {
           // dQ_i^T = K^T dS^T  (A: K^T [d][key] read MN-major from the K tile; B: dS^T [query][key] read
@@ -397,14 +402,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       }
       mbar_arrive(bars.rowv_empty(rs));
       tmem_st32(tX + lane_bits + h * 64 + 32, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bars.pd_ready());  // dV_i, dK_i and S_{i+1} may go
       if (it > 0 && !(ok = mbar_wait_warp(bars.ds_empty(), (it - 1) & 1, wc))) break;
 #pragma unroll
       for (int u = 0; u < 8; ++u)
         st_shared_v4(ds_row + sw128_offset(r, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       fence_proxy_async_smem();
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bars.ds_ready());
+      mbar_arrive(bars.dss_ready());  // dQ_i may go
 
       // The previous tile's dQ has been ready since before this tile's dP^T.
       if (it > 0 && !(ok = drain_dq(it - 1))) break;
