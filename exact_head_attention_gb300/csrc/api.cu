@@ -296,3 +296,5 @@ extern "C" attn_status attn_check_device_error(void* stream) {
 }
 
 extern "C" const char* attn_last_error(void) { return g_last_error; }
+
+void exattn::set_last_error(const char* msg) { std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }

@@ -41,6 +41,9 @@ struct BwdArgs {
 // Backward steps (bit mask for launch_bwd).
 constexpr int kBwdPre = 1, kBwdMain = 2, kBwdConvert = 4, kBwdAll = 7;
 
+// Sets the message attn_last_error returns on this host thread.
+void set_last_error(const char* msg);
+
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, int steps, cudaStream_t stream);

@@ -122,6 +122,34 @@ attn_status attn_bwd_dq_convert(const void* Q, const void* K, const void* V, con
                                 int B, int H, int Nq, int Nk, int d, int causal, float scale,
                                 attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Backward for callers that cannot allocate device memory -- for example a
+ * plugin inside an engine that owns all device memory and forbids allocation
+ * while it runs, or a latency-bound loop that cannot risk an allocator call
+ * (or its failure) on every step.  The paper has no counterpart: this is a
+ * deployment convenience of this library.
+ *
+ * Same arguments, layouts and results as attn_bwd, minus the workspace: the
+ * scratch comes from one fixed array of ATTN_BWD_NOALLOC_MAX_WORKSPACE_BYTES
+ * built into the library, which every GPU that loads the library reserves
+ * until the process exits.  Nothing is allocated by this call.
+ *   - Shapes whose attn_bwd_workspace_size exceeds the maximum are rejected
+ *     with ATTN_ERR_WORKSPACE (attn_last_error gives the sizes); nothing runs.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - All calls share the one array, which keeps the last call's contents;
+ *     each call clears what must start at zero.  Calls whose executions
+ *     overlap on the GPU (different streams, or different host threads on
+ *     the same device) race on the array and give wrong results: serialise
+ *     them.
+ */
+#define ATTN_BWD_NOALLOC_MAX_WORKSPACE_BYTES ((size_t)64 << 20)
+attn_status attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                             const float* LSE, void* dQ, void* dK, void* dV,
+                             int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                             attn_dtype dtype, void* stream);
+
 /* Static description of a status code. */
 const char* attn_status_string(attn_status status);
 
