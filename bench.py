@@ -186,6 +186,23 @@ def run_reference(args, w) -> None:
     }), flush=True)
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest `value` over all ranks (identity when not distributed)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own batch (weak scaling), timed by the slowest rank."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ main
 
 def traffic_from_profile(kernel_key: str) -> float | None:
@@ -243,7 +260,7 @@ def main() -> None:
     _build.build()
     exattn.load()
 
-    x = workloads.make_inputs(w)
+    x = workloads.make_inputs(w, seed_offset=10 * rank)  # each rank: its own batch (tensor seeds use +0..3)
     cpu = cpu_baseline(x, w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
 
     stream = torch.cuda.current_stream()
@@ -295,10 +312,7 @@ def main() -> None:
     ms_per_step = statistics.mean(step_ms)
     kern_ms = {name: statistics.mean(p[j] for p in per)
                for j, name in enumerate(("fwd", "bwd_preprocess", "bwd_kv_blocks", "bwd_dq_convert"))}
-    if dist:
-        t = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = max_over_ranks(ms_per_step, dist, dev)
 
     # end to end through the C ABI: pinned host inputs -> device -> fwd + bwd -> host outputs
     hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "do"))
@@ -332,15 +346,11 @@ def main() -> None:
         b.synchronize()
         e_ms.append(a.elapsed_time(b))
     sampler.stop()
-    e2e_ms = statistics.mean(e_ms) if e_ms else float("nan")
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(statistics.mean(e_ms) if e_ms else float("nan"), dist, dev)
 
     fwd_f, bwd_f = step_flops(w)
     flops = fwd_f + bwd_f
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(flops, world, ms_per_step)
     pk = peaks()
     dominant = "bwd_kv_blocks"
     achieved = bwd_f / (kern_ms[dominant] * 1e-3) / 1e12
@@ -361,7 +371,7 @@ def main() -> None:
                      "traffic": traffic_from_profile(f"{dominant}:{w.name}"),
                      "peak_kind": f"bf16 dense burst ({pk['source']})"},
         "cpu_baseline": ({k_: v_ for k_, v_ in cpu.items() if k_ != "seconds"} if cpu else None),
-        "e2e": ({"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        "e2e": ({"value": job_throughput(flops, world, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                  "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms} if e_ms else None),
         "gpu_launches": 4 * args.steps,
         "clocks": sampler.summary(t_wall0, t_wall1),
