@@ -204,17 +204,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       constexpr uint32_t idQT = idesc_f16(D, 128, BF16, true, true);      // dQ^T: A = K^T MN-major, B = dS^T MN-major
       auto slot_of = [](int L) { return L % NR; };
       auto phase_of = [](int L) { return static_cast<uint32_t>((L / NR) & 1); };
+      // Descriptor low words of the operand bases (K-major: leading offset unused; MN-major: the
+      // 64-column chunk stride).  A K step adds a constant, so one thread keeps up with the tensor core.
+      constexpr uint32_t kTileLo = C::TILE >> 4;
+      const uint32_t k_kmaj = sdesc_lo(sK, 16), v_kmaj = sdesc_lo(sV, 16), ring_kmaj = sdesc_lo(sRing, 16);
+      const uint32_t ring_mn = sdesc_lo(sRing, kChunkBytes), k_mn = sdesc_lo(sK, kChunkBytes);
+      const uint32_t ds_mn = sdesc_lo(sDS, kChunkBytes);
 
       // S^T_i = K Q_i^T into X
       auto issue_S = [&](int it) -> bool {
         const int L = 2 * it;
         if (!mbar_wait(bars.ring_full(slot_of(L)), phase_of(L), wc)) return false;
         tc_fence_after();
-        const uint32_t sq = sRing + slot_of(L) * C::TILE;
+        const uint32_t b_lo = ring_kmaj + slot_of(L) * kTileLo;
+        mma_ss_lo<false>(tX, k_kmaj, b_lo, idS);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
-          mma_ss(tX, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sq + off, 16, 1024), idS, k > 0);
+        for (int k = 1; k < D / 16; ++k) {
+          const uint32_t off = ((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4;
+          mma_ss_lo<true>(tX, k_kmaj + off, b_lo + off, idS);
         }
         mma_commit(bars.s_full());
         return true;
@@ -225,11 +232,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         if (!mbar_wait(bars.ring_full(slot_of(L)), phase_of(L), wc)) return false;
         if (!mbar_wait(bars.s_used(), it & 1, wc)) return false;
         tc_fence_after();
-        const uint32_t sdo = sRing + slot_of(L) * C::TILE;
+        const uint32_t b_lo = ring_kmaj + slot_of(L) * kTileLo;
+        mma_ss_lo<false>(tX, v_kmaj, b_lo, idS);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
-          mma_ss(tX, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024), idS, k > 0);
+        for (int k = 1; k < D / 16; ++k) {
+          const uint32_t off = ((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4;
+          mma_ss_lo<true>(tX, v_kmaj + off, b_lo + off, idS);
         }
         mma_commit(bars.dp_full());
         return true;
@@ -241,17 +249,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       for (int it = 0; ok && it < n; ++it) {
         if (!(ok = mbar_wait(bars.pd_ready(), it & 1, wc))) break;
         tc_fence_after();
-        const uint32_t sq = sRing + slot_of(2 * it) * C::TILE;
-        const uint32_t sdo = sRing + slot_of(2 * it + 1) * C::TILE;
-        // dV += P^T dO_i   (A: P^T packed in TMEM X; B: dO_i [query][d] MN-major)
+        const uint32_t q_lo = ring_mn + slot_of(2 * it) * kTileLo;
+        const uint32_t do_lo = ring_mn + slot_of(2 * it + 1) * kTileLo;
+        const uint32_t acc0 = it > 0 ? 1u : 0u;
+        // dV += P^T dO_i   (A: P^T packed in TMEM X; B: dO_i [query][d] MN-major, 16 query rows per K step)
+        mma_ts_lo_rt(tdV, tX + packed_col(0, 0), do_lo, idG, acc0);
 #pragma unroll
-        for (int k = 0; k < 128 / 16; ++k)
-          mma_ts(tdV, tX + packed_col(k, 0), sdesc_sw128(sdo + k * 2048, kChunkBytes, 1024), idG, (it > 0 || k > 0));
+        for (int k = 1; k < 128 / 16; ++k) mma_ts_lo<true>(tdV, tX + packed_col(k, 0), do_lo + k * (2048 >> 4), idG);
         mma_commit(bars.ring_empty(slot_of(2 * it + 1)));
         // dK += dS^T Q_i   (A: dS^T packed in TMEM X; B: Q_i [query][d] MN-major)
+        mma_ts_lo_rt(tdK, tX + packed_col(0, 32), q_lo, idG, acc0);
 #pragma unroll
-        for (int k = 0; k < 128 / 16; ++k)
-          mma_ts(tdK, tX + packed_col(k, 32), sdesc_sw128(sq + k * 2048, kChunkBytes, 1024), idG, (it > 0 || k > 0));
+        for (int k = 1; k < 128 / 16; ++k) mma_ts_lo<true>(tdK, tX + packed_col(k, 32), q_lo + k * (2048 >> 4), idG);
         mma_commit(bars.ring_empty(slot_of(2 * it)));
         // S^T_{i+1} overwrites X after dV_i, dK_i have read it (MMAs of one thread run in order).
         if (it + 1 < n && !(ok = issue_S(it + 1))) break;
@@ -261,16 +270,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         if constexpr (D == 128) {
           // dQ_i^T = K^T dS^T  (A: K^T [d][key] read MN-major from the K tile; B: dS^T [query][key] read
           // MN-major from the dS^T tile).  TMEM lane = d, so each warp's reduction covers whole rows.
+          mma_ss_lo<false>(tY, k_mn, ds_mn, idQT);
 #pragma unroll
-          for (int k = 0; k < 128 / 16; ++k)
-            mma_ss(tY, sdesc_sw128(sK + k * 2048, kChunkBytes, 1024), sdesc_sw128(sDS + k * 2048, kChunkBytes, 1024),
-                   idQT, k > 0);
+          for (int k = 1; k < 128 / 16; ++k) mma_ss_lo<true>(tY, k_mn + k * (2048 >> 4), ds_mn + k * (2048 >> 4), idQT);
         } else {
           // dQ_i = dS K  (A: dS [query][key] read MN-major from the dS^T tile; B: K [key][d] MN-major)
+          mma_ss_lo<false>(tY, ds_mn, k_mn, idQ);
 #pragma unroll
-          for (int k = 0; k < 128 / 16; ++k)
-            mma_ss(tY, sdesc_sw128(sDS + k * 2048, kChunkBytes, 1024), sdesc_sw128(sK + k * 2048, kChunkBytes, 1024),
-                   idQ, k > 0);
+          for (int k = 1; k < 128 / 16; ++k) mma_ss_lo<true>(tY, ds_mn + k * (2048 >> 4), k_mn + k * (2048 >> 4), idQ);
         }
         mma_commit(bars.dq_full());
         mma_commit(bars.ds_empty());

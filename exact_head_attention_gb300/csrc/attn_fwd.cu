@@ -220,17 +220,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       constexpr uint32_t idS = idesc_f16(128, 128, BF16, false, false);
       constexpr uint32_t idPV = idesc_f16(128, D, BF16, false, true);
       bool ok = mbar_wait(bars.q_full(), 0, wc);
+      // Descriptor low words of the operand bases; a K step adds a constant (the issue loop of a
+      // single thread must keep up with one MMA per 64 tensor-core cycles).
+      constexpr uint32_t kTileLo = C::TILE >> 4;
+      const uint32_t q_lo = sdesc_lo(sQ, 16), k_lo = sdesc_lo(sK, 16), v_lo = sdesc_lo(sV, kChunkBytes);
 
       auto issue_S = [&](int t, int j) -> bool {
         const int s = j % NS;
         if (!mbar_wait(bars.k_full(s), (j / NS) & 1, wc)) return false;
         tc_fence_after();
+        const uint32_t d = tmem + t * 128, a_lo = q_lo + t * kTileLo, b_lo = k_lo + s * kTileLo;
+        mma_ss_lo<false>(d, a_lo, b_lo, idS);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
-          const uint64_t ad = sdesc_sw128(sQ + t * C::TILE + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sK + s * C::TILE + off, 16, 1024);
-          mma_ss(tmem + t * 128, ad, bd, idS, k > 0 ? 1u : 0u);
+        for (int k = 1; k < D / 16; ++k) {
+          const uint32_t off = ((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4;
+          mma_ss_lo<true>(d, a_lo + off, b_lo + off, idS);
         }
         mma_commit(bars.s_full(t));
         return true;
@@ -240,11 +244,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         if (!mbar_wait(bars.v_full(s), (j / NS) & 1, wc)) return false;
         if (!mbar_wait(bars.p_full(t), j & 1, wc)) return false;
         tc_fence_after();
+        const uint32_t d = tmem + 256 + t * 128, a = tmem + t * 128, b_lo = v_lo + s * kTileLo;
+        mma_ts_lo_rt(d, a, b_lo, idPV, j > 0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 0; k < kTileRows / 16; ++k) {
-          const uint64_t bd = sdesc_sw128(sV + s * C::TILE + k * 2048, kChunkBytes, 1024);
-          mma_ts(tmem + 256 + t * 128, tmem + t * 128 + k * 8, bd, idPV, (j > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 1; k < kTileRows / 16; ++k) mma_ts_lo<true>(d, a + k * 8, b_lo + k * (2048 >> 4), idPV);
         return true;
       };
 
