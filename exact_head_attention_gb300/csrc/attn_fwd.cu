@@ -5,11 +5,12 @@
 // read once, K/V streamed, O written once; parallel over batch x heads x
 // query-row blocks as in "Fast Transformer training with long sequences").
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads, registers re-split per warpgroup):
 //   warps 0-3  softmax warpgroup for query tile 0 (thread = query row)
 //   warps 4-7  softmax warpgroup for query tile 1
 //   warp  8    TMA producer: Q once, then K_j / V_j into NS-deep rings
 //   warp  9    MMA issuer (one thread) and TMEM owner
+//   warps 10-11 idle (they complete the control warpgroup)
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   [  0,128) S0 = Q0 K_j^T fp32; P0 (16-bit, packed in pairs) overwrites its first 64 columns
@@ -34,7 +35,11 @@
 namespace exattn {
 namespace {
 
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 384;
+// Register shares after reallocation (launch: 168 each).  Each SM sub-partition holds one warp of
+// each of the three warpgroups, so the shares must sum to 3 x 168 = 504.
+constexpr uint32_t kRegsSoftmax = 208, kRegsControl = 88;
+static_assert(2 * kRegsSoftmax + kRegsControl == 3 * 168, "register split must match the launch");
 constexpr uint32_t kChunkBytes = 128 * 128;  // 128 rows x 128 bytes
 
 template <int D>
@@ -67,71 +72,86 @@ struct FwdBars {
   __device__ uint32_t mma_done() const { return base + 8 * (7 + 4 * ns); }
 };
 
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-// Max of this thread's 128 scores in TMEM (read 64 columns at a time); with MASKED, columns at or
-// past `lim` are ignored.
-template <bool MASKED>
-__device__ __forceinline__ float tile_row_max(uint32_t tS, int lim) {
-  float mx = -INFINITY;
+// One key tile of the online softmax for this thread's query row (= TMEM lane).  Reads the 128
+// scores of S once, updates the running max m (base-2 units of the scaled scores) and sum l,
+// rescales the O row in TMEM when the max grows by more than 2^8 (the final O / l is exact with a
+// stale max), and writes P = exp2(s * c_log2 - m) over the first 64 S columns as packed 16-bit
+// pairs: scores [64h, 64h + 64) become packed columns [32h, 32h + 32), the A operand of the PV
+// MMA (every score is in registers before the first packed column is written).  With MASKED,
+// columns at or past `lim` count as -inf.  The exponent argument and the sums use paired fp32
+// instructions.
+template <int D, bool MASKED, bool BF16>
+__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int lim, float c_log2, bool first, float& m,
+                                             float& l) {
+  uint32_t sr[4][32];
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    uint32_t sr[2][32];
-    tmem_ld32(tS + hh * 64, sr[0]);
-    tmem_ld32(tS + hh * 64 + 32, sr[1]);
-    tmem_wait_ld();
-    reg_fence32(sr[0]);
-    reg_fence32(sr[1]);
+  for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+  tmem_wait_ld();
 #pragma unroll
-    for (int i = 0; i < 64; i += 2) {
-      float a = __uint_as_float(sr[i >> 5][i & 31]), b = __uint_as_float(sr[i >> 5][(i + 1) & 31]);
-      if constexpr (MASKED) {
-        if (hh * 64 + i >= lim) a = -INFINITY;
-        if (hh * 64 + i + 1 >= lim) b = -INFINITY;
+  for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
+  if constexpr (MASKED) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(-INFINITY);
+  }
+  float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
+#pragma unroll
+  for (int p = 0; p < 64; ++p)
+    mx4[p & 3] = max3(mx4[p & 3], __uint_as_float(sr[p >> 4][(2 * p) & 31]), __uint_as_float(sr[p >> 4][(2 * p + 1) & 31]));
+  const float m_new = fmaxf(m, max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * c_log2);
+  if (first) {
+    m = m_new;
+  } else {
+    const bool need = m_new > m + 8.0f;
+    if (__any_sync(0xffffffffu, need)) {
+      // O is complete for the previous key tile: its last MMA was issued before this tile's S.
+      const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_wait_ld();
+        reg_fence32(o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st32(tO + c * 32, o);
       }
-      mx = max3(mx, a, b);
+      tmem_wait_st();
+      l *= alpha;
+      if (need) m = m_new;
     }
   }
-  return mx;
-}
-
-// P = exp2(s * c_log2 - ms) for this thread's 128 scores, packed into 16-bit pairs: scores
-// [64h, 64h + 64) become packed columns [32h, 32h + 32), the A operand of the P V MMA.  Every
-// score of a half is loaded before its packed result overwrites the first half of the S columns.
-// Returns the sum of the (fp32) probabilities.
-template <bool MASKED, bool BF16>
-__device__ __forceinline__ float tile_exp_pack(uint32_t tS, int lim, float c_log2, float ms) {
-  float l = 0.f;
+  const float ms = (m == -INFINITY) ? 0.f : m;
+  const uint64_t c2 = f2_pack(c_log2, c_log2), nm2 = f2_pack(-ms, -ms);
+  uint64_t acc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = f2_pack(0.f, 0.f);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    uint32_t sr[2][32];
-    tmem_ld32(tS + h * 64, sr[0]);
-    tmem_ld32(tS + h * 64 + 32, sr[1]);
-    tmem_wait_ld();
-    reg_fence32(sr[0]);
-    reg_fence32(sr[1]);
     uint32_t pk[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      float s0 = __uint_as_float(sr[i >> 4][(2 * i) & 31]);
-      float s1 = __uint_as_float(sr[i >> 4][(2 * i + 1) & 31]);
-      if constexpr (MASKED) {
-        if (h * 64 + 2 * i >= lim) s0 = -INFINITY;
-        if (h * 64 + 2 * i + 1 >= lim) s1 = -INFINITY;
-      }
-      const float p0 = ex2_approx(fmaf(s0, c_log2, -ms));
-      const float p1 = ex2_approx(fmaf(s1, c_log2, -ms));
-      l += p0 + p1;
+      const int p = h * 32 + i;  // score pair (2p, 2p + 1)
+      const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[p >> 4][(2 * p) & 31]), __uint_as_float(sr[p >> 4][(2 * p + 1) & 31])),
+                                c2, nm2);
+      float x0, x1;
+      f2_unpack(x, x0, x1);
+      const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+      acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
       pk[i] = pack2<BF16>(p0, p1);
     }
     tmem_st32(tS + h * 32, pk);
   }
-  return l;
+  float s0, s1, s2, s3;
+  f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
+  (void)s2;
+  (void)s3;
+  l += s0 + s1;
 }
+
+
 
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdArgs a) {
@@ -182,9 +202,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp >= 8) {
+    // ------------------------------------------------------------ control warpgroup
+    // warp 8: TMA producer, warp 9: MMA issuer, warps 10-11: idle.
+    regs_decrease<kRegsControl>();
+    if (warp == 8 && lane == 0) {
+      // ---- producer
       prefetch_tmap(&a.tm_q);
       prefetch_tmap(&a.tm_k);
       prefetch_tmap(&a.tm_v);
@@ -213,10 +236,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         for (int j = max(0, issued_v - NS); j < issued_v; ++j) mbar_drain(bars.v_full(j % NS), (j / NS) & 1, a.timeout_ns);
         mbar_drain(bars.q_full(), 0, a.timeout_ns);
       }
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 9 && lane == 0) {
+      // ---- MMA issuer
       constexpr uint32_t idS = idesc_f16(128, 128, BF16, false, false);
       constexpr uint32_t idPV = idesc_f16(128, D, BF16, false, true);
       bool ok = mbar_wait(bars.q_full(), 0, wc);
@@ -274,6 +295,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     }
   } else {
     // ------------------------------------------------------------ softmax
+    regs_increase<kRegsSoftmax>();
     const int t = warp >> 2;                  // query tile of this warpgroup
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
     const int r = quarter * 32 + lane;        // row inside the tile = TMEM lane
@@ -293,34 +315,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       // Columns at or past `lim` are masked (ragged last key tile, causal diagonal tile).
       const bool need_mask = ((j + 1) * kTileRows > a.Nk) || (CAUSAL && j * kTileRows + kTileRows - 1 > q0 + t * kTileRows);
       const int lim = need_mask ? (CAUSAL ? min(a.Nk, row + 1) : a.Nk) - j * kTileRows : kTileRows;
-      // Pass 1: row max over the 128 scores.
-      const float mx = need_mask ? tile_row_max<true>(tS, lim) : tile_row_max<false>(tS, lim);
-      const float m_new = fmaxf(m, mx * c_log2);
-      if (j == 0) {
-        m = m_new;
-      } else {
-        const bool need = m_new > m + 8.0f;
-        if (__any_sync(0xffffffffu, need)) {
-          // O_t is complete for key tile j-1: its last MMA was issued before S_t[j].
-          const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_wait_ld();
-            reg_fence32(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + c * 32, o);
-          }
-          tmem_wait_st();
-          l *= alpha;
-          if (need) m = m_new;
-        }
-      }
-      const float ms = (m == -INFINITY) ? 0.f : m;
-      // Pass 2: P = exp2(s * scale*log2e - m), written back into TMEM as the PV MMA's A operand.
-      l += need_mask ? tile_exp_pack<true, BF16>(tS, lim, c_log2, ms) : tile_exp_pack<false, BF16>(tS, lim, c_log2, ms);
+      if (need_mask)
+        softmax_tile<D, true, BF16>(tS, tO, lim, c_log2, j == 0, m, l);
+      else
+        softmax_tile<D, false, BF16>(tS, tO, lim, c_log2, j == 0, m, l);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bars.p_full(t));
