@@ -53,20 +53,23 @@ struct BwdCfg {
   static constexpr int NCH = D / 64;
   static constexpr uint32_t TILE = kTileRows * D * 2;
   static constexpr uint32_t PT = 128 * 128 * 2;  // dS^T tile
-  // Q/dO ring slots: with 4, the loads of tile i+1 reuse the slots tile i-1 released, a whole
-  // tile ahead of their use.
-  static constexpr int NR = (D == 64) ? 6 : 4;
+  // Q/dO ring slots.  d = 128 gives one slot to the dQ staging tile: reducing dQ with the copy
+  // engine from shared memory is far cheaper than per-thread atomics, which outweighs the shallower ring.
+  static constexpr int NR = (D == 64) ? 6 : 3;
+  // fp32 dQ staging for d = 128: 64 query rows x 128 d, the accumulator's own row-major layout
+  static constexpr uint32_t STAGE_BYTES = (D == 128) ? 64 * 128 * 4 : 0;
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + TILE;
   static constexpr uint32_t OFF_DS = OFF_V + TILE;
   static constexpr uint32_t OFF_RING = OFF_DS + PT;
+  static constexpr uint32_t OFF_STAGE = OFF_RING + NR * TILE;
   // two slots of the query tile's row vectors: 128 base-2 LSE then 128 D values (fp32)
-  static constexpr uint32_t OFF_ROWV = OFF_RING + NR * TILE;
+  static constexpr uint32_t OFF_ROWV = OFF_STAGE + STAGE_BYTES;
   static constexpr uint32_t ROWV_BYTES = 2 * 128 * 4;
   static constexpr uint32_t OFF_BAR = OFF_ROWV + 2 * ROWV_BYTES;
   // kv_full, ring_full[NR], ring_empty[NR], s_full, s_used, dp_full, pd_ready, ds_empty,
-  // dq_full, dq_empty, done, mma_done, rowv_full[2], rowv_empty[2], dss_ready
-  static constexpr int NBAR = 1 + 2 * NR + 14;
+  // dq_full, dq_empty, done, mma_done, rowv_full[2], rowv_empty[2], dss_ready, dstile_free
+  static constexpr int NBAR = 1 + 2 * NR + 15;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   // The operand tiles need 1024-byte alignment; the dynamic shared memory base is checked at entry
@@ -87,6 +90,8 @@ struct BwdBars {
   __device__ uint32_t dp_full() const { return at(2); }
   __device__ uint32_t pd_ready() const { return at(3); }   // P^T, dS^T packed in TMEM X
   __device__ uint32_t dss_ready() const { return at(13); } // dS^T in shared memory
+  // d = 128: the copy engine has read warpgroup 1's dQ rows out of the dS^T tile
+  __device__ uint32_t dstile_free() const { return at(14); }
   __device__ uint32_t ds_empty() const { return at(4); }
   __device__ uint32_t dq_full() const { return at(5); }
   __device__ uint32_t dq_empty() const { return at(6); }
@@ -136,6 +141,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     mbar_init(bars.dp_full(), 1);
     mbar_init(bars.pd_ready(), 256);
     mbar_init(bars.dss_ready(), 256);
+    mbar_init(bars.dstile_free(), 1);
     mbar_init(bars.ds_empty(), 1);
     mbar_init(bars.dq_full(), 1);
     mbar_init(bars.dq_empty(), 256);
@@ -305,8 +311,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       if (!mbar_wait_warp(bars.dq_full(), it & 1, wc)) return false;
       tc_fence_after();
       if constexpr (D == 128) {
-        // dQ_i^T: lane = d, column = query row.  This warpgroup reduces query rows [64h, 64h + 64); for
-        // each row a warp's 32 scalar reductions cover 32 consecutive floats (one 128-byte line).
+        // dQ_i^T: lane = d, column = query row.  This warpgroup reduces query rows [64h, 64h + 64):
+        // it writes them row-major (the accumulator's layout; a warp's 32 lanes are 32 consecutive
+        // floats of a row) into a 32 KB buffer and one thread has the copy engine add that contiguous
+        // block into the accumulator.  Warpgroup 0 owns the staging tile (its previous reduction was
+        // issued a whole tile ago); warpgroup 1 uses the dS^T tile, free from the end of the dQ_i MMA
+        // until the next dS^T store, which waits for this reduction's read (see dstile_free).
         uint32_t v[2][32];
         tmem_ld32(tY + lane_bits + h * 64, v[0]);
         tmem_ld32(tY + lane_bits + h * 64 + 32, v[1]);
@@ -315,10 +325,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         reg_fence32(v[1]);
         tc_fence_before();
         mbar_arrive(bars.dq_empty());
-        const size_t row0 = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows + h * 64;
-        float* dst = a.dq_acc + row0 * D + r;
+        const uint32_t buf_off = h ? C::OFF_DS : C::OFF_STAGE;
+        if (h == 0) {
+          if (r == 0) tma_store_wait_read_all();  // the previous reduction from the staging tile
+          named_bar_sync(1, 128);
+        }
+        float* buf = reinterpret_cast<float*>(gbase + buf_off);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) red_add_f32(dst + static_cast<size_t>(c) * D, __uint_as_float(v[c >> 5][c & 31]));
+        for (int c = 0; c < 64; ++c) buf[c * D + r] = __uint_as_float(v[c >> 5][c & 31]);
+        fence_proxy_async_smem();
+        named_bar_sync(1 + h, 128);
+        if (r == 0) {
+          const size_t row0 = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows + h * 64;
+          bulk_reduce_add_f32(a.dq_acc + row0 * D, sbase + buf_off, C::STAGE_BYTES);
+          tma_store_commit();
+        }
       } else {
         // dQ_i: lane = query row; this warpgroup reduces d columns [32h, 32h + 32).
         uint32_t v[32];
@@ -382,6 +403,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
 #pragma unroll
       for (int i = 0; i < 32; ++i) pp[i] = pack2<BF16>(p[2 * i], p[2 * i + 1]);
 
+      // d = 128: dQ of the previous tile completes just before this tile's dP^T; staging it for the
+      // copy engine fits in that window.
+      if (D == 128 && it > 0 && !(ok = drain_dq(it - 1))) break;
+
       if (!(ok = mbar_wait_warp(bars.dp_full(), it & 1, wc))) break;
       tc_fence_after();
       tmem_ld32(tX + lane_bits + h * 64, s[0]);
@@ -413,14 +438,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       tc_fence_before();
       mbar_arrive(bars.pd_ready());  // dV_i, dK_i and S_{i+1} may go
       if (it > 0 && !(ok = mbar_wait_warp(bars.ds_empty(), (it - 1) & 1, wc))) break;
+      if constexpr (D == 128) {
+        // The dS^T tile held warpgroup 1's dQ_{i-1} rows; the copy engine must have read them.
+        if (it > 0 && h == 1) {
+          if (r == 0) tma_store_wait_read_all();
+          named_bar_sync(2, 128);
+          if (r == 0) mbar_arrive(bars.dstile_free());
+        }
+        if (it > 0 && h == 0 && !(ok = mbar_wait_warp(bars.dstile_free(), (it - 1) & 1, wc))) break;
+      }
 #pragma unroll
       for (int u = 0; u < 8; ++u)
         st_shared_v4(ds_row + sw128_offset(r, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       fence_proxy_async_smem();
       mbar_arrive(bars.dss_ready());  // dQ_i may go
 
-      // The previous tile's dQ has been ready since before this tile's dP^T.
-      if (it > 0 && !(ok = drain_dq(it - 1))) break;
+      // d = 64: the previous tile's per-thread reductions run after this tile is handed over.
+      if (D == 64 && it > 0 && !(ok = drain_dq(it - 1))) break;
     }
     if (ok && n > 0) ok = drain_dq(n - 1);
 
@@ -462,8 +496,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       const CUtensorMap* map = h ? &a.tm_dk : &a.tm_dv;
       for (int ch = 0; ch < C::NCH; ++ch) tma_store_3d(map, stage + ch * kChunkBytes, ch * 64, k0, bh);
       tma_store_commit();
-      tma_store_wait_all();
     }
+    if (r == 0) tma_store_wait_all();  // this thread's stores and dQ reductions have completed
   }
 
   tc_fence_before();

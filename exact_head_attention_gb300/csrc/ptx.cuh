@@ -150,6 +150,15 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                : "memory");
 }
 
+// Element-wise fp32 add of `bytes` contiguous bytes of shared memory into global memory, performed
+// by the copy engine (whole lines; no per-thread atomics).  Both addresses 16-byte aligned, size a
+// multiple of 16.  Tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_store_wait_read_all() {
