@@ -7,9 +7,14 @@ product path (the CUDA library and its binding) never does, and the two share
 no code.
 
 Definitions (cited in ``attn_oracle.c``):
-  * forward  O = softmax(scale * Q K^T [+ top-left causal mask]) V
+  * forward  O = softmax(scale * Q K^T [+ causal mask]) V
     -- SparkAttention (arXiv 2502.12784), Equation 1; CANN ops-transformer MHA
     article, section 1;
+  * causal = 1 (or True, "top_left"): query q sees keys k <= q;
+    causal = 2 ("bottom_right"): the queries are the last Nq positions of the
+    Nk-long sequence (SparkAttention Figure 1, masked self-attention over
+    preceding positions), so query q sees keys k <= q + Nk - Nq; a row that
+    sees no key has O = 0, LSE = -inf and zero gradients;
   * LSE_q = m_q + ln sum_k exp(s_qk - m_q) -- StreamKL summary, Methodology 1-2;
   * backward of sum(O * dO): dV = P^T dO, dP = dO V^T, D = rowsum(P o dP),
     dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q -- SparkAttention,
@@ -86,6 +91,17 @@ def _lptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_long))
 
 
+_MASKS = {False: 0, True: 1, 0: 0, 1: 1, 2: 2, "none": 0, "top_left": 1, "bottom_right": 2}
+
+
+def _mask(causal) -> int:
+    """Mask code: 0 none, 1 top-left causal, 2 bottom-right causal."""
+    key = causal.item() if isinstance(causal, np.generic) else causal
+    if key not in _MASKS:
+        raise ValueError(f"unknown causal mask {causal!r}")
+    return _MASKS[key]
+
+
 def _shape(q, k):
     B, H, Nq, d = q.shape
     Bk, Hk, Nk, dk = k.shape
@@ -94,20 +110,20 @@ def _shape(q, k):
     return B, H, Nq, Nk, d
 
 
-def attn_fwd(q, k, v, causal: bool, scale: float):
+def attn_fwd(q, k, v, causal, scale: float):
     """O [B,H,Nq,d] and LSE [B,H,Nq] in fp64 for the full problem."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, Nq, Nk, d = _shape(q, k)
     o = np.zeros((B, H, Nq, d))
     lse = np.zeros((B, H, Nq))
     rc = _load().oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                                 B, H, Nq, Nk, d, int(causal), float(scale))
+                                 B, H, Nq, Nk, d, _mask(causal), float(scale))
     if rc != 0:
         raise MemoryError("oracle_attn_fwd failed")
     return o, lse
 
 
-def attn_bwd(q, k, v, do, causal: bool, scale: float):
+def attn_bwd(q, k, v, do, causal, scale: float):
     """(dQ, dK, dV, D) in fp64 for the loss sum(O * dO)."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, Nq, Nk, d = _shape(q, k)
@@ -116,27 +132,27 @@ def attn_bwd(q, k, v, do, causal: bool, scale: float):
     dv = np.zeros((B, H, Nk, d))
     D = np.zeros((B, H, Nq))
     rc = _load().oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
-                                 _ptr(D), B, H, Nq, Nk, d, int(causal), float(scale))
+                                 _ptr(D), B, H, Nq, Nk, d, _mask(causal), float(scale))
     if rc != 0:
         raise MemoryError("oracle_attn_bwd failed")
     return dq, dk, dv, D
 
 
-def attn_fwd_rows(q, k, v, causal: bool, scale: float, rows):
+def attn_fwd_rows(q, k, v, causal, scale: float, rows):
     """O and LSE for chosen query rows; rows[i] = (b*H + h)*Nq + q."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, Nq, Nk, d = _shape(q, k)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     o = np.zeros((len(rows), d))
     lse = np.zeros(len(rows))
-    rc = _load().oracle_attn_fwd_rows(_ptr(q), _ptr(k), _ptr(v), B, H, Nq, Nk, d, int(causal),
+    rc = _load().oracle_attn_fwd_rows(_ptr(q), _ptr(k), _ptr(v), B, H, Nq, Nk, d, _mask(causal),
                                       float(scale), len(rows), _lptr(rows), _ptr(o), _ptr(lse))
     if rc != 0:
         raise MemoryError("oracle_attn_fwd_rows failed")
     return o, lse
 
 
-def attn_dq_rows(q, k, v, do, causal: bool, scale: float, rows):
+def attn_dq_rows(q, k, v, do, causal, scale: float, rows):
     """dQ and D for chosen query rows; rows[i] = (b*H + h)*Nq + q."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, Nq, Nk, d = _shape(q, k)
@@ -144,13 +160,13 @@ def attn_dq_rows(q, k, v, do, causal: bool, scale: float, rows):
     dq = np.zeros((len(rows), d))
     D = np.zeros(len(rows))
     rc = _load().oracle_attn_dq_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, H, Nq, Nk, d,
-                                     int(causal), float(scale), len(rows), _lptr(rows), _ptr(dq), _ptr(D))
+                                     _mask(causal), float(scale), len(rows), _lptr(rows), _ptr(dq), _ptr(D))
     if rc != 0:
         raise MemoryError("oracle_attn_dq_rows failed")
     return dq, D
 
 
-def attn_dkdv_cols(q, k, v, do, causal: bool, scale: float, cols):
+def attn_dkdv_cols(q, k, v, do, causal, scale: float, cols):
     """dK and dV for chosen key rows; cols[i] = (b*H + h)*Nk + k."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, Nq, Nk, d = _shape(q, k)
@@ -158,18 +174,18 @@ def attn_dkdv_cols(q, k, v, do, causal: bool, scale: float, cols):
     dk = np.zeros((len(cols), d))
     dv = np.zeros((len(cols), d))
     rc = _load().oracle_attn_dkdv_cols(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, H, Nq, Nk, d,
-                                       int(causal), float(scale), len(cols), _lptr(cols), _ptr(dk), _ptr(dv))
+                                       _mask(causal), float(scale), len(cols), _lptr(cols), _ptr(dk), _ptr(dv))
     if rc != 0:
         raise MemoryError("oracle_attn_dkdv_cols failed")
     return dk, dv
 
 
-def attn_probs(qh, kh, causal: bool, scale: float):
+def attn_probs(qh, kh, causal, scale: float):
     """P [Nq, Nk] and LSE [Nq] of one head (qh [Nq, d], kh [Nk, d])."""
     qh, kh = _f64(qh), _f64(kh)
     Nq, d = qh.shape
     Nk = kh.shape[0]
     p = np.zeros((Nq, Nk))
     lse = np.zeros(Nq)
-    _load().oracle_attn_probs(_ptr(qh), _ptr(kh), Nq, Nk, d, int(causal), float(scale), _ptr(p), _ptr(lse))
+    _load().oracle_attn_probs(_ptr(qh), _ptr(kh), Nq, Nk, d, _mask(causal), float(scale), _ptr(p), _ptr(lse))
     return p, lse

@@ -22,7 +22,13 @@
  *
  * Conventions (the plainest readings where the pages are silent):
  *   - tensors are contiguous row-major [B][H][N][d]; LSE and D are [B][H][Nq];
- *   - causal masking is top-left aligned: query q sees keys k <= q;
+ *   - causal = 1 is top-left aligned: query q sees keys k <= q;
+ *   - causal = 2 is bottom-right aligned: the Nq queries are the last Nq
+ *     positions of the Nk-long sequence (a decoder continuing a cached
+ *     prefix; SparkAttention Figure 1, masked self-attention over preceding
+ *     positions), so query q sees keys k <= q + Nk - Nq;
+ *   - a query row that sees no key (bottom-right with Nq > Nk) has O = 0,
+ *     LSE = -inf and zero gradients;
  *   - LSE is in natural-log units of the scaled scores;
  *   - D is the softmax Jacobian term sum_k P_qk dP_qk (mathematically equal to
  *     rowsum(dO o O)).
@@ -35,7 +41,10 @@
 #include <stdlib.h>
 #include <string.h>
 
-static int key_visible(long q, long k, int causal) { return !causal || k <= q; }
+/* Diagonal offset of the causal mask: query q sees keys k <= q + offset. */
+static long mask_offset(int causal, long Nq, long Nk) { return causal == 2 ? Nk - Nq : 0; }
+
+static int key_visible(long q, long k, int causal, long off) { return !causal || k <= q + off; }
 
 static double dot(const double* a, const double* b, int d) {
   double acc = 0.0;
@@ -51,12 +60,12 @@ static double dot(const double* a, const double* b, int d) {
  * Returns the number of visible keys (0 leaves P all zero and *lse = -inf).
  */
 static long row_probs(const double* Qh, const double* Kh, long Nk, int d, long q,
-                      int causal, double scale, double* P, double* lse) {
+                      int causal, long off, double scale, double* P, double* lse) {
   const double* qrow = Qh + (size_t)q * d;
   double m = -INFINITY;
   long nvis = 0;
   for (long k = 0; k < Nk; ++k) {
-    if (key_visible(q, k, causal)) {
+    if (key_visible(q, k, causal, off)) {
       P[k] = scale * dot(qrow, Kh + (size_t)k * d, d);
       if (P[k] > m) m = P[k];
       ++nvis;
@@ -70,7 +79,7 @@ static long row_probs(const double* Qh, const double* Kh, long Nk, int d, long q
   }
   double z = 0.0;
   for (long k = 0; k < Nk; ++k) {
-    if (key_visible(q, k, causal)) {
+    if (key_visible(q, k, causal, off)) {
       P[k] = exp(P[k] - m);
       z += P[k];
     }
@@ -95,6 +104,7 @@ static double row_dp(const double* dOh, const double* Vh, long Nk, int d, long q
 /* Full forward: O [B][H][Nq][d], LSE [B][H][Nq]. Returns 0, or -1 on allocation failure. */
 int oracle_attn_fwd(const double* Q, const double* K, const double* V, double* O, double* LSE,
                     int B, int H, long Nq, long Nk, int d, int causal, double scale) {
+  const long off = mask_offset(causal, Nq, Nk);
   double* P = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
   if (!P) return -1;
   for (long bh = 0; bh < (long)B * H; ++bh) {
@@ -103,7 +113,7 @@ int oracle_attn_fwd(const double* Q, const double* K, const double* V, double* O
     const double* Vh = V + (size_t)bh * Nk * d;
     for (long q = 0; q < Nq; ++q) {
       double lse;
-      row_probs(Qh, Kh, Nk, d, q, causal, scale, P, &lse);
+      row_probs(Qh, Kh, Nk, d, q, causal, off, scale, P, &lse);
       double* orow = O + ((size_t)bh * Nq + q) * d;
       for (int c = 0; c < d; ++c) orow[c] = 0.0;
       for (long k = 0; k < Nk; ++k) {
@@ -125,6 +135,7 @@ int oracle_attn_fwd(const double* Q, const double* K, const double* V, double* O
 int oracle_attn_bwd(const double* Q, const double* K, const double* V, const double* dO,
                     double* dQ, double* dK, double* dV, double* Dout,
                     int B, int H, long Nq, long Nk, int d, int causal, double scale) {
+  const long off = mask_offset(causal, Nq, Nk);
   double* P = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
   double* dP = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
   if (!P || !dP) {
@@ -144,7 +155,7 @@ int oracle_attn_bwd(const double* Q, const double* K, const double* V, const dou
     memset(dVh, 0, sizeof(double) * (size_t)Nk * d);
     for (long q = 0; q < Nq; ++q) {
       double lse;
-      row_probs(Qh, Kh, Nk, d, q, causal, scale, P, &lse);
+      row_probs(Qh, Kh, Nk, d, q, causal, off, scale, P, &lse);
       double D = row_dp(dOh, Vh, Nk, d, q, P, dP);
       if (Dout) Dout[(size_t)bh * Nq + q] = D;
       double* dqrow = dQh + (size_t)q * d;
@@ -152,7 +163,7 @@ int oracle_attn_bwd(const double* Q, const double* K, const double* V, const dou
       const double* dorow = dOh + (size_t)q * d;
       for (int c = 0; c < d; ++c) dqrow[c] = 0.0;
       for (long k = 0; k < Nk; ++k) {
-        if (!key_visible(q, k, causal)) continue;
+        if (!key_visible(q, k, causal, off)) continue;
         double dS = P[k] * (dP[k] - D);
         const double* krow = Kh + (size_t)k * d;
         double* dkrow = dKh + (size_t)k * d;
@@ -177,6 +188,7 @@ int oracle_attn_bwd(const double* Q, const double* K, const double* V, const dou
 int oracle_attn_fwd_rows(const double* Q, const double* K, const double* V,
                          int B, int H, long Nq, long Nk, int d, int causal, double scale,
                          long nrows, const long* rows, double* O_rows, double* lse_rows) {
+  const long off = mask_offset(causal, Nq, Nk);
   (void)B;
   (void)H;
   double* P = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
@@ -186,7 +198,7 @@ int oracle_attn_fwd_rows(const double* Q, const double* K, const double* V,
     const double* Qh = Q + (size_t)bh * Nq * d;
     const double* Kh = K + (size_t)bh * Nk * d;
     const double* Vh = V + (size_t)bh * Nk * d;
-    row_probs(Qh, Kh, Nk, d, q, causal, scale, P, &lse_rows[i]);
+    row_probs(Qh, Kh, Nk, d, q, causal, off, scale, P, &lse_rows[i]);
     double* orow = O_rows + (size_t)i * d;
     for (int c = 0; c < d; ++c) orow[c] = 0.0;
     for (long k = 0; k < Nk; ++k) {
@@ -202,6 +214,7 @@ int oracle_attn_fwd_rows(const double* Q, const double* K, const double* V,
 int oracle_attn_dq_rows(const double* Q, const double* K, const double* V, const double* dO,
                         int B, int H, long Nq, long Nk, int d, int causal, double scale,
                         long nrows, const long* rows, double* dQ_rows, double* D_rows) {
+  const long off = mask_offset(causal, Nq, Nk);
   (void)B;
   (void)H;
   double* P = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
@@ -218,13 +231,13 @@ int oracle_attn_dq_rows(const double* Q, const double* K, const double* V, const
     const double* Vh = V + (size_t)bh * Nk * d;
     const double* dOh = dO + (size_t)bh * Nq * d;
     double lse;
-    row_probs(Qh, Kh, Nk, d, q, causal, scale, P, &lse);
+    row_probs(Qh, Kh, Nk, d, q, causal, off, scale, P, &lse);
     double D = row_dp(dOh, Vh, Nk, d, q, P, dP);
     if (D_rows) D_rows[i] = D;
     double* dqrow = dQ_rows + (size_t)i * d;
     for (int c = 0; c < d; ++c) dqrow[c] = 0.0;
     for (long k = 0; k < Nk; ++k) {
-      if (!key_visible(q, k, causal)) continue;
+      if (!key_visible(q, k, causal, off)) continue;
       double dS = P[k] * (dP[k] - D);
       for (int c = 0; c < d; ++c) dqrow[c] += scale * dS * Kh[(size_t)k * d + c];
     }
@@ -242,6 +255,7 @@ int oracle_attn_dq_rows(const double* Q, const double* K, const double* V, const
 int oracle_attn_dkdv_cols(const double* Q, const double* K, const double* V, const double* dO,
                           int B, int H, long Nq, long Nk, int d, int causal, double scale,
                           long ncols, const long* cols, double* dK_cols, double* dV_cols) {
+  const long off = mask_offset(causal, Nq, Nk);
   double* P = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
   double* dP = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
   if (!P || !dP) {
@@ -252,7 +266,7 @@ int oracle_attn_dkdv_cols(const double* Q, const double* K, const double* V, con
   memset(dK_cols, 0, sizeof(double) * (size_t)ncols * d);
   memset(dV_cols, 0, sizeof(double) * (size_t)ncols * d);
   for (long bh = 0; bh < (long)B * H; ++bh) {
-    /* smallest chosen key of this head: rows q < kmin see none of them when causal */
+    /* smallest chosen key of this head: rows q < kmin - off see none of them when causal */
     long kmin = -1;
     for (long i = 0; i < ncols; ++i)
       if (cols[i] / Nk == bh && (kmin < 0 || cols[i] % Nk < kmin)) kmin = cols[i] % Nk;
@@ -261,16 +275,16 @@ int oracle_attn_dkdv_cols(const double* Q, const double* K, const double* V, con
     const double* Kh = K + (size_t)bh * Nk * d;
     const double* Vh = V + (size_t)bh * Nk * d;
     const double* dOh = dO + (size_t)bh * Nq * d;
-    for (long q = causal ? kmin : 0; q < Nq; ++q) {
+    for (long q = (causal && kmin - off > 0) ? kmin - off : 0; q < Nq; ++q) {
       double lse;
-      row_probs(Qh, Kh, Nk, d, q, causal, scale, P, &lse);
+      row_probs(Qh, Kh, Nk, d, q, causal, off, scale, P, &lse);
       double D = row_dp(dOh, Vh, Nk, d, q, P, dP);
       const double* qrow = Qh + (size_t)q * d;
       const double* dorow = dOh + (size_t)q * d;
       for (long i = 0; i < ncols; ++i) {
         if (cols[i] / Nk != bh) continue;
         long k = cols[i] % Nk;
-        if (!key_visible(q, k, causal)) continue;
+        if (!key_visible(q, k, causal, off)) continue;
         double dS = P[k] * (dP[k] - D);
         for (int c = 0; c < d; ++c) {
           dK_cols[(size_t)i * d + c] += scale * dS * qrow[c];
@@ -287,6 +301,7 @@ int oracle_attn_dkdv_cols(const double* Q, const double* K, const double* V, con
 /* The full probability matrix of one head, P [Nq][Nk] (small shapes; used by invariant checks). */
 int oracle_attn_probs(const double* Qh, const double* Kh, long Nq, long Nk, int d, int causal,
                       double scale, double* P, double* lse) {
-  for (long q = 0; q < Nq; ++q) row_probs(Qh, Kh, Nk, d, q, causal, scale, P + (size_t)q * Nk, &lse[q]);
+  const long off = mask_offset(causal, Nq, Nk);
+  for (long q = 0; q < Nq; ++q) row_probs(Qh, Kh, Nk, d, q, causal, off, scale, P + (size_t)q * Nk, &lse[q]);
   return 0;
 }

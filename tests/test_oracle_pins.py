@@ -233,3 +233,112 @@ def test_sampled_rows_and_cols_match_full(causal):
     dk_c, dv_c = oracle.attn_dkdv_cols(q, k, v, do, causal, 0.3, cols)
     np.testing.assert_allclose(dk_c, dk.reshape(-1, Nk, d)[bk, ki], atol=1e-13)
     np.testing.assert_allclose(dv_c, dv.reshape(-1, Nk, d)[bk, ki], atol=1e-13)
+
+
+# ------------------------------------------------- bottom-right causal mask
+
+def test_bottom_right_square_is_top_left():
+    q, k, v, do = _qkv(1, 2, 24, 24, 8, seed=20)
+    for f in (lambda c: oracle.attn_fwd(q, k, v, c, 0.4), lambda c: oracle.attn_bwd(q, k, v, do, c, 0.4)):
+        for a, b in zip(f(1), f(2)):
+            np.testing.assert_array_equal(a, b)
+
+
+def test_bottom_right_single_query_sees_every_key():
+    q, k, v, do = _qkv(2, 1, 1, 37, 8, seed=21)
+    for a, b in zip(oracle.attn_bwd(q, k, v, do, 0, 0.4), oracle.attn_bwd(q, k, v, do, "bottom_right", 0.4)):
+        np.testing.assert_array_equal(a, b)
+    o0, l0 = oracle.attn_fwd(q, k, v, False, 0.4)
+    o2, l2 = oracle.attn_fwd(q, k, v, 2, 0.4)
+    np.testing.assert_array_equal(o0, o2)
+    np.testing.assert_array_equal(l0, l2)
+
+
+@pytest.mark.parametrize("Nq", [1, 9, 30])
+def test_bottom_right_is_suffix_of_square_causal(Nq):
+    """The last Nq queries of a square top-left problem, posed alone with bottom-right alignment,
+    give the same rows of O, LSE, dQ; with dO zero on the leading rows, the same dK, dV."""
+    Nk, d = 30, 8
+    qf, k, v, dof = _qkv(1, 2, Nk, Nk, d, seed=22)
+    dof[:, :, : Nk - Nq] = 0.0
+    qs, dos = qf[:, :, Nk - Nq:], dof[:, :, Nk - Nq:]
+    of, lf = oracle.attn_fwd(qf, k, v, True, 0.35)
+    os_, ls = oracle.attn_fwd(qs, k, v, "bottom_right", 0.35)
+    np.testing.assert_array_equal(os_, of[:, :, Nk - Nq:])
+    np.testing.assert_array_equal(ls, lf[:, :, Nk - Nq:])
+    dqf, dkf, dvf, _ = oracle.attn_bwd(qf, k, v, dof, True, 0.35)
+    dqs, dks, dvs, _ = oracle.attn_bwd(qs, k, v, dos, "bottom_right", 0.35)
+    np.testing.assert_array_equal(dqs, dqf[:, :, Nk - Nq:])
+    np.testing.assert_allclose(dks, dkf, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(dvs, dvf, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("Nq,Nk", [(20, 45), (45, 20), (64, 64)])
+def test_bottom_right_matches_torch_masked_sdpa(Nq, Nk):
+    B, H, d = 1, 2, 16
+    q, k, v, do = _qkv(B, H, Nq, Nk, d, seed=23)
+    sc = 1.0 / math.sqrt(d)
+    allowed = torch.ones(Nq, Nk, dtype=torch.bool).tril(diagonal=Nk - Nq)
+    seen = allowed.any(dim=1).numpy()  # rows that see at least one key
+    tq, tk, tv = (torch.from_numpy(x).requires_grad_(True) for x in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(
+        tq[:, :, seen], tk, tv, attn_mask=allowed[torch.from_numpy(seen)], scale=sc)
+    to.backward(torch.from_numpy(do[:, :, seen]))
+    o, lse = oracle.attn_fwd(q, k, v, 2, sc)
+    dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, 2, sc)
+    np.testing.assert_allclose(o[:, :, seen], to.detach().numpy(), atol=1e-12)
+    np.testing.assert_allclose(dq[:, :, seen], tq.grad.numpy()[:, :, seen], atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-12)
+    # rows that see no key: zero output, -inf LSE, zero dQ
+    assert np.all(o[:, :, ~seen] == 0.0) and np.all(dq[:, :, ~seen] == 0.0)
+    assert np.all(np.isneginf(lse[:, :, ~seen]))
+    s = sc * torch.from_numpy(q[:, :, seen]) @ torch.from_numpy(k).transpose(-1, -2)
+    s = s.masked_fill(~allowed[torch.from_numpy(seen)], float("-inf"))
+    np.testing.assert_allclose(lse[:, :, seen], torch.logsumexp(s, dim=-1).numpy(), atol=1e-12)
+
+
+@pytest.mark.parametrize("Nq,Nk", [(5, 7), (7, 5)])
+def test_bottom_right_gradients_match_finite_differences(Nq, Nk):
+    d, sc, h = 4, 0.8, 1e-6
+    q, k, v, do = _qkv(1, 1, Nq, Nk, d, seed=24)
+    dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, 2, sc)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.attn_fwd(qq, kk, vv, 2, sc)
+        return float((o * do).sum())
+
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            args = {"q": q, "k": k, "v": v}
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args[name] = xp
+            lp = loss(args["q"], args["k"], args["v"])
+            args[name] = xm
+            lm = loss(args["q"], args["k"], args["v"])
+            num[idx] = (lp - lm) / (2 * h)
+        err = np.linalg.norm(num - g) / max(np.linalg.norm(g), 1e-30)
+        assert err < 1e-6, (name, err)
+
+
+@pytest.mark.parametrize("Nq,Nk", [(30, 40), (40, 30)])
+def test_bottom_right_sampled_rows_and_cols_match_full(Nq, Nk):
+    B, H, d = 2, 2, 8
+    q, k, v, do = _qkv(B, H, Nq, Nk, d, seed=25)
+    o, lse = oracle.attn_fwd(q, k, v, 2, 0.3)
+    dq, dk, dv, D = oracle.attn_bwd(q, k, v, do, 2, 0.3)
+    rows = np.array([0, 5, Nq - 1, Nq + 7, 3 * Nq + Nq - 1])
+    bh, qi = rows // Nq, rows % Nq
+    o_r, lse_r = oracle.attn_fwd_rows(q, k, v, 2, 0.3, rows)
+    np.testing.assert_allclose(o_r, o.reshape(-1, Nq, d)[bh, qi], atol=1e-13)
+    np.testing.assert_array_equal(lse_r, lse.reshape(-1, Nq)[bh, qi])
+    dq_r, D_r = oracle.attn_dq_rows(q, k, v, do, 2, 0.3, rows)
+    np.testing.assert_allclose(dq_r, dq.reshape(-1, Nq, d)[bh, qi], atol=1e-13)
+    cols = np.array([0, 17, Nk - 1, Nk + 1, 2 * Nk + 20, 3 * Nk + Nk - 1])
+    bk, ki = cols // Nk, cols % Nk
+    dk_c, dv_c = oracle.attn_dkdv_cols(q, k, v, do, 2, 0.3, cols)
+    np.testing.assert_allclose(dk_c, dk.reshape(-1, Nk, d)[bk, ki], atol=1e-13)
+    np.testing.assert_allclose(dv_c, dv.reshape(-1, Nk, d)[bk, ki], atol=1e-13)
