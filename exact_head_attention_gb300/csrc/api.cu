@@ -96,25 +96,47 @@ attn_status device_state(DeviceState** out) {
   return ATTN_OK;
 }
 
-// 3-D map over a contiguous [BH][N][d] 16-bit tensor; box = 64 columns x 128 rows x 1,
-// 128-byte swizzle (matches the kernels' shared-memory operand layout); rows
+// 4-D map {d, N, H, B} over a 16-bit tensor with element strides `st` (d contiguous); box = 64
+// columns x 128 rows x 1 x 1, 128-byte swizzle (the kernels' shared-memory operand layout); rows
 // past N read as zero and are dropped on store.
-CUresult encode_map(CUtensorMap* map, const void* ptr, bool bf16, int bh, int n, int d) {
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(n) * d * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTileRows), 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+CUresult encode_map(CUtensorMap* map, const void* ptr, bool bf16, int B, int H, int n, int d, const RowStrides& st) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n) * 2, static_cast<cuuint64_t>(st.h) * 2,
+                                 static_cast<cuuint64_t>(st.b) * 2};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kTileRows), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                               const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r;
 }
 
+RowStrides contiguous(int H, int n, int d) {
+  return RowStrides{static_cast<long long>(H) * n * d, static_cast<long long>(n) * d, d};
+}
+
+// Checks a caller's strides and replaces the stride of a dimension of extent 1 (never used to
+// address anything) by the row stride, so that the tensor map accepts it.
+bool normalise_strides(const attn_strides& in, int B, int H, int d, RowStrides* out) {
+  constexpr long long kMax = (1ll << 39) - 1;  // byte strides below 2^40
+  RowStrides st{in.batch, in.head, in.row};
+  if (st.n < d || st.n % 8 != 0 || st.n > kMax) return false;
+  if (H == 1) st.h = st.n;
+  if (B == 1) st.b = st.n;
+  if (st.h <= 0 || st.h % 8 != 0 || st.h > kMax) return false;
+  if (st.b <= 0 || st.b % 8 != 0 || st.b > kMax) return false;
+  *out = st;
+  return true;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-attn_status check_common(int B, int H, int Nq, int Nk, int d, float scale, attn_dtype dtype) {
+attn_status check_common(int B, int H, int Nq, int Nk, int d, int causal, float scale, attn_dtype dtype) {
   if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != ATTN_MASK_NONE && causal != ATTN_MASK_CAUSAL && causal != ATTN_MASK_CAUSAL_BOTTOM_RIGHT)
+    return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
@@ -129,6 +151,9 @@ int padded_rows(int Nq) { return (Nq + kTileRows - 1) / kTileRows * kTileRows; }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Diagonal offset of the causal mask: query q sees keys k <= q + offset.
+int causal_offset(int causal, int Nq, int Nk) { return causal == ATTN_MASK_CAUSAL_BOTTOM_RIGHT ? Nk - Nq : 0; }
+
 attn_status finish(cudaError_t e, cudaStream_t stream) {
   if (e != cudaSuccess) return cuda_fail("kernel launch", e);
   if (checked_mode()) return attn_check_device_error(stream);
@@ -140,35 +165,66 @@ attn_status finish(cudaError_t e, cudaStream_t stream) {
 
 using namespace exattn;
 
-extern "C" attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
-                                int Nq, int Nk, int d, int causal, float scale, attn_dtype dtype, void* stream) {
-  attn_status st = check_common(B, H, Nq, Nk, d, scale, dtype);
-  if (st != ATTN_OK) return st;
-  if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
-    return ATTN_ERR_MISALIGNED;
+namespace {
+
+attn_status fwd_impl(const void* Q, const RowStrides& qs, const void* K, const RowStrides& ks, const void* V,
+                     const RowStrides& vs, void* O, const RowStrides& os, float* LSE, int B, int H, int Nq, int Nk,
+                     int d, int causal, float scale, attn_dtype dtype, void* stream) {
   DeviceState* ds = nullptr;
-  if ((st = device_state(&ds)) != ATTN_OK) return st;
+  attn_status st = device_state(&ds);
+  if (st != ATTN_OK) return st;
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));
   const bool bf16 = dtype == ATTN_BF16;
-  const int bh = B * H;
   CUresult r;
-  if ((r = encode_map(&a.tm_q, Q, bf16, bh, Nq, d)) != CUDA_SUCCESS || (r = encode_map(&a.tm_k, K, bf16, bh, Nk, d)) != CUDA_SUCCESS ||
-      (r = encode_map(&a.tm_v, V, bf16, bh, Nk, d)) != CUDA_SUCCESS || (r = encode_map(&a.tm_o, O, bf16, bh, Nq, d)) != CUDA_SUCCESS)
+  if ((r = encode_map(&a.tm_q, Q, bf16, B, H, Nq, d, qs)) != CUDA_SUCCESS ||
+      (r = encode_map(&a.tm_k, K, bf16, B, H, Nk, d, ks)) != CUDA_SUCCESS ||
+      (r = encode_map(&a.tm_v, V, bf16, B, H, Nk, d, vs)) != CUDA_SUCCESS ||
+      (r = encode_map(&a.tm_o, O, bf16, B, H, Nq, d, os)) != CUDA_SUCCESS)
     return driver_fail("cuTensorMapEncodeTiled", r);
   a.lse = LSE;
   a.err_word = ds->err_word;
-  a.bh_count = bh;
+  a.bh_count = B * H;
+  a.heads = H;
   a.Nq = Nq;
   a.Nk = Nk;
   a.d = d;
-  a.causal = causal != 0;
+  a.causal = causal != ATTN_MASK_NONE;
+  a.causal_off = causal_offset(causal, Nq, Nk);
   a.bf16 = bf16;
   a.scale = scale;
   a.timeout_ns = wait_timeout_ns();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return finish(launch_fwd(a, s), s);
+}
+
+}  // namespace
+
+extern "C" attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                                int Nq, int Nk, int d, int causal, float scale, attn_dtype dtype, void* stream) {
+  attn_status st = check_common(B, H, Nq, Nk, d, causal, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+    return ATTN_ERR_MISALIGNED;
+  const RowStrides qs = contiguous(H, Nq, d), ks = contiguous(H, Nk, d);
+  return fwd_impl(Q, qs, K, ks, V, ks, O, qs, LSE, B, H, Nq, Nk, d, causal, scale, dtype, stream);
+}
+
+extern "C" attn_status attn_fwd_strided(const void* Q, attn_strides q_strides, const void* K, attn_strides k_strides,
+                                        const void* V, attn_strides v_strides, void* O, attn_strides o_strides,
+                                        float* LSE, int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                                        attn_dtype dtype, void* stream) {
+  attn_status st = check_common(B, H, Nq, Nk, d, causal, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
+  RowStrides qs, ks, vs, os;
+  if (!normalise_strides(q_strides, B, H, d, &qs) || !normalise_strides(k_strides, B, H, d, &ks) ||
+      !normalise_strides(v_strides, B, H, d, &vs) || !normalise_strides(o_strides, B, H, d, &os))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+    return ATTN_ERR_MISALIGNED;
+  return fwd_impl(Q, qs, K, ks, V, vs, O, os, LSE, B, H, Nq, Nk, d, causal, scale, dtype, stream);
 }
 
 extern "C" size_t attn_bwd_workspace_size(int B, int H, int Nq, int d) {
@@ -179,26 +235,34 @@ extern "C" size_t attn_bwd_workspace_size(int B, int H, int Nq, int d) {
 
 namespace {
 
+// Tensor views of one backward call (element strides; d contiguous).
+struct BwdViews {
+  RowStrides q, k, v, o, dout, dq, dk, dv;
+};
+
 attn_status bwd_steps(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
-                      void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk, int d, int causal, float scale,
-                      attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream, int steps) {
-  attn_status st = check_common(B, H, Nq, Nk, d, scale, dtype);
-  if (st != ATTN_OK) return st;
+                      void* dQ, void* dK, void* dV, const BwdViews& vw, int B, int H, int Nq, int Nk, int d,
+                      int causal, float scale, attn_dtype dtype, void* workspace, size_t workspace_bytes,
+                      void* stream, int steps) {
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < attn_bwd_workspace_size(B, H, Nq, d)) return ATTN_ERR_WORKSPACE;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) || !aligned16(LSE) ||
       !aligned16(dQ) || !aligned16(dK) || !aligned16(dV) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return ATTN_ERR_MISALIGNED;
   DeviceState* ds = nullptr;
-  if ((st = device_state(&ds)) != ATTN_OK) return st;
+  attn_status st = device_state(&ds);
+  if (st != ATTN_OK) return st;
   BwdArgs a;
   std::memset(&a, 0, sizeof(a));
   const bool bf16 = dtype == ATTN_BF16;
   const int bh = B * H;
   CUresult r;
-  if ((r = encode_map(&a.tm_q, Q, bf16, bh, Nq, d)) != CUDA_SUCCESS || (r = encode_map(&a.tm_k, K, bf16, bh, Nk, d)) != CUDA_SUCCESS ||
-      (r = encode_map(&a.tm_v, V, bf16, bh, Nk, d)) != CUDA_SUCCESS || (r = encode_map(&a.tm_do, dO, bf16, bh, Nq, d)) != CUDA_SUCCESS ||
-      (r = encode_map(&a.tm_dk, dK, bf16, bh, Nk, d)) != CUDA_SUCCESS || (r = encode_map(&a.tm_dv, dV, bf16, bh, Nk, d)) != CUDA_SUCCESS)
+  if ((r = encode_map(&a.tm_q, Q, bf16, B, H, Nq, d, vw.q)) != CUDA_SUCCESS ||
+      (r = encode_map(&a.tm_k, K, bf16, B, H, Nk, d, vw.k)) != CUDA_SUCCESS ||
+      (r = encode_map(&a.tm_v, V, bf16, B, H, Nk, d, vw.v)) != CUDA_SUCCESS ||
+      (r = encode_map(&a.tm_do, dO, bf16, B, H, Nq, d, vw.dout)) != CUDA_SUCCESS ||
+      (r = encode_map(&a.tm_dk, dK, bf16, B, H, Nk, d, vw.dk)) != CUDA_SUCCESS ||
+      (r = encode_map(&a.tm_dv, dV, bf16, B, H, Nk, d, vw.dv)) != CUDA_SUCCESS)
     return driver_fail("cuTensorMapEncodeTiled", r);
   const int nq_pad = padded_rows(Nq);
   const size_t rows = static_cast<size_t>(bh) * nq_pad;
@@ -207,21 +271,39 @@ attn_status bwd_steps(const void* Q, const void* K, const void* V, const void* O
   a.dout = dO;
   a.lse = LSE;
   a.dq = dQ;
+  a.so = vw.o;
+  a.sdo = vw.dout;
+  a.sdq = vw.dq;
   a.dq_acc = reinterpret_cast<float*>(ws);
   a.lse2 = reinterpret_cast<float*>(ws + align256(rows * d * sizeof(float)));
   a.dsum = reinterpret_cast<float*>(ws + align256(rows * d * sizeof(float)) + align256(rows * sizeof(float)));
   a.err_word = ds->err_word;
   a.bh_count = bh;
+  a.heads = H;
   a.Nq = Nq;
   a.Nq_pad = nq_pad;
   a.Nk = Nk;
   a.d = d;
-  a.causal = causal != 0;
+  a.causal = causal != ATTN_MASK_NONE;
+  a.causal_off = causal_offset(causal, Nq, Nk);
   a.bf16 = bf16;
   a.scale = scale;
   a.timeout_ns = wait_timeout_ns();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return finish(launch_bwd(a, steps, s), s);
+}
+
+// Contiguous [B][H][N][d] tensors.
+attn_status bwd_contiguous(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                           const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk, int d,
+                           int causal, float scale, attn_dtype dtype, void* workspace, size_t workspace_bytes,
+                           void* stream, int steps) {
+  attn_status st = check_common(B, H, Nq, Nk, d, causal, scale, dtype);
+  if (st != ATTN_OK) return st;
+  const RowStrides qs = contiguous(H, Nq, d), ks = contiguous(H, Nk, d);
+  const BwdViews vw{qs, ks, ks, qs, qs, qs, ks, ks};
+  return bwd_steps(Q, K, V, O, dO, LSE, dQ, dK, dV, vw, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
+                   workspace_bytes, stream, steps);
 }
 
 }  // namespace
@@ -230,7 +312,26 @@ extern "C" attn_status attn_bwd(const void* Q, const void* K, const void* V, con
                                 const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk, int d,
                                 int causal, float scale, attn_dtype dtype, void* workspace, size_t workspace_bytes,
                                 void* stream) {
-  return bwd_steps(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
+  return bwd_contiguous(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
+                        workspace_bytes, stream, kBwdAll);
+}
+
+extern "C" attn_status attn_bwd_strided(const void* Q, attn_strides q_strides, const void* K, attn_strides k_strides,
+                                        const void* V, attn_strides v_strides, const void* O, attn_strides o_strides,
+                                        const void* dO, attn_strides do_strides, const float* LSE, void* dQ,
+                                        attn_strides dq_strides, void* dK, attn_strides dk_strides, void* dV,
+                                        attn_strides dv_strides, int B, int H, int Nq, int Nk, int d, int causal,
+                                        float scale, attn_dtype dtype, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  attn_status st = check_common(B, H, Nq, Nk, d, causal, scale, dtype);
+  if (st != ATTN_OK) return st;
+  BwdViews vw;
+  if (!normalise_strides(q_strides, B, H, d, &vw.q) || !normalise_strides(k_strides, B, H, d, &vw.k) ||
+      !normalise_strides(v_strides, B, H, d, &vw.v) || !normalise_strides(o_strides, B, H, d, &vw.o) ||
+      !normalise_strides(do_strides, B, H, d, &vw.dout) || !normalise_strides(dq_strides, B, H, d, &vw.dq) ||
+      !normalise_strides(dk_strides, B, H, d, &vw.dk) || !normalise_strides(dv_strides, B, H, d, &vw.dv))
+    return ATTN_ERR_INVALID_ARG;
+  return bwd_steps(Q, K, V, O, dO, LSE, dQ, dK, dV, vw, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
                    workspace_bytes, stream, kBwdAll);
 }
 
@@ -238,24 +339,24 @@ extern "C" attn_status attn_bwd_preprocess(const void* Q, const void* K, const v
                                            const void* dO, const float* LSE, void* dQ, void* dK, void* dV, int B,
                                            int H, int Nq, int Nk, int d, int causal, float scale, attn_dtype dtype,
                                            void* workspace, size_t workspace_bytes, void* stream) {
-  return bwd_steps(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
-                   workspace_bytes, stream, kBwdPre);
+  return bwd_contiguous(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
+                        workspace_bytes, stream, kBwdPre);
 }
 
 extern "C" attn_status attn_bwd_kv_blocks(const void* Q, const void* K, const void* V, const void* O,
                                           const void* dO, const float* LSE, void* dQ, void* dK, void* dV, int B,
                                           int H, int Nq, int Nk, int d, int causal, float scale, attn_dtype dtype,
                                           void* workspace, size_t workspace_bytes, void* stream) {
-  return bwd_steps(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
-                   workspace_bytes, stream, kBwdMain);
+  return bwd_contiguous(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
+                        workspace_bytes, stream, kBwdMain);
 }
 
 extern "C" attn_status attn_bwd_dq_convert(const void* Q, const void* K, const void* V, const void* O,
                                            const void* dO, const float* LSE, void* dQ, void* dK, void* dV, int B,
                                            int H, int Nq, int Nk, int d, int causal, float scale, attn_dtype dtype,
                                            void* workspace, size_t workspace_bytes, void* stream) {
-  return bwd_steps(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
-                   workspace_bytes, stream, kBwdConvert);
+  return bwd_contiguous(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
+                        workspace_bytes, stream, kBwdConvert);
 }
 
 extern "C" const char* attn_status_string(attn_status status) {

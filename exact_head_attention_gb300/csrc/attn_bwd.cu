@@ -123,10 +123,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
+  const int head = bh % a.heads, batch = bh / a.heads;
   const int jb = blockIdx.y;  // key block; causal work decreases with jb, so low jb are scheduled first
   const int k0 = jb * kTileRows;
   const int nq_tiles = (a.Nq + kTileRows - 1) / kTileRows;
-  const int i_start = CAUSAL ? jb : 0;
+  // Causal: query q sees key k iff k <= q + coff, so the first query tile to visit holds row k0 - coff.
+  const int coff = CAUSAL ? a.causal_off : 0;
+  const int i_start = CAUSAL ? max(0, k0 - coff) / kTileRows : 0;
   const int n = max(0, nq_tiles - i_start);  // query tiles this block visits
 
   if (threadIdx.x == 0) {
@@ -170,8 +173,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       prefetch_tmap(&a.tm_do);
       mbar_arrive_expect_tx(bars.kv_full(), 2 * C::TILE);
       for (int c = 0; c < C::NCH; ++c) {
-        tma_load_3d(sK + c * kChunkBytes, &a.tm_k, c * 64, k0, bh, bars.kv_full());
-        tma_load_3d(sV + c * kChunkBytes, &a.tm_v, c * 64, k0, bh, bars.kv_full());
+        tma_load_4d(sK + c * kChunkBytes, &a.tm_k, c * 64, k0, head, batch, bars.kv_full());
+        tma_load_4d(sV + c * kChunkBytes, &a.tm_v, c * 64, k0, head, batch, bars.kv_full());
       }
       int issued = 0, issued_rowv = 0;
       for (int L = 0; L < 2 * n; ++L) {
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         const CUtensorMap* map = (L & 1) ? &a.tm_do : &a.tm_q;
         const int q_row = (i_start + (L >> 1)) * kTileRows;
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(sRing + s * C::TILE + c * kChunkBytes, map, c * 64, q_row, bh, bars.ring_full(s));
+          tma_load_4d(sRing + s * C::TILE + c * kChunkBytes, map, c * 64, q_row, head, batch, bars.ring_full(s));
         ++issued;
       }
       if (*abort_flag) {
@@ -377,9 +380,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       mbar_arrive(bars.s_used());
       if (!(ok = mbar_wait_warp(bars.rowv_full(rs), (it >> 1) & 1, wc))) break;
 
-      // P^T = exp2(S^T * scale*log2e - LSE2); masked entries are exactly 0.  Only the causal
-      // diagonal tile and a ragged last key block need the mask: columns below `lo` are zeroed.
-      const bool diag = CAUSAL && (i_start + it == jb);
+      // P^T = exp2(S^T * scale*log2e - LSE2); masked entries are exactly 0.  Only query tiles the
+      // causal diagonal crosses and a ragged last key block need the mask: columns below `lo` are zeroed.
+      const bool diag = CAUSAL && ((i_start + it) * kTileRows + coff < k0 + kTileRows - 1);
       float p[64];
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
@@ -392,7 +395,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         }
       }
       if (diag || ragged_kv) {
-        const int lo = !kv_valid ? 64 : (diag ? kv - qb : 0);
+        const int lo = !kv_valid ? 64 : (diag ? kv - coff - qb : 0);
 #pragma unroll
         for (int col = 0; col < 64; ++col)
           if (col < lo) p[col] = 0.f;
@@ -494,7 +497,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     named_bar_sync(1 + h, 128);
     if (ok && r == 0 && !*abort_flag) {
       const CUtensorMap* map = h ? &a.tm_dk : &a.tm_dv;
-      for (int ch = 0; ch < C::NCH; ++ch) tma_store_3d(map, stage + ch * kChunkBytes, ch * 64, k0, bh);
+      for (int ch = 0; ch < C::NCH; ++ch) tma_store_4d(map, stage + ch * kChunkBytes, ch * 64, k0, head, batch);
       tma_store_commit();
     }
     if (r == 0) tma_store_wait_all();  // this thread's stores and dQ reductions have completed
@@ -508,7 +511,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   }
 }
 
-// D = rowsum(dO o O), LSE2 = LSE * log2(e) (+inf on padding rows), dQacc = 0.
+// D = rowsum(dO o O), LSE2 = LSE * log2(e) (+inf on padding rows and on rows that see no key, so
+// that their recomputed probabilities are exactly 0), dQacc = 0.
 // TPR threads per row, 8 elements (16 bytes) per thread.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ BwdArgs a) {
@@ -522,9 +526,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
   const int q = in_range ? static_cast<int>(row % a.Nq_pad) : a.Nq;
   float acc = 0.f;
   if (in_range && q < a.Nq) {
-    const size_t src = (static_cast<size_t>(bh) * a.Nq + q) * D + sub * 8;
-    const uint4 ov = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.o) + src));
-    const uint4 dv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dout) + src));
+    const long long b = bh / a.heads, h = bh % a.heads;
+    const long long so = b * a.so.b + h * a.so.h + q * a.so.n + sub * 8;
+    const long long sd = b * a.sdo.b + h * a.sdo.h + q * a.sdo.n + sub * 8;
+    const uint4 ov = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.o) + so));
+    const uint4 dv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dout) + sd));
     const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -540,7 +546,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
   z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (sub == 0) {
     if (q < a.Nq) {
-      a.lse2[row] = a.lse[static_cast<size_t>(bh) * a.Nq + q] * 1.4426950408889634f;
+      const float lse = a.lse[static_cast<size_t>(bh) * a.Nq + q];
+      a.lse2[row] = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
       a.dsum[row] = acc;
     } else {
       a.lse2[row] = INFINITY;
@@ -559,6 +566,8 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const __grid_consta
   const int col = static_cast<int>(e % D);
   const size_t bh = row / a.Nq, q = row % a.Nq;
   const float4* src = reinterpret_cast<const float4*>(a.dq_acc + (bh * a.Nq_pad + q) * D + col);
+  const long long b = static_cast<long long>(bh / a.heads), h = static_cast<long long>(bh % a.heads);
+  const long long dst = b * a.sdq.b + h * a.sdq.h + static_cast<long long>(q) * a.sdq.n + col;
   const float4 x = src[0], y = src[1];
   const float s = a.scale;
   uint4 out;
@@ -566,7 +575,7 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const __grid_consta
   out.y = pack2<BF16>(x.z * s, x.w * s);
   out.z = pack2<BF16>(y.x * s, y.y * s);
   out.w = pack2<BF16>(y.z * s, y.w * s);
-  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + e) = out;
+  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + dst) = out;
 }
 
 // steps: bit 0 = preprocess, bit 1 = main, bit 2 = dQ conversion (launched in that order).

@@ -24,8 +24,11 @@
 // back into TMEM, and the MMA warp issues O_t += P_t V_j with P_t read from
 // TMEM.  Issue order S0[0] S1[0] | PV0[j] S0[j+1] PV1[j] S1[j+1] | ... keeps
 // the tensor pipe busy on one tile while the other tile's softmax runs.
-// Causal: key tiles past a query tile's diagonal are skipped entirely and only
-// the diagonal (or ragged last) tile is masked.
+// Causal (query q sees keys k <= q + causal_off: 0 for top-left alignment,
+// Nk - Nq for bottom-right): key tiles past a query tile's diagonal are skipped
+// entirely and only tiles the diagonal crosses (or the ragged last tile) are
+// masked.  A query tile that sees no key at all (bottom-right, Nq > Nk) writes
+// O = 0 and LSE = -inf without touching the tensor pipe.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -169,12 +172,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
+  const int head = bh % a.heads, batch = bh / a.heads;
   const int qb = gridDim.y - 1 - blockIdx.y;  // heaviest (causal) query blocks are scheduled first
   const int q0 = qb * (kFwdSubTiles * kTileRows);
   const int nkv = (a.Nk + kTileRows - 1) / kTileRows;
-  // key tiles visited by query tile 0 / 1 (causal: up to and including the diagonal tile)
-  const int ntile0 = CAUSAL ? min(nkv, q0 / kTileRows + 1) : nkv;
-  const int ntile1 = CAUSAL ? min(nkv, q0 / kTileRows + 2) : nkv;
+  const int coff = CAUSAL ? a.causal_off : 0;
+  // key tiles visited by query tile t (causal: through the tile holding the last key its last row sees)
+  auto tiles_of = [&](int t) {
+    if (!CAUSAL) return nkv;
+    const int last_key = q0 + t * kTileRows + kTileRows - 1 + coff;
+    return last_key < 0 ? 0 : min(nkv, last_key / kTileRows + 1);
+  };
+  const int ntile0 = tiles_of(0), ntile1 = tiles_of(1);  // ntile1 >= ntile0
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
@@ -206,7 +215,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     // ------------------------------------------------------------ control warpgroup
     // warp 8: TMA producer, warp 9: MMA issuer, warps 10-11: idle.
     regs_decrease<kRegsControl>();
-    if (warp == 8 && lane == 0) {
+    if (warp == 8 && lane == 0 && ntile1 > 0) {
       // ---- producer
       prefetch_tmap(&a.tm_q);
       prefetch_tmap(&a.tm_k);
@@ -214,7 +223,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       mbar_arrive_expect_tx(bars.q_full(), 2 * C::TILE);
       for (int t = 0; t < 2; ++t)
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(sQ + t * C::TILE + c * kChunkBytes, &a.tm_q, c * 64, q0 + t * kTileRows, bh, bars.q_full());
+          tma_load_4d(sQ + t * C::TILE + c * kChunkBytes, &a.tm_q, c * 64, q0 + t * kTileRows, head, batch, bars.q_full());
       int issued_k = 0, issued_v = 0;
       for (int j = 0; j < ntile1; ++j) {
         const int s = j % NS;
@@ -222,12 +231,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         if (!mbar_wait(bars.k_empty(s), ph ^ 1, wc)) break;
         mbar_arrive_expect_tx(bars.k_full(s), C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(sK + s * C::TILE + c * kChunkBytes, &a.tm_k, c * 64, j * kTileRows, bh, bars.k_full(s));
+          tma_load_4d(sK + s * C::TILE + c * kChunkBytes, &a.tm_k, c * 64, j * kTileRows, head, batch, bars.k_full(s));
         ++issued_k;
         if (!mbar_wait(bars.v_empty(s), ph ^ 1, wc)) break;
         mbar_arrive_expect_tx(bars.v_full(s), C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(sV + s * C::TILE + c * kChunkBytes, &a.tm_v, c * 64, j * kTileRows, bh, bars.v_full(s));
+          tma_load_4d(sV + s * C::TILE + c * kChunkBytes, &a.tm_v, c * 64, j * kTileRows, head, batch, bars.v_full(s));
         ++issued_v;
       }
       // On abort, every load this thread issued must land before the CTA exits.
@@ -236,7 +245,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         for (int j = max(0, issued_v - NS); j < issued_v; ++j) mbar_drain(bars.v_full(j % NS), (j / NS) & 1, a.timeout_ns);
         mbar_drain(bars.q_full(), 0, a.timeout_ns);
       }
-    } else if (warp == 9 && lane == 0) {
+    } else if (warp == 9 && lane == 0 && ntile1 > 0) {
       // ---- MMA issuer
       constexpr uint32_t idS = idesc_f16(128, 128, BF16, false, false);
       constexpr uint32_t idPV = idesc_f16(128, D, BF16, false, true);
@@ -272,7 +281,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         return true;
       };
 
-      if (ok) ok = issue_S(0, 0);
+      if (ok && ntile0 > 0) ok = issue_S(0, 0);
       if (ok) ok = issue_S(1, 0);
       if (ok) mma_commit(bars.k_empty(0));
       for (int j = 0; ok && j < ntile1; ++j) {
@@ -313,8 +322,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       if (!(ok = mbar_wait_warp(bars.s_full(t), j & 1, wc))) break;
       tc_fence_after();
       // Columns at or past `lim` are masked (ragged last key tile, causal diagonal tile).
-      const bool need_mask = ((j + 1) * kTileRows > a.Nk) || (CAUSAL && j * kTileRows + kTileRows - 1 > q0 + t * kTileRows);
-      const int lim = need_mask ? (CAUSAL ? min(a.Nk, row + 1) : a.Nk) - j * kTileRows : kTileRows;
+      const bool need_mask =
+          ((j + 1) * kTileRows > a.Nk) || (CAUSAL && j * kTileRows + kTileRows - 1 > q0 + t * kTileRows + coff);
+      const int lim = need_mask ? (CAUSAL ? min(a.Nk, row + coff + 1) : a.Nk) - j * kTileRows : kTileRows;
       if (need_mask)
         softmax_tile<D, true, BF16>(tS, tO, lim, c_log2, j == 0, m, l);
       else
@@ -325,20 +335,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok) ok = mbar_wait_warp(bars.o_full(t), 0, wc);
+    // A row that saw no key (l = 0) gets O = 0 and LSE = -inf.  A tile with no key tiles at all
+    // never had its O accumulated; it stages zeros once the Q copy into its staging tile has landed.
+    // (With no key tile anywhere in the block nothing was loaded and there is nothing to wait for.)
+    if (ok && (n > 0 || ntile1 > 0)) ok = mbar_wait_warp(n > 0 ? bars.o_full(t) : bars.q_full(), 0, wc);
     if (ok) {
       tc_fence_after();
-      const float inv_l = 1.0f / l;
-      if (row < a.Nq) a.lse[static_cast<size_t>(bh) * a.Nq + row] = (m + __log2f(l)) * 0.6931471805599453f;
+      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+      if (row < a.Nq)
+        a.lse[static_cast<size_t>(bh) * a.Nq + row] = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
       const uint32_t stage = sQ + t * C::TILE;  // Q_t is dead: all of its MMAs completed before o_full
 #pragma unroll
       for (int ch = 0; ch < C::NCH; ++ch) {
         uint32_t o[2][32];
-        tmem_ld32(tO + ch * 64, o[0]);
-        tmem_ld32(tO + ch * 64 + 32, o[1]);
-        tmem_wait_ld();
-        reg_fence32(o[0]);
-        reg_fence32(o[1]);
+        if (n > 0) {
+          tmem_ld32(tO + ch * 64, o[0]);
+          tmem_ld32(tO + ch * 64 + 32, o[1]);
+          tmem_wait_ld();
+          reg_fence32(o[0]);
+          reg_fence32(o[1]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[0][i] = o[1][i] = 0u;
+        }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const int h = u >> 2, b = (u & 3) * 8;
@@ -354,7 +373,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     named_bar_sync(1 + t, 128);
     if (ok && r == 0 && q0 + t * kTileRows < a.Nq && !*abort_flag) {
       for (int ch = 0; ch < C::NCH; ++ch)
-        tma_store_3d(&a.tm_o, sQ + t * C::TILE + ch * kChunkBytes, ch * 64, q0 + t * kTileRows, bh);
+        tma_store_4d(&a.tm_o, sQ + t * C::TILE + ch * kChunkBytes, ch * 64, q0 + t * kTileRows, head, batch);
       tma_store_commit();
       tma_store_wait_all();
     }

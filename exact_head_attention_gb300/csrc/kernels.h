@@ -12,28 +12,39 @@ namespace exattn {
 constexpr int kTileRows = 128;   // query rows per MMA tile (tcgen05 M) and key rows per K/V tile
 constexpr int kFwdSubTiles = 2;  // query tiles per forward CTA (256 rows)
 
+// Element strides of a [B][H][N][d] view whose d elements are contiguous.
+struct RowStrides {
+  long long b, h, n;
+};
+
+// Causal masks: query q sees keys k <= q + causal_off, where causal_off is 0 (top-left alignment) or
+// Nk - Nq (bottom-right alignment).
+
 struct FwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 3-D maps {d, N, B*H}, box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 4-D maps {d, N, H, B}, box {64, 128, 1, 1}, 128-byte swizzle
   float* lse;                          // [B*H][Nq]
   uint32_t* err_word;
-  int bh_count, Nq, Nk, d;
+  int bh_count, heads, Nq, Nk, d;
   bool causal, bf16;
+  int causal_off;
   float scale;
   uint64_t timeout_ns;
 };
 
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv;
-  const void* o;       // [B*H][Nq][d] 16-bit
-  const void* dout;    // [B*H][Nq][d] 16-bit
+  const void* o;       // [B][H][Nq][d] 16-bit, strides so
+  const void* dout;    // [B][H][Nq][d] 16-bit, strides sdo
   const float* lse;    // [B*H][Nq]
-  void* dq;            // [B*H][Nq][d] 16-bit
+  void* dq;            // [B][H][Nq][d] 16-bit, strides sdq
+  RowStrides so, sdo, sdq;
   float* dq_acc;       // [B*H][Nq_pad][d] fp32 workspace
   float* lse2;         // [B*H][Nq_pad] fp32 workspace: LSE * log2(e), +inf on padding rows
   float* dsum;         // [B*H][Nq_pad] fp32 workspace: rowsum(dO o O), 0 on padding rows
   uint32_t* err_word;
-  int bh_count, Nq, Nq_pad, Nk, d;
+  int bh_count, heads, Nq, Nq_pad, Nk, d;
   bool causal, bf16;
+  int causal_off;
   float scale;
   uint64_t timeout_ns;
 };

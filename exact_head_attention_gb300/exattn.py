@@ -19,11 +19,19 @@ ATTN_OK = 0
 STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_MISALIGNED",
                 4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_TIMEOUT", 6: "ATTN_ERR_WORKSPACE", 7: "ATTN_ERR_NOT_IMPLEMENTED"}
 ATTN_BF16, ATTN_FP16 = 0, 1
+# attn_mask: none, top-left causal (query q sees keys k <= q), bottom-right causal (k <= q + Nk - Nq)
+ATTN_MASK_NONE, ATTN_MASK_CAUSAL, ATTN_MASK_CAUSAL_BOTTOM_RIGHT = 0, 1, 2
+_MASKS = {False: 0, True: 1, 0: 0, 1: 1, 2: 2, "none": 0, "top_left": 1, "bottom_right": 2}
 # attn_bwd is these three C-ABI calls in this order
 BWD_STEPS = ("attn_bwd_preprocess", "attn_bwd_kv_blocks", "attn_bwd_dq_convert")
 
 _lock = threading.Lock()
 _lib = None
+
+
+class Strides(ctypes.Structure):
+    """attn_strides: element strides of a [B][H][N][d] view with contiguous d."""
+    _fields_ = [("batch", ctypes.c_longlong), ("head", ctypes.c_longlong), ("row", ctypes.c_longlong)]
 
 
 class AttnError(RuntimeError):
@@ -50,6 +58,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
             lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
             lib.attn_fwd.restype = i
+            st = Strides
+            lib.attn_fwd_strided.argtypes = [vp, st, vp, st, vp, st, vp, st, vp, i, i, i, i, i, i, f, i, vp]
+            lib.attn_fwd_strided.restype = i
+            lib.attn_bwd_strided.argtypes = [vp, st, vp, st, vp, st, vp, st, vp, st, vp, vp, st, vp, st, vp, st,
+                                             i, i, i, i, i, i, f, i, vp, sz, vp]
+            lib.attn_bwd_strided.restype = i
             lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
             lib.attn_bwd_workspace_size.restype = sz
             for name in ("attn_bwd",) + BWD_STEPS:
@@ -78,12 +92,30 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}; expected bfloat16 or float16")
 
 
+def mask_code(causal) -> int:
+    """attn_mask value of `causal`: False/0/"none", True/1/"top_left", 2/"bottom_right"."""
+    if causal not in _MASKS:
+        raise ValueError(f"unknown causal mask {causal!r}")
+    return _MASKS[causal]
+
+
 def _ptr(t):
     if t is None:
         return None
     if not (t.is_cuda and t.is_contiguous()):
         raise ValueError("tensors must be contiguous CUDA tensors")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _view(t):
+    """(pointer, Strides) of a [B, H, N, d] CUDA tensor whose last dimension is contiguous."""
+    if not t.is_cuda or t.dim() != 4 or t.stride(3) != 1:
+        raise ValueError("tensors must be [B, H, N, d] CUDA tensors with a contiguous last dimension")
+    return ctypes.c_void_p(t.data_ptr()), Strides(t.stride(0), t.stride(1), t.stride(2))
+
+
+def _all_contiguous(*ts) -> bool:
+    return all(t.is_contiguous() for t in ts)
 
 
 def _stream(stream):
@@ -103,20 +135,34 @@ def _check(status: int, where: str):
         raise AttnError(status, where)
 
 
-def fwd_raw(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> int:
-    """Calls attn_fwd on caller-provided tensors; returns the status code."""
+def fwd_raw(q, k, v, o, lse, causal, scale: float, stream=None) -> int:
+    """Calls attn_fwd on caller-provided contiguous tensors; returns the status code."""
     B, H, Nq, Nk, d = _dims(q, k)
-    return load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, int(bool(causal)),
+    return load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, mask_code(causal),
                            float(scale), _dtype_code(q), _stream(stream))
 
 
-def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
-    """O [B,H,Nq,d] (dtype of q) and LSE [B,H,Nq] fp32."""
+def fwd_strided_raw(q, k, v, o, lse, causal, scale: float, stream=None) -> int:
+    """Calls attn_fwd_strided with each tensor's own strides; returns the status code."""
+    B, H, Nq, Nk, d = _dims(q, k)
+    return load().attn_fwd_strided(*_view(q), *_view(k), *_view(v), *_view(o), _ptr(lse), B, H, Nq, Nk, d,
+                                   mask_code(causal), float(scale), _dtype_code(q), _stream(stream))
+
+
+def forward(q, k, v, causal=False, scale: float | None = None, stream=None):
+    """O [B,H,Nq,d] (dtype and, where dense, strides of q) and LSE [B,H,Nq] fp32.
+
+    `causal`: False, True (top-left) or "bottom_right".  Non-contiguous views whose last
+    dimension is contiguous (e.g. [B, N, H, d] storage seen as [B, H, N, d]) go through
+    attn_fwd_strided without a copy."""
     B, H, Nq, Nk, d = _dims(q, k)
     scale = (1.0 / d ** 0.5) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    _check(fwd_raw(q, k, v, o, lse, causal, scale, stream), "attn_fwd")
+    if _all_contiguous(q, k, v, o):
+        _check(fwd_raw(q, k, v, o, lse, causal, scale, stream), "attn_fwd")
+    else:
+        _check(fwd_strided_raw(q, k, v, o, lse, causal, scale, stream), "attn_fwd_strided")
     return o, lse
 
 
@@ -124,25 +170,43 @@ def workspace_size(B: int, H: int, Nq: int, d: int) -> int:
     return int(load().attn_bwd_workspace_size(B, H, Nq, d))
 
 
-def bwd_raw(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, workspace, stream=None,
-            step: str = "attn_bwd") -> int:
-    """Calls attn_bwd (or one of BWD_STEPS) on caller-provided tensors; returns the status code."""
-    B, H, Nq, Nk, d = _dims(q, k)
+def _workspace(workspace):
     ws_ptr = None if workspace is None else ctypes.c_void_p(workspace.data_ptr())
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return ws_ptr, ws_bytes
+
+
+def bwd_raw(q, k, v, o, do, lse, dq, dk, dv, causal, scale: float, workspace, stream=None,
+            step: str = "attn_bwd") -> int:
+    """Calls attn_bwd (or one of BWD_STEPS) on caller-provided contiguous tensors; returns the status code."""
+    B, H, Nq, Nk, d = _dims(q, k)
     fn = getattr(load(), step)
     return fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-              B, H, Nq, Nk, d, int(bool(causal)), float(scale), _dtype_code(q), ws_ptr, ws_bytes, _stream(stream))
+              B, H, Nq, Nk, d, mask_code(causal), float(scale), _dtype_code(q), *_workspace(workspace),
+              _stream(stream))
 
 
-def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None, workspace=None, stream=None):
-    """(dQ, dK, dV) for the loss sum(O * dO).  `workspace` (uint8 CUDA tensor) is allocated if omitted."""
+def bwd_strided_raw(q, k, v, o, do, lse, dq, dk, dv, causal, scale: float, workspace, stream=None) -> int:
+    """Calls attn_bwd_strided with each tensor's own strides; returns the status code."""
+    B, H, Nq, Nk, d = _dims(q, k)
+    return load().attn_bwd_strided(*_view(q), *_view(k), *_view(v), *_view(o), *_view(do), _ptr(lse),
+                                   *_view(dq), *_view(dk), *_view(dv), B, H, Nq, Nk, d, mask_code(causal),
+                                   float(scale), _dtype_code(q), *_workspace(workspace), _stream(stream))
+
+
+def backward(q, k, v, o, do, lse, causal=False, scale: float | None = None, workspace=None, stream=None):
+    """(dQ, dK, dV) for the loss sum(O * dO).  `workspace` (uint8 CUDA tensor) is allocated if omitted.
+    Gradients take the strides of q, k, v where those are dense; views go through attn_bwd_strided."""
     B, H, Nq, Nk, d = _dims(q, k)
     scale = (1.0 / d ** 0.5) if scale is None else scale
     if workspace is None:
         workspace = torch.empty(workspace_size(B, H, Nq, d), dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    _check(bwd_raw(q, k, v, o, do, lse, dq, dk, dv, causal, scale, workspace, stream), "attn_bwd")
+    if _all_contiguous(q, k, v, o, do, dq, dk, dv):
+        _check(bwd_raw(q, k, v, o, do, lse, dq, dk, dv, causal, scale, workspace, stream), "attn_bwd")
+    else:
+        _check(bwd_strided_raw(q, k, v, o, do, lse, dq, dk, dv, causal, scale, workspace, stream),
+               "attn_bwd_strided")
     return dq, dk, dv
 
 
@@ -162,11 +226,13 @@ class _AttnFunction(torch.autograd.Function):
     @staticmethod
     def backward(ctx, do):
         q, k, v, o, lse = ctx.saved_tensors
-        dq, dk, dv = backward(q, k, v, o, do.contiguous(), lse, ctx.causal, ctx.scale)
+        if do.stride(-1) != 1:
+            do = do.contiguous()
+        dq, dk, dv = backward(q, k, v, o, do, lse, ctx.causal, ctx.scale)
         return dq, dk, dv, None, None
 
 
-def attention(q, k, v, causal: bool = False, scale: float | None = None):
-    """Autograd-aware exact attention over [B, H, N, d] tensors."""
+def attention(q, k, v, causal=False, scale: float | None = None):
+    """Autograd-aware exact attention over [B, H, N, d] tensors (causal: False, True or "bottom_right")."""
     scale = (1.0 / q.shape[-1] ** 0.5) if scale is None else scale
     return _AttnFunction.apply(q, k, v, causal, scale)

@@ -33,7 +33,7 @@ class Workload:
     Nk: int
     d: int
     dtype: str          # "bf16" | "fp16"
-    causal: bool
+    causal: bool | str  # False, True (top-left) or "bottom_right"
     sigma_qk: float = 1.0
     sigma_v: float = 1.0
     sigma_do: float = 1.0
@@ -90,8 +90,9 @@ def make_inputs(w: Workload, seed_offset: int = 0, with_grad_out: bool = True) -
     return out
 
 
-def custom(B: int, H: int, Nq: int, Nk: int, d: int, dtype: str = "bf16", causal: bool = False,
+def custom(B: int, H: int, Nq: int, Nk: int, d: int, dtype: str = "bf16", causal: bool | str = False,
            index: int = 7, sigma_qk: float = 1.0) -> Workload:
     """An ad-hoc workload (ragged and edge-case shapes in the tests)."""
-    name = f"custom_B{B}_H{H}_q{Nq}_k{Nk}_d{d}_{dtype}_{'c' if causal else 'nc'}"
+    mask = "br" if causal == "bottom_right" else ("c" if causal else "nc")
+    name = f"custom_B{B}_H{H}_q{Nq}_k{Nk}_d{d}_{dtype}_{mask}"
     return Workload(name, index, B, H, Nq, Nk, d, dtype, causal, sigma_qk=sigma_qk)

@@ -3,11 +3,13 @@
  * GB300 GPU (sm_103a).  Plain C ABI: device pointers, sizes and a stream; no
  * framework types.
  *
- * What is computed (per batch b and head h, all tensors contiguous row-major):
+ * What is computed (per batch b and head h):
  *   S = scale * Q K^T                         [Nq x Nk]
- *   S_qk = -inf where causal and k > q         (top-left aligned mask)
+ *   S_qk = -inf where the causal mask hides k from q (see attn_mask)
  *   P = softmax_row(S),  O = P V              [Nq x d]
  *   LSE_q = ln sum_k exp(S_qk)                 (natural log, scaled scores)
+ * A query row that sees no key (only possible with the bottom-right mask and
+ * Nq > Nk) gets O = 0, LSE = -inf and zero gradients.
  * -- SparkAttention (arXiv 2502.12784), Equation 1 and the masked decoder MHA
  * of Figure 1; CANN ops-transformer MHA article, section 1 (scale 1/sqrt(d_k)).
  * The score matrix never reaches global memory: the forward is tiled with an
@@ -15,10 +17,11 @@
  * parallel over batch x heads x query-row blocks ("Fast Transformer training
  * with long sequences", attention parallelism section).
  *
- * Layouts:
- *   Q, O, dO, dQ : [B][H][Nq][d]   16-bit (bf16 or fp16, see attn_dtype)
- *   K, V, dK, dV : [B][H][Nk][d]   16-bit
- *   LSE          : [B][H][Nq]      fp32
+ * Layouts (the plain entry points; the *_strided ones take any strides, see
+ * attn_strides):
+ *   Q, O, dO, dQ : [B][H][Nq][d]   16-bit (bf16 or fp16, see attn_dtype), contiguous
+ *   K, V, dK, dV : [B][H][Nk][d]   16-bit, contiguous
+ *   LSE          : [B][H][Nq]      fp32, contiguous (always)
  * All pointers are device pointers owned by the caller and must be 16-byte
  * aligned.  d must be 64 or 128.  All arithmetic accumulates in fp32; outputs
  * are rounded to nearest even into the input dtype.
@@ -42,7 +45,7 @@ extern "C" {
 
 typedef enum {
   ATTN_OK = 0,
-  ATTN_ERR_INVALID_ARG = 1,     /* null pointer, non-positive size, bad scale, bad dtype */
+  ATTN_ERR_INVALID_ARG = 1,     /* null pointer, non-positive size, bad scale, dtype, mask or strides */
   ATTN_ERR_UNSUPPORTED = 2,     /* d not in {64, 128}, or no sm_103a device */
   ATTN_ERR_MISALIGNED = 3,      /* a pointer is not 16-byte aligned */
   ATTN_ERR_CUDA = 4,            /* a CUDA runtime/driver call or launch failed */
@@ -54,10 +57,47 @@ typedef enum {
 typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1 } attn_dtype;
 
 /*
+ * Values of the `causal` argument (any other value is ATTN_ERR_INVALID_ARG).
+ *   ATTN_MASK_NONE                 every query sees every key.
+ *   ATTN_MASK_CAUSAL               top-left alignment: query q sees keys k <= q.
+ *   ATTN_MASK_CAUSAL_BOTTOM_RIGHT  the Nq queries are the last Nq positions of
+ *                                  the Nk-long sequence (a decoder continuing a
+ *                                  cached prefix): query q sees keys
+ *                                  k <= q + Nk - Nq.
+ * Both causal forms are the masked decoder self-attention of SparkAttention
+ * Figure 1 (a position attends to itself and the positions before it); they
+ * differ only when Nq != Nk.
+ */
+typedef enum {
+  ATTN_MASK_NONE = 0,
+  ATTN_MASK_CAUSAL = 1,
+  ATTN_MASK_CAUSAL_BOTTOM_RIGHT = 2
+} attn_mask;
+
+/*
+ * Element strides of a 16-bit [B][H][N][d] view whose d elements are
+ * contiguous (stride 1): element (b, h, n, c) is at
+ * base + b*batch + h*head + n*row + c.
+ *   contiguous [B][H][N][d]:          {H*N*d, N*d, d}
+ *   [B][N][H][d] (rows of [S, H*D]):  {N*H*d, d, H*d}
+ * Rules (ATTN_ERR_INVALID_ARG otherwise): row >= d; every stride a positive
+ * multiple of 8 elements (16 bytes, a tensor-copy requirement) below 2^39;
+ * the stride of a dimension of extent 1 is ignored.  Outputs must not overlap
+ * one another or any input.  The CANN ops-transformer MHA article, section 1,
+ * stores attention inputs as [S, H*D] rows; this struct admits that layout
+ * and the per-head [N][d] matrices alike.
+ */
+typedef struct attn_strides {
+  long long batch;
+  long long head;
+  long long row;
+} attn_strides;
+
+/*
  * Forward.  Writes O and LSE.
  *   Q [B,H,Nq,d], K [B,H,Nk,d], V [B,H,Nk,d] inputs; O [B,H,Nq,d] and
- *   LSE [B,H,Nq] (fp32) outputs.  causal != 0 applies the top-left mask
- *   (query q sees keys k <= q).  scale > 0 and finite multiplies Q K^T.
+ *   LSE [B,H,Nq] (fp32) outputs.  causal is an attn_mask value.  scale > 0
+ *   and finite multiplies Q K^T.
  * Tiling, online softmax and per-block output as in SparkAttention Figure 6
  * (read Q once, stream K/V tiles, write O once); LSE is the saved row
  * statistic of the StreamKL summary, Methodology 1-2 (LSE = m + log l).
@@ -65,6 +105,17 @@ typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1 } attn_dtype;
 attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                      int B, int H, int Nq, int Nk, int d, int causal, float scale,
                      attn_dtype dtype, void* stream);
+
+/*
+ * attn_fwd on strided views: each 16-bit tensor comes with its attn_strides
+ * (Q and O over Nq rows, K and V over Nk rows).  LSE stays contiguous
+ * [B][H][Nq].  Same results and errors as attn_fwd, plus ATTN_ERR_INVALID_ARG
+ * for strides that break the attn_strides rules.
+ */
+attn_status attn_fwd_strided(const void* Q, attn_strides q_strides, const void* K, attn_strides k_strides,
+                             const void* V, attn_strides v_strides, void* O, attn_strides o_strides,
+                             float* LSE, int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                             attn_dtype dtype, void* stream);
 
 /*
  * Bytes of device workspace attn_bwd needs for this shape: an fp32 dQ
@@ -93,6 +144,20 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
                      const float* LSE, void* dQ, void* dK, void* dV,
                      int B, int H, int Nq, int Nk, int d, int causal, float scale,
                      attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_bwd on strided views (see attn_strides): Q, O, dO, dQ over Nq rows,
+ * K, V, dK, dV over Nk rows; LSE contiguous [B][H][Nq]; the workspace as for
+ * attn_bwd.  Same results and errors as attn_bwd, plus ATTN_ERR_INVALID_ARG
+ * for strides that break the attn_strides rules.
+ */
+attn_status attn_bwd_strided(const void* Q, attn_strides q_strides, const void* K, attn_strides k_strides,
+                             const void* V, attn_strides v_strides, const void* O, attn_strides o_strides,
+                             const void* dO, attn_strides do_strides, const float* LSE, void* dQ,
+                             attn_strides dq_strides, void* dK, attn_strides dk_strides, void* dV,
+                             attn_strides dv_strides, int B, int H, int Nq, int Nk, int d, int causal,
+                             float scale, attn_dtype dtype, void* workspace, size_t workspace_bytes,
+                             void* stream);
 
 /*
  * The three steps attn_bwd launches, callable one at a time (same arguments

@@ -44,6 +44,12 @@ def rel_l2(a, b) -> float:
 
 
 def check_fwd(w, got_o, got_lse, ref_o, ref_lse, what=""):
+    # Rows that see no key (bottom-right mask, Nq > Nk): exactly O = 0 and LSE = -inf.
+    empty = np.isneginf(ref_lse)
+    if empty.any():
+        assert np.isneginf(got_lse[empty]).all(), f"{what}: LSE of rows without keys is not -inf"
+        assert (got_o[empty] == 0).all(), f"{what}: O of rows without keys is not 0"
+        got_o, got_lse, ref_o, ref_lse = got_o[~empty], got_lse[~empty], ref_o[~empty], ref_lse[~empty]
     err_o = float(np.abs(got_o - ref_o).max()) if ref_o.size else 0.0
     err_l = float(np.abs(got_lse - ref_lse).max()) if ref_lse.size else 0.0
     assert np.isfinite(got_o).all() and np.isfinite(got_lse).all(), f"{what}: non-finite output"

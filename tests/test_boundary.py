@@ -85,3 +85,47 @@ def test_bwd_rejects_bad_arguments(lib):
     assert _bwd(lib, ws_bytes=100) == 6
     assert _bwd(lib, ptrs=[FAKE] * 6 + [FAKE + 2] + [FAKE] * 2) == 3
     assert _bwd(lib, ws=FAKE + 16) == 3  # workspace must be 256-byte aligned
+
+
+@pytest.mark.parametrize("causal,code", [(3, 1), (-1, 1), (100, 1)])
+def test_rejects_unknown_mask(lib, causal, code):
+    assert _fwd(lib, causal=causal) == code
+    p = [ctypes.c_void_p(FAKE)] * 9
+    need = lib.attn_bwd_workspace_size(1, 1, 128, 64)
+    assert lib.attn_bwd(*p, 1, 1, 128, 128, 64, causal, 0.125, 0, ctypes.c_void_p(FAKE), need, None) == code
+
+
+def _strided_fwd(lib, strides, B=2, H=3, Nq=128, Nk=128, d=64, causal=0, lse=FAKE + 4):
+    # The LSE pointer is misaligned on purpose: a call that passes every other check stops there
+    # (ATTN_ERR_MISALIGNED, after the stride checks) and never launches on the fake pointers.
+    from exact_head_attention_gb300.exattn import Strides
+    args = []
+    for st in strides:
+        args += [ctypes.c_void_p(FAKE), Strides(*st)]
+    return lib.attn_fwd_strided(*args, ctypes.c_void_p(lse), B, H, Nq, Nk, d, causal, 0.125, 0, None)
+
+
+@pytest.mark.parametrize("bad", [
+    (3 * 128 * 64, 128 * 64, 32),         # row stride below d
+    (3 * 128 * 64, 128 * 64, 68),         # row stride not a multiple of 8 elements
+    (3 * 128 * 64, 100, 64),              # head stride not a multiple of 8
+    (0, 128 * 64, 64),                    # zero batch stride with B > 1
+    (3 * 128 * 64, -128 * 64, 64),        # negative head stride
+    (1 << 40, 128 * 64, 64),              # byte stride beyond 2^40
+])
+def test_strided_rejects_bad_strides(lib, bad):
+    good = (3 * 128 * 64, 128 * 64, 64)
+    for i in range(4):
+        strides = [good] * 4
+        strides[i] = bad
+        assert _strided_fwd(lib, strides) == 1, (i, bad)
+
+
+def test_strided_accepts_valid_layouts(lib):
+    B, H, N, d = 2, 3, 128, 64
+    bhnd, bnhd = (H * N * d, N * d, d), (N * H * d, d, H * d)
+    assert _strided_fwd(lib, [bhnd] * 4) == 3
+    assert _strided_fwd(lib, [bnhd] * 4) == 3
+    assert _strided_fwd(lib, [bnhd, bhnd, bnhd, bhnd]) == 3
+    # B = H = 1: the batch and head strides address nothing and are not checked
+    assert _strided_fwd(lib, [(0, 0, 64)] * 4, B=1, H=1) == 3
