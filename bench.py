@@ -219,7 +219,7 @@ def traffic_from_profile(kernel_key: str) -> float | None:
 
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for f in ("attn_fwd.cu", "attn_bwd.cu", "ptx.cuh", "kernels.h"):
+    for f in ("attn_fwd.cu", "attn_bwd.cu", "ptx.cuh", "kernels.h", "softmax.cuh"):
         h.update(open(os.path.join(ROOT, "exact_head_attention_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 

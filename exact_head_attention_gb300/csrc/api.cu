@@ -1,5 +1,6 @@
 // C-ABI entry points declared in include/exattn.h: argument validation,
 // TMA tensor-map encoding, the per-device error word and kernel dispatch.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -399,3 +400,140 @@ extern "C" attn_status attn_check_device_error(void* stream) {
 extern "C" const char* attn_last_error(void) { return g_last_error; }
 
 void exattn::set_last_error(const char* msg) { std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+
+// ----------------------------------------------------------------- split-KV forward
+
+namespace {
+
+constexpr int kMaxSplits = 256;
+
+// Slices per query tile that minimise (waves of CTAs) x (key tiles per CTA + one tile of fixed cost),
+// with one slice CTA resident per SM.  1 means the plain forward is the better launch, which is always
+// the case once the query tiles alone fill the SMs.
+int choose_splits(long long bh, int Nq, int Nk, int sm_count) {
+  const long long base = bh * ((Nq + kTileRows - 1) / kTileRows);
+  const int nkv = (Nk + kTileRows - 1) / kTileRows;
+  if (base >= sm_count) return 1;
+  int best = 1;
+  double best_cost = 0.0;
+  for (int s = 1; s <= std::min(nkv, kMaxSplits); ++s) {
+    const long long waves = (base * s + sm_count - 1) / sm_count;
+    const double cost = static_cast<double>(waves) * ((nkv + s - 1) / s + 1);
+    if (s == 1 || cost < best_cost * 0.98) {  // a split must win clearly: it adds a merge pass
+      best = s;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+int device_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return sms;
+}
+
+size_t split_workspace(int B, int H, int Nq, int d, int splits) {
+  const size_t rows = static_cast<size_t>(splits) * B * H * Nq;
+  return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+attn_status fwd_split_impl(const void* Q, const RowStrides& qs, const void* K, const RowStrides& ks, const void* V,
+                           const RowStrides& vs, void* O, const RowStrides& os, float* LSE, int B, int H, int Nq,
+                           int Nk, int d, int causal, float scale, attn_dtype dtype, int num_splits,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  if (num_splits < 0 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  if ((Nq + kTileRows - 1) / kTileRows > 65535 || static_cast<long long>(B) * H * Nq / 8 >= 0x7fffffffLL)
+    return ATTN_ERR_INVALID_ARG;
+  if (num_splits == 0) {
+    int sms = device_sm_count();
+    num_splits = choose_splits(static_cast<long long>(B) * H, Nq, Nk, sms > 0 ? sms : 1);
+    if (num_splits == 1) return fwd_impl(Q, qs, K, ks, V, vs, O, os, LSE, B, H, Nq, Nk, d, causal, scale, dtype, stream);
+  }
+  if (!workspace || workspace_bytes < split_workspace(B, H, Nq, d, num_splits)) return ATTN_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  attn_status st = device_state(&ds);
+  if (st != ATTN_OK) return st;
+  SplitArgs a;
+  std::memset(&a, 0, sizeof(a));
+  const bool bf16 = dtype == ATTN_BF16;
+  CUresult r;
+  if ((r = encode_map(&a.tm_q, Q, bf16, B, H, Nq, d, qs)) != CUDA_SUCCESS ||
+      (r = encode_map(&a.tm_k, K, bf16, B, H, Nk, d, ks)) != CUDA_SUCCESS ||
+      (r = encode_map(&a.tm_v, V, bf16, B, H, Nk, d, vs)) != CUDA_SUCCESS)
+    return driver_fail("cuTensorMapEncodeTiled", r);
+  const size_t rows = static_cast<size_t>(num_splits) * B * H * Nq;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.o_part = reinterpret_cast<float*>(ws);
+  a.l_part = reinterpret_cast<float*>(ws + align256(rows * d * sizeof(float)));
+  a.o = O;
+  a.so = os;
+  a.lse = LSE;
+  a.err_word = ds->err_word;
+  a.bh_count = B * H;
+  a.heads = H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.splits = num_splits;
+  a.causal = causal != ATTN_MASK_NONE;
+  a.causal_off = causal_offset(causal, Nq, Nk);
+  a.bf16 = bf16;
+  a.scale = scale;
+  a.timeout_ns = wait_timeout_ns();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return finish(launch_fwd_split(a, s), s);
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int d, int sm_count) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return 0;
+  if (sm_count <= 0) sm_count = device_sm_count();
+  if (sm_count <= 0) return 0;
+  return choose_splits(static_cast<long long>(B) * H, Nq, Nk, sm_count);
+}
+
+extern "C" size_t attn_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128) || num_splits < 0 || num_splits > kMaxSplits)
+    return 0;
+  if (num_splits == 0) {
+    num_splits = attn_fwd_splitkv_num_splits(B, H, Nq, Nk, d, 0);
+    if (num_splits <= 1) return 0;
+  }
+  return split_workspace(B, H, Nq, d, num_splits);
+}
+
+extern "C" attn_status attn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                                        int Nq, int Nk, int d, int causal, float scale, attn_dtype dtype,
+                                        int num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  attn_status st = check_common(B, H, Nq, Nk, d, causal, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+    return ATTN_ERR_MISALIGNED;
+  const RowStrides qs = contiguous(H, Nq, d), ks = contiguous(H, Nk, d);
+  return fwd_split_impl(Q, qs, K, ks, V, ks, O, qs, LSE, B, H, Nq, Nk, d, causal, scale, dtype, num_splits,
+                        workspace, workspace_bytes, stream);
+}
+
+extern "C" attn_status attn_fwd_splitkv_strided(const void* Q, attn_strides q_strides, const void* K,
+                                                attn_strides k_strides, const void* V, attn_strides v_strides,
+                                                void* O, attn_strides o_strides, float* LSE, int B, int H, int Nq,
+                                                int Nk, int d, int causal, float scale, attn_dtype dtype,
+                                                int num_splits, void* workspace, size_t workspace_bytes,
+                                                void* stream) {
+  attn_status st = check_common(B, H, Nq, Nk, d, causal, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
+  RowStrides qs, ks, vs, os;
+  if (!normalise_strides(q_strides, B, H, d, &qs) || !normalise_strides(k_strides, B, H, d, &ks) ||
+      !normalise_strides(v_strides, B, H, d, &vs) || !normalise_strides(o_strides, B, H, d, &os))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+    return ATTN_ERR_MISALIGNED;
+  return fwd_split_impl(Q, qs, K, ks, V, vs, O, os, LSE, B, H, Nq, Nk, d, causal, scale, dtype, num_splits,
+                        workspace, workspace_bytes, stream);
+}

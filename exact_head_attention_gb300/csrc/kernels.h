@@ -49,6 +49,23 @@ struct BwdArgs {
   uint64_t timeout_ns;
 };
 
+// Split-KV forward: each CTA covers one 128-row query tile and one contiguous slice of the key tiles
+// it sees; a second kernel merges the slices' partial results by their LSE.
+struct SplitArgs {
+  CUtensorMap tm_q, tm_k, tm_v;  // as in FwdArgs
+  float* o_part;                 // [splits][B*H][Nq][d] fp32: O of each slice, normalised by its own sum
+  float* l_part;                 // [splits][B*H][Nq] fp32: base-2 LSE of each slice (-inf: no key seen)
+  void* o;                       // merged O, 16-bit, strides so
+  RowStrides so;
+  float* lse;                    // [B*H][Nq], natural log
+  uint32_t* err_word;
+  int bh_count, heads, Nq, Nk, d, splits;
+  bool causal, bf16;
+  int causal_off;
+  float scale;
+  uint64_t timeout_ns;
+};
+
 // Backward steps (bit mask for launch_bwd).
 constexpr int kBwdPre = 1, kBwdMain = 2, kBwdConvert = 4, kBwdAll = 7;
 
@@ -57,6 +74,7 @@ void set_last_error(const char* msg);
 
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_fwd_split(const SplitArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, int steps, cudaStream_t stream);
 
 }  // namespace exattn

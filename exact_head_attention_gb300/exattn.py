@@ -64,6 +64,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_bwd_strided.argtypes = [vp, st, vp, st, vp, st, vp, st, vp, st, vp, vp, st, vp, st, vp, st,
                                              i, i, i, i, i, i, f, i, vp, sz, vp]
             lib.attn_bwd_strided.restype = i
+            lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, sz, vp]
+            lib.attn_fwd_splitkv.restype = i
+            lib.attn_fwd_splitkv_strided.argtypes = [vp, st, vp, st, vp, st, vp, st, vp, i, i, i, i, i, i, f, i, i, vp,
+                                                     sz, vp]
+            lib.attn_fwd_splitkv_strided.restype = i
+            lib.attn_fwd_splitkv_num_splits.argtypes = [i, i, i, i, i, i]
+            lib.attn_fwd_splitkv_num_splits.restype = i
+            lib.attn_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i, i]
+            lib.attn_fwd_splitkv_workspace_size.restype = sz
             lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
             lib.attn_bwd_workspace_size.restype = sz
             for name in ("attn_bwd",) + BWD_STEPS:
@@ -163,6 +172,39 @@ def forward(q, k, v, causal=False, scale: float | None = None, stream=None):
         _check(fwd_raw(q, k, v, o, lse, causal, scale, stream), "attn_fwd")
     else:
         _check(fwd_strided_raw(q, k, v, o, lse, causal, scale, stream), "attn_fwd_strided")
+    return o, lse
+
+
+def splitkv_num_splits(B: int, H: int, Nq: int, Nk: int, d: int, sm_count: int = 0) -> int:
+    """Slices per query tile attn_fwd_splitkv picks for num_splits = 0 (sm_count 0: the current device)."""
+    return int(load().attn_fwd_splitkv_num_splits(B, H, Nq, Nk, d, sm_count))
+
+
+def splitkv_workspace_size(B: int, H: int, Nq: int, Nk: int, d: int, num_splits: int = 0) -> int:
+    return int(load().attn_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, num_splits))
+
+
+def fwd_splitkv_raw(q, k, v, o, lse, causal, scale: float, num_splits: int, workspace, stream=None) -> int:
+    """Calls attn_fwd_splitkv (contiguous tensors) or attn_fwd_splitkv_strided; returns the status code."""
+    B, H, Nq, Nk, d = _dims(q, k)
+    common = (B, H, Nq, Nk, d, mask_code(causal), float(scale), _dtype_code(q), int(num_splits),
+              *_workspace(workspace), _stream(stream))
+    if _all_contiguous(q, k, v, o):
+        return load().attn_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), *common)
+    return load().attn_fwd_splitkv_strided(*_view(q), *_view(k), *_view(v), *_view(o), _ptr(lse), *common)
+
+
+def forward_splitkv(q, k, v, causal=False, scale: float | None = None, num_splits: int = 0, stream=None):
+    """forward() for few query rows with the key dimension divided across blocks (decoding).
+
+    num_splits = 0 lets the library choose (possibly 1, i.e. the plain forward)."""
+    B, H, Nq, Nk, d = _dims(q, k)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    ws_bytes = splitkv_workspace_size(B, H, Nq, Nk, d, num_splits)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device) if ws_bytes else None
+    _check(fwd_splitkv_raw(q, k, v, o, lse, causal, scale, num_splits, ws, stream), "attn_fwd_splitkv")
     return o, lse
 
 

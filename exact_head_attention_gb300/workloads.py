@@ -14,6 +14,11 @@ The workloads are the long-sequence / small-batch regime of "Fast Transformer
 training with long sequences" (attention layer benchmark: H = 12, d = 128,
 sequence 8k) and the encoder-decoder MHA of SparkAttention (arXiv 2502.12784),
 Figure 1 (masked decoder self-attention and encoder-decoder cross-attention).
+The two decoding workloads are the small-query regime the StreamKL summary
+names for its split-K variant (autoregressive decoding, N_Q = 1, long
+contexts): one new token, or a chunk of 64, attending to a long cache with the
+bottom-right causal mask, on the heads of the 8k benchmark (H = 12, d = 128)
+and of the SparkAttention decoder (H = 16, d = 64).
 """
 from __future__ import annotations
 
@@ -50,7 +55,8 @@ class Workload:
         return dataclasses.replace(self, **kw)
 
 
-# The five workload families (two have a causal and a non-causal / d variant).
+# The five training workload families (two have a causal and a non-causal / d variant) and two
+# decoding workloads.
 WORKLOADS = {
     "tiny_fp16": Workload("tiny_fp16", 1, 1, 2, 128, 128, 64, "fp16", False),
     "self1k_bf16": Workload("self1k_bf16", 2, 8, 16, 1024, 1024, 64, "bf16", False),
@@ -61,6 +67,11 @@ WORKLOADS = {
                                    sigma_qk=1.5),
     "ctx32k_d128_causal_bf16": Workload("ctx32k_d128_causal_bf16", 5, 1, 8, 32768, 32768, 128, "bf16", True),
     "ctx32k_d64_causal_bf16": Workload("ctx32k_d64_causal_bf16", 5, 1, 8, 32768, 32768, 64, "bf16", True),
+    # decoding (split-KV forward)
+    "decode_q1_kv32k_d128_bf16": Workload("decode_q1_kv32k_d128_bf16", 6, 8, 12, 1, 32768, 128, "bf16",
+                                          "bottom_right"),
+    "chunk_q64_kv16k_d64_fp16": Workload("chunk_q64_kv16k_d64_fp16", 8, 4, 16, 64, 16384, 64, "fp16",
+                                         "bottom_right"),
 }
 
 # The workload the throughput metric is quoted on.

@@ -118,6 +118,53 @@ attn_status attn_fwd_strided(const void* Q, attn_strides q_strides, const void* 
                              attn_dtype dtype, void* stream);
 
 /*
+ * Split-KV forward for few query rows (autoregressive decoding: Nq = 1 up to a
+ * few hundred).  Same inputs, outputs, masks and results as attn_fwd (exact up
+ * to fp32 rounding order).  With few query rows the plain forward has only
+ * B*H*ceil(Nq/256) blocks of work; here the key dimension is also divided across
+ * blocks (the "Split-K variant" of the StreamKL summary, GPU kernel
+ * optimisations): block (b*H+h, query tile, s) runs the online softmax of one
+ * 128-row query tile over the s-th contiguous slice of the key tiles it sees,
+ * and a second kernel merges the slices of each row by their log-sum-exp:
+ *   LSE = ln sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s.
+ * num_splits: 1..256 slices per query tile, or 0 to let the library choose
+ * (attn_fwd_splitkv_num_splits); when it chooses 1 this is exactly attn_fwd
+ * and needs no workspace.  workspace: at least
+ * attn_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, num_splits) bytes of device
+ * memory, 256-byte aligned, contents on entry irrelevant (fp32 partial O and
+ * LSE of every slice).  Errors as attn_fwd, plus ATTN_ERR_INVALID_ARG for
+ * num_splits outside [0, 256] and ATTN_ERR_WORKSPACE for a missing or small
+ * workspace.
+ */
+attn_status attn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                             int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                             attn_dtype dtype, int num_splits, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* attn_fwd_splitkv on strided views (see attn_strides and attn_fwd_strided). */
+attn_status attn_fwd_splitkv_strided(const void* Q, attn_strides q_strides, const void* K, attn_strides k_strides,
+                                     const void* V, attn_strides v_strides, void* O, attn_strides o_strides,
+                                     float* LSE, int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                                     attn_dtype dtype, int num_splits, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/*
+ * The number of slices attn_fwd_splitkv uses for num_splits = 0: 1 when the
+ * B*H*ceil(Nq/128) query tiles alone fill sm_count SMs; otherwise the count
+ * that minimises (waves of blocks over sm_count SMs, one resident block each)
+ * x (key tiles per block + one tile of fixed cost), kept at 1 unless a split
+ * wins by more than 2 %.  sm_count <= 0 asks the current device.  Returns 0
+ * for invalid sizes (or when no device answers for sm_count <= 0).
+ */
+int attn_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int d, int sm_count);
+
+/*
+ * Workspace bytes of attn_fwd_splitkv for num_splits (0: the library's choice
+ * on the current device, which may need none).  0 for invalid arguments.
+ */
+size_t attn_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
+
+/*
  * Bytes of device workspace attn_bwd needs for this shape: an fp32 dQ
  * accumulator [B,H,ceil(Nq/128)*128,d] plus two fp32 row vectors of the same
  * padded length (D = rowsum(dO o O) and the base-2 LSE).  Returns 0 for

@@ -129,3 +129,36 @@ def test_strided_accepts_valid_layouts(lib):
     assert _strided_fwd(lib, [bnhd, bhnd, bnhd, bhnd]) == 3
     # B = H = 1: the batch and head strides address nothing and are not checked
     assert _strided_fwd(lib, [(0, 0, 64)] * 4, B=1, H=1) == 3
+
+
+def test_splitkv_heuristic(lib):
+    from exact_head_attention_gb300 import exattn
+    # query tiles alone fill the SMs: no split
+    assert exattn.splitkv_num_splits(1, 12, 8192, 8192, 128, sm_count=152) == 1
+    assert exattn.splitkv_num_splits(8, 16, 1024, 1024, 64, sm_count=152) == 1
+    # one key tile: nothing to divide
+    assert exattn.splitkv_num_splits(1, 1, 1, 128, 64, sm_count=152) == 1
+    # decoding: 96 rows over 256 key tiles -> 3 slices (288 blocks in 2 waves of 86 tiles)
+    assert exattn.splitkv_num_splits(8, 12, 1, 32768, 128, sm_count=152) == 3
+    for shape in [(4, 16, 64, 16384, 64), (1, 8, 1, 524288, 128), (2, 2, 1, 1000, 128)]:
+        s = exattn.splitkv_num_splits(*shape, sm_count=152)
+        assert 1 < s <= 256
+    assert exattn.splitkv_num_splits(0, 1, 1, 1, 64, sm_count=152) == 0
+    # workspace: fp32 O and LSE of every slice, each 256-byte aligned
+    rows = 3 * 8 * 12 * 1
+    assert lib.attn_fwd_splitkv_workspace_size(8, 12, 1, 32768, 128, 3) == \
+        (rows * 128 * 4 + 255) // 256 * 256 + (rows * 4 + 255) // 256 * 256
+    assert lib.attn_fwd_splitkv_workspace_size(8, 12, 1, 32768, 128, 257) == 0
+
+
+def test_splitkv_rejects_bad_arguments(lib):
+    p = [ctypes.c_void_p(FAKE)] * 5
+    need = lib.attn_fwd_splitkv_workspace_size(1, 2, 1, 1000, 64, 4)
+    call = lambda splits, ws=FAKE, nbytes=need, causal=0: lib.attn_fwd_splitkv(  # noqa: E731
+        *p, 1, 2, 1, 1000, 64, causal, 0.125, 0, splits, ctypes.c_void_p(ws) if ws else None, nbytes, None)
+    assert call(-1) == 1
+    assert call(257) == 1
+    assert call(4, causal=5) == 1
+    assert call(4, ws=None) == 6
+    assert call(4, nbytes=need - 1) == 6
+    assert call(4, ws=FAKE + 16) == 3
