@@ -18,6 +18,12 @@ runs an independent replica of the workload (no collective on the data path).
 --impl reference times the CPU oracle (the plain fp64 definition) on the host
 cores instead, on bounded samples of the same workload.
 
+--workload NAME picks another workload.  A decoding workload (few queries over a
+long key/value cache) times one split-KV forward (attn_fwd_splitkv: the slice
+kernel and the merge kernel) per step and reports the bandwidth of its
+algorithmic bytes (Q, K, V read once, O and LSE written once) against the
+measured HBM copy bandwidth.
+
 Prints ONE JSON line on rank 0.
 """
 from __future__ import annotations
@@ -59,9 +65,26 @@ def peaks() -> dict:
                 "source": "fallback"}
 
 
+def visible_pairs(w) -> int:
+    """(query, key) pairs the mask leaves visible, per head."""
+    if not w.causal:
+        return w.Nq * w.Nk
+    off = w.Nk - w.Nq if w.causal == "bottom_right" else 0
+    return sum(max(0, min(w.Nk, q + off + 1)) for q in range(w.Nq))
+
+
+def decode_bytes(w) -> int:
+    """Algorithmic bytes of one decoding forward: Q, K, V read once; O (16-bit) and LSE (fp32) written once."""
+    return w.B * w.H * (2 * w.Nq * w.d * 2 + 2 * w.Nk * w.d * 2 + w.Nq * 4)
+
+
 def config_dict(w, extra=None) -> dict:
     c = {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
-         "dtype": w.dtype, "sigma_qk": w.sigma_qk, "flops_per_step": sum(step_flops(w))}
+         "dtype": w.dtype, "sigma_qk": w.sigma_qk}
+    if w.kind == "decode":
+        c.update(kind="decode", bytes_per_step=decode_bytes(w), flops_per_step=4.0 * w.B * w.H * w.d * visible_pairs(w))
+    else:
+        c["flops_per_step"] = sum(step_flops(w))
     if extra:
         c.update(extra)
     return c
@@ -224,6 +247,176 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
+# ------------------------------------------------------------------ decoding workloads
+
+DECODE_METRIC = "decoding attention forward (split-KV): algorithmic bytes per second"
+
+
+def _oracle_decode_heads(x, w, nheads: int) -> float:
+    import oracle
+    t = time.perf_counter()
+    for i in range(nheads):
+        b, h = divmod(i, w.H)
+        oracle.attn_fwd(x["q"][b:b + 1, h:h + 1], x["k"][b:b + 1, h:h + 1], x["v"][b:b + 1, h:h + 1], w.causal,
+                        w.scale)
+    return time.perf_counter() - t
+
+
+def _decode_pick_heads(x, w, budget_s: float) -> int:
+    import oracle
+    oracle.build()
+    t1 = max(_oracle_decode_heads(x, w, 1), 1e-4)
+    return max(1, min(w.B * w.H, int(budget_s / t1)))
+
+
+def decode_cpu_sample(x, w, nheads: int) -> tuple[float, float, str]:
+    dt = _oracle_decode_heads(x, w, nheads)
+    gbs = decode_bytes(w) * nheads / (w.B * w.H) / dt / 1e9
+    sample = (f"fp64 oracle forward of the first {nheads} of {w.B * w.H} heads (all {w.Nq} queries, {w.Nk} keys), "
+              f"{dt:.1f} s on 1 thread (host has {len(os.sched_getaffinity(0))} cores available)")
+    return gbs, dt, sample
+
+
+def run_decode(args, w, rank: int, world: int) -> None:
+    from exact_head_attention_gb300 import workloads
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        x = workloads.make_inputs(w, with_grad_out=False)
+        nheads = _decode_pick_heads(x, w, max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup))))
+        for _ in range(args.warmup):
+            _oracle_decode_heads(x, w, nheads)
+        times = [_oracle_decode_heads(x, w, nheads) for _ in range(args.steps)]
+        mean = statistics.mean(times)
+        value = decode_bytes(w) * nheads / (w.B * w.H) / mean / 1e9
+        sample = f"per step: fp64 oracle forward of the first {nheads} of {w.B * w.H} heads, 1 thread"
+        print(json.dumps({
+            "impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w, {"sample_heads": nheads}),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
+
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from exact_head_attention_gb300 import build as _build
+    from exact_head_attention_gb300 import exattn
+    _build.build()
+    exattn.load()
+
+    x = workloads.make_inputs(w, seed_offset=10 * rank, with_grad_out=False)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, _, sample = decode_cpu_sample(x, w, _decode_pick_heads(x, w, 15.0))
+        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample}
+
+    stream = torch.cuda.current_stream()
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    splits = exattn.splitkv_num_splits(w.B, w.H, w.Nq, w.Nk, w.d)
+    ws = torch.empty(max(256, exattn.splitkv_workspace_size(w.B, w.H, w.Nq, w.Nk, w.d, splits)), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def launch():
+        st = exattn.fwd_splitkv_raw(q, k, v, o, lse, w.causal, w.scale, splits, ws)
+        if st:
+            raise RuntimeError(f"C-ABI status {st}: {exattn.last_error()}")
+
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    if exattn.check_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+    props = torch.cuda.get_device_properties(dev)
+    sampler = ClockSampler(getattr(props, "uuid", None) and f"GPU-{props.uuid}")
+    for _ in range(args.warmup):
+        launch()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record(stream)
+        launch()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    if exattn.check_device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+    ms_per_step = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), dist, dev)
+
+    # end to end: pinned host Q, K, V -> device -> split-KV forward -> host O, LSE
+    hq, hk, hv = (x[n].pin_memory() for n in ("q", "k", "v"))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        launch()
+        ho.copy_(o, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ms = []
+    for i in range(args.e2e_steps):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e_ms.append(a.elapsed_time(b))
+    sampler.stop()
+    e2e_ms = max_over_ranks(statistics.mean(e_ms) if e_ms else float("nan"), dist, dev)
+
+    nbytes = decode_bytes(w)
+    pk = peaks()
+    achieved = nbytes / (ms_per_step * 1e-3) / 1e9  # the slice and merge kernels together
+    line = {
+        "metric": DECODE_METRIC, "value": world * nbytes / (ms_per_step * 1e-3) / 1e9, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "fp16", "data": "synthetic: seeded normal Q, K, V (sigma 1)",
+        "config": config_dict(w, {"num_splits": splits, "parallelism": "replicas" if world > 1 else "single GPU",
+                                  "l2": "256 MiB flush write between timed steps, outside the CUDA events"}),
+        "fwd_tflops": 4.0 * w.B * w.H * w.d * visible_pairs(w) / (ms_per_step * 1e-3) / 1e12,
+        "roofline": {"kernel": "fwd_split_kernel + fwd_combine_kernel (attn_fwd_splitkv)", "bound": "hbm",
+                     "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                     "traffic": None, "peak_kind": f"HBM copy bandwidth ({pk['source']})"},
+        "cpu_baseline": cpu,
+        "e2e": ({"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms} if e_ms else None),
+        "gpu_launches": 2 * args.steps,
+        "clocks": sampler.summary(t_wall0, t_wall1),
+        "wall_s_timed_region": t_wall1 - t_wall0,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
 def main() -> None:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -240,6 +433,9 @@ def main() -> None:
     w = workloads.WORKLOADS[args.workload or workloads.HEADLINE]
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if w.kind == "decode":
+        run_decode(args, w, rank, world)
+        return
 
     if args.impl == "reference":
         if rank == 0:

@@ -42,6 +42,7 @@ class Workload:
     sigma_qk: float = 1.0
     sigma_v: float = 1.0
     sigma_do: float = 1.0
+    kind: str = "train"  # "train": forward + backward; "decode": forward only (split-KV)
 
     @property
     def scale(self) -> float:
@@ -69,9 +70,9 @@ WORKLOADS = {
     "ctx32k_d64_causal_bf16": Workload("ctx32k_d64_causal_bf16", 5, 1, 8, 32768, 32768, 64, "bf16", True),
     # decoding (split-KV forward)
     "decode_q1_kv32k_d128_bf16": Workload("decode_q1_kv32k_d128_bf16", 6, 8, 12, 1, 32768, 128, "bf16",
-                                          "bottom_right"),
+                                          "bottom_right", kind="decode"),
     "chunk_q64_kv16k_d64_fp16": Workload("chunk_q64_kv16k_d64_fp16", 8, 4, 16, 64, 16384, 64, "fp16",
-                                         "bottom_right"),
+                                         "bottom_right", kind="decode"),
 }
 
 # The workload the throughput metric is quoted on.
