@@ -244,7 +244,9 @@ struct BwdViews {
 attn_status bwd_steps(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                       void* dQ, void* dK, void* dV, const BwdViews& vw, int B, int H, int Nq, int Nk, int d,
                       int causal, float scale, attn_dtype dtype, void* workspace, size_t workspace_bytes,
-                      void* stream, int steps) {
+                      void* stream, int steps, int dq_mode = ATTN_DQ_ATOMIC) {
+  if (dq_mode != ATTN_DQ_ATOMIC && dq_mode != ATTN_DQ_DETERMINISTIC && dq_mode != ATTN_DQ_AUTO)
+    return ATTN_ERR_INVALID_ARG;
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < attn_bwd_workspace_size(B, H, Nq, d)) return ATTN_ERR_WORKSPACE;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) || !aligned16(LSE) ||
@@ -263,8 +265,13 @@ attn_status bwd_steps(const void* Q, const void* K, const void* V, const void* O
       (r = encode_map(&a.tm_v, V, bf16, B, H, Nk, d, vw.v)) != CUDA_SUCCESS ||
       (r = encode_map(&a.tm_do, dO, bf16, B, H, Nq, d, vw.dout)) != CUDA_SUCCESS ||
       (r = encode_map(&a.tm_dk, dK, bf16, B, H, Nk, d, vw.dk)) != CUDA_SUCCESS ||
-      (r = encode_map(&a.tm_dv, dV, bf16, B, H, Nk, d, vw.dv)) != CUDA_SUCCESS)
+      (r = encode_map(&a.tm_dv, dV, bf16, B, H, Nk, d, vw.dv)) != CUDA_SUCCESS ||
+      (r = encode_map(&a.tm_dq, dQ, bf16, B, H, Nq, d, vw.dq)) != CUDA_SUCCESS)
     return driver_fail("cuTensorMapEncodeTiled", r);
+  // ATTN_DQ_AUTO: the reductions into the fp32 accumulator were faster than the query-tile kernel on every
+  // shape measured on GB300 (accumulators up to four times the L2, one head whose key blocks all add into
+  // the same rows at once), so the choice resolves to them.
+  if (dq_mode == ATTN_DQ_AUTO) dq_mode = ATTN_DQ_ATOMIC;
   const int nq_pad = padded_rows(Nq);
   const size_t rows = static_cast<size_t>(bh) * nq_pad;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -290,6 +297,10 @@ attn_status bwd_steps(const void* Q, const void* K, const void* V, const void* O
   a.bf16 = bf16;
   a.scale = scale;
   a.timeout_ns = wait_timeout_ns();
+  if (dq_mode == ATTN_DQ_DETERMINISTIC) {
+    a.dq_acc = nullptr;  // no accumulator: dK, dV from the key/value blocks, dQ from the query-tile kernel
+    steps = kBwdDeterministic;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return finish(launch_bwd(a, steps, s), s);
 }
@@ -298,13 +309,13 @@ attn_status bwd_steps(const void* Q, const void* K, const void* V, const void* O
 attn_status bwd_contiguous(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                            const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk, int d,
                            int causal, float scale, attn_dtype dtype, void* workspace, size_t workspace_bytes,
-                           void* stream, int steps) {
+                           void* stream, int steps, int dq_mode = ATTN_DQ_ATOMIC) {
   attn_status st = check_common(B, H, Nq, Nk, d, causal, scale, dtype);
   if (st != ATTN_OK) return st;
   const RowStrides qs = contiguous(H, Nq, d), ks = contiguous(H, Nk, d);
   const BwdViews vw{qs, ks, ks, qs, qs, qs, ks, ks};
   return bwd_steps(Q, K, V, O, dO, LSE, dQ, dK, dV, vw, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
-                   workspace_bytes, stream, steps);
+                   workspace_bytes, stream, steps, dq_mode);
 }
 
 }  // namespace
@@ -317,13 +328,14 @@ extern "C" attn_status attn_bwd(const void* Q, const void* K, const void* V, con
                         workspace_bytes, stream, kBwdAll);
 }
 
-extern "C" attn_status attn_bwd_strided(const void* Q, attn_strides q_strides, const void* K, attn_strides k_strides,
-                                        const void* V, attn_strides v_strides, const void* O, attn_strides o_strides,
-                                        const void* dO, attn_strides do_strides, const float* LSE, void* dQ,
-                                        attn_strides dq_strides, void* dK, attn_strides dk_strides, void* dV,
-                                        attn_strides dv_strides, int B, int H, int Nq, int Nk, int d, int causal,
-                                        float scale, attn_dtype dtype, void* workspace, size_t workspace_bytes,
-                                        void* stream) {
+extern "C" attn_status attn_bwd_strided_ex(const void* Q, attn_strides q_strides, const void* K,
+                                           attn_strides k_strides, const void* V, attn_strides v_strides,
+                                           const void* O, attn_strides o_strides, const void* dO,
+                                           attn_strides do_strides, const float* LSE, void* dQ,
+                                           attn_strides dq_strides, void* dK, attn_strides dk_strides, void* dV,
+                                           attn_strides dv_strides, int B, int H, int Nq, int Nk, int d, int causal,
+                                           float scale, attn_dtype dtype, int dq_mode, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
   attn_status st = check_common(B, H, Nq, Nk, d, causal, scale, dtype);
   if (st != ATTN_OK) return st;
   BwdViews vw;
@@ -333,7 +345,27 @@ extern "C" attn_status attn_bwd_strided(const void* Q, attn_strides q_strides, c
       !normalise_strides(dk_strides, B, H, d, &vw.dk) || !normalise_strides(dv_strides, B, H, d, &vw.dv))
     return ATTN_ERR_INVALID_ARG;
   return bwd_steps(Q, K, V, O, dO, LSE, dQ, dK, dV, vw, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
-                   workspace_bytes, stream, kBwdAll);
+                   workspace_bytes, stream, kBwdAll, dq_mode);
+}
+
+extern "C" attn_status attn_bwd_strided(const void* Q, attn_strides q_strides, const void* K, attn_strides k_strides,
+                                        const void* V, attn_strides v_strides, const void* O, attn_strides o_strides,
+                                        const void* dO, attn_strides do_strides, const float* LSE, void* dQ,
+                                        attn_strides dq_strides, void* dK, attn_strides dk_strides, void* dV,
+                                        attn_strides dv_strides, int B, int H, int Nq, int Nk, int d, int causal,
+                                        float scale, attn_dtype dtype, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  return attn_bwd_strided_ex(Q, q_strides, K, k_strides, V, v_strides, O, o_strides, dO, do_strides, LSE, dQ,
+                             dq_strides, dK, dk_strides, dV, dv_strides, B, H, Nq, Nk, d, causal, scale, dtype,
+                             ATTN_DQ_ATOMIC, workspace, workspace_bytes, stream);
+}
+
+extern "C" attn_status attn_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                                   const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk,
+                                   int d, int causal, float scale, attn_dtype dtype, int dq_mode, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  return bwd_contiguous(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, Nq, Nk, d, causal, scale, dtype, workspace,
+                        workspace_bytes, stream, kBwdAll, dq_mode);
 }
 
 extern "C" attn_status attn_bwd_preprocess(const void* Q, const void* K, const void* V, const void* O,

@@ -105,7 +105,9 @@ struct BwdBars {
 // query columns [0, 64) sit in [off, off + 32), query columns [64, 128) in [64 + off, 64 + off + 32).
 __device__ __forceinline__ uint32_t packed_col(int k, int off) { return (k < 4 ? k * 8 : 64 + (k - 4) * 8) + off; }
 
-template <int D, bool CAUSAL, bool BF16>
+// DQ = false: dK and dV only (the deterministic mode computes dQ in bwd_dq_kernel instead); the dQ
+// MMA, the dS^T tile in shared memory and the reductions are left out.
+template <int D, bool CAUSAL, bool BF16, bool DQ>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
   using C = BwdCfg<D>;
   constexpr int NR = C::NR;
@@ -273,6 +275,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         mma_commit(bars.ring_empty(slot_of(2 * it)));
         // S^T_{i+1} overwrites X after dV_i, dK_i have read it (MMAs of one thread run in order).
         if (it + 1 < n && !(ok = issue_S(it + 1))) break;
+        if constexpr (!DQ) {
+          if (it + 1 < n && !(ok = issue_dP(it + 1))) break;
+          continue;
+        }
         if (it > 0 && !(ok = mbar_wait(bars.dq_empty(), (it - 1) & 1, wc))) break;
         if (!(ok = mbar_wait(bars.dss_ready(), it & 1, wc))) break;
         tc_fence_after();
@@ -408,7 +414,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
 
       // d = 128: dQ of the previous tile completes just before this tile's dP^T; staging it for the
       // copy engine fits in that window.
-      if (D == 128 && it > 0 && !(ok = drain_dq(it - 1))) break;
+      if (DQ && D == 128 && it > 0 && !(ok = drain_dq(it - 1))) break;
 
       if (!(ok = mbar_wait_warp(bars.dp_full(), it & 1, wc))) break;
       tc_fence_after();
@@ -440,6 +446,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bars.pd_ready());  // dV_i, dK_i and S_{i+1} may go
+      if constexpr (!DQ) continue;
       if (it > 0 && !(ok = mbar_wait_warp(bars.ds_empty(), (it - 1) & 1, wc))) break;
       if constexpr (D == 128) {
         // The dS^T tile held warpgroup 1's dQ_{i-1} rows; the copy engine must have read them.
@@ -457,9 +464,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       mbar_arrive(bars.dss_ready());  // dQ_i may go
 
       // d = 64: the previous tile's per-thread reductions run after this tile is handed over.
-      if (D == 64 && it > 0 && !(ok = drain_dq(it - 1))) break;
+      if (DQ && D == 64 && it > 0 && !(ok = drain_dq(it - 1))) break;
     }
-    if (ok && n > 0) ok = drain_dq(n - 1);
+    if (DQ && ok && n > 0) ok = drain_dq(n - 1);
 
     // ------------------------------------------------------------ epilogue
     // warps 0-3 write dV (staged in the V tile), warps 4-7 write dK * scale (staged in the K tile).
@@ -541,9 +548,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
 #pragma unroll
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (!in_range) return;
-  float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D + sub * 8);
-  z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-  z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (a.dq_acc != nullptr) {  // no accumulator in the deterministic mode
+    float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D + sub * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   if (sub == 0) {
     if (q < a.Nq) {
       const float lse = a.lse[static_cast<size_t>(bh) * a.Nq + q];
@@ -590,7 +599,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int steps, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   if (steps & kBwdMain) {
-    auto kern = bwd_main_kernel<D, CAUSAL, BF16>;
+    // no accumulator: the deterministic mode, where bwd_dq_kernel produces dQ
+    auto kern = a.dq_acc ? bwd_main_kernel<D, CAUSAL, BF16, true> : bwd_main_kernel<D, CAUSAL, BF16, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     dim3 grid(a.bh_count, (a.Nk + kTileRows - 1) / kTileRows, 1);
@@ -598,11 +608,13 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int steps, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  if (steps & kBwdConvert) {
+  if ((steps & kBwdConvert) && a.dq_acc) {
     const size_t total = static_cast<size_t>(a.bh_count) * a.Nq * D / 8;
     bwd_dq_convert_kernel<D, BF16><<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(a);
-    return cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
+  if (steps & kBwdDq) return launch_bwd_dq(a, stream);
   return cudaSuccess;
 }
 

@@ -32,13 +32,13 @@ struct FwdArgs {
 };
 
 struct BwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv;
+  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv, tm_dq;
   const void* o;       // [B][H][Nq][d] 16-bit, strides so
   const void* dout;    // [B][H][Nq][d] 16-bit, strides sdo
   const float* lse;    // [B*H][Nq]
   void* dq;            // [B][H][Nq][d] 16-bit, strides sdq
   RowStrides so, sdo, sdq;
-  float* dq_acc;       // [B*H][Nq_pad][d] fp32 workspace
+  float* dq_acc;       // [B*H][Nq_pad][d] fp32 workspace (nullptr: deterministic dQ)
   float* lse2;         // [B*H][Nq_pad] fp32 workspace: LSE * log2(e), +inf on padding rows
   float* dsum;         // [B*H][Nq_pad] fp32 workspace: rowsum(dO o O), 0 on padding rows
   uint32_t* err_word;
@@ -66,8 +66,10 @@ struct SplitArgs {
   uint64_t timeout_ns;
 };
 
-// Backward steps (bit mask for launch_bwd).
-constexpr int kBwdPre = 1, kBwdMain = 2, kBwdConvert = 4, kBwdAll = 7;
+// Backward steps (bit mask for launch_bwd).  The atomic dQ mode runs pre, main, convert; the
+// deterministic mode (dq_acc == nullptr) runs pre, main (dK and dV only), then the dQ kernel.
+constexpr int kBwdPre = 1, kBwdMain = 2, kBwdConvert = 4, kBwdAll = 7, kBwdDq = 8;
+constexpr int kBwdDeterministic = kBwdPre | kBwdMain | kBwdDq;
 
 // Sets the message attn_last_error returns on this host thread.
 void set_last_error(const char* msg);
@@ -76,5 +78,6 @@ void set_last_error(const char* msg);
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_split(const SplitArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, int steps, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
 
 }  // namespace exattn

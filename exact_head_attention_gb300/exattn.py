@@ -22,6 +22,8 @@ ATTN_BF16, ATTN_FP16 = 0, 1
 # attn_mask: none, top-left causal (query q sees keys k <= q), bottom-right causal (k <= q + Nk - Nq)
 ATTN_MASK_NONE, ATTN_MASK_CAUSAL, ATTN_MASK_CAUSAL_BOTTOM_RIGHT = 0, 1, 2
 _MASKS = {False: 0, True: 1, 0: 0, 1: 1, 2: 2, "none": 0, "top_left": 1, "bottom_right": 2}
+# attn_dq_mode
+DQ_MODES = {"atomic": 0, "deterministic": 1, "auto": 2}
 # attn_bwd is these three C-ABI calls in this order
 BWD_STEPS = ("attn_bwd_preprocess", "attn_bwd_kv_blocks", "attn_bwd_dq_convert")
 
@@ -73,6 +75,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_fwd_splitkv_num_splits.restype = i
             lib.attn_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i, i]
             lib.attn_fwd_splitkv_workspace_size.restype = sz
+            lib.attn_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, sz, vp]
+            lib.attn_bwd_ex.restype = i
+            lib.attn_bwd_strided_ex.argtypes = [vp, st, vp, st, vp, st, vp, st, vp, st, vp, vp, st, vp, st, vp, st,
+                                                i, i, i, i, i, i, f, i, i, vp, sz, vp]
+            lib.attn_bwd_strided_ex.restype = i
             lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
             lib.attn_bwd_workspace_size.restype = sz
             for name in ("attn_bwd",) + BWD_STEPS:
@@ -236,15 +243,41 @@ def bwd_strided_raw(q, k, v, o, do, lse, dq, dk, dv, causal, scale: float, works
                                    float(scale), _dtype_code(q), *_workspace(workspace), _stream(stream))
 
 
-def backward(q, k, v, o, do, lse, causal=False, scale: float | None = None, workspace=None, stream=None):
+def dq_mode_code(dq_mode) -> int:
+    if isinstance(dq_mode, str):
+        if dq_mode not in DQ_MODES:
+            raise ValueError(f"unknown dq_mode {dq_mode!r}")
+        return DQ_MODES[dq_mode]
+    return int(dq_mode)
+
+
+def bwd_ex_raw(q, k, v, o, do, lse, dq, dk, dv, causal, scale: float, dq_mode, workspace, stream=None) -> int:
+    """Calls attn_bwd_ex (contiguous) or attn_bwd_strided_ex with a dQ mode; returns the status code."""
+    B, H, Nq, Nk, d = _dims(q, k)
+    common = (B, H, Nq, Nk, d, mask_code(causal), float(scale), _dtype_code(q), dq_mode_code(dq_mode),
+              *_workspace(workspace), _stream(stream))
+    if _all_contiguous(q, k, v, o, do, dq, dk, dv):
+        return load().attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), *common)
+    return load().attn_bwd_strided_ex(*_view(q), *_view(k), *_view(v), *_view(o), *_view(do), _ptr(lse),
+                                      *_view(dq), *_view(dk), *_view(dv), *common)
+
+
+def backward(q, k, v, o, do, lse, causal=False, scale: float | None = None, workspace=None, stream=None,
+             dq_mode="atomic"):
     """(dQ, dK, dV) for the loss sum(O * dO).  `workspace` (uint8 CUDA tensor) is allocated if omitted.
-    Gradients take the strides of q, k, v where those are dense; views go through attn_bwd_strided."""
+
+    dq_mode: "atomic" (attn_bwd), "deterministic" (dQ from a query-tile kernel, same bits on every
+    run) or "auto".  Gradients take the strides of q, k, v where those are dense; views go through
+    the strided entry points."""
     B, H, Nq, Nk, d = _dims(q, k)
     scale = (1.0 / d ** 0.5) if scale is None else scale
     if workspace is None:
         workspace = torch.empty(workspace_size(B, H, Nq, d), dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    if _all_contiguous(q, k, v, o, do, dq, dk, dv):
+    if dq_mode_code(dq_mode) != DQ_MODES["atomic"]:
+        _check(bwd_ex_raw(q, k, v, o, do, lse, dq, dk, dv, causal, scale, dq_mode, workspace, stream), "attn_bwd_ex")
+    elif _all_contiguous(q, k, v, o, do, dq, dk, dv):
         _check(bwd_raw(q, k, v, o, do, lse, dq, dk, dv, causal, scale, workspace, stream), "attn_bwd")
     else:
         _check(bwd_strided_raw(q, k, v, o, do, lse, dq, dk, dv, causal, scale, workspace, stream),
@@ -259,10 +292,10 @@ def check_device_error(stream=None) -> int:
 
 class _AttnFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, causal, scale):
+    def forward(ctx, q, k, v, causal, scale, dq_mode):
         o, lse = forward(q, k, v, causal, scale)
         ctx.save_for_backward(q, k, v, o, lse)
-        ctx.causal, ctx.scale = causal, scale
+        ctx.causal, ctx.scale, ctx.dq_mode = causal, scale, dq_mode
         return o
 
     @staticmethod
@@ -270,11 +303,12 @@ class _AttnFunction(torch.autograd.Function):
         q, k, v, o, lse = ctx.saved_tensors
         if do.stride(-1) != 1:
             do = do.contiguous()
-        dq, dk, dv = backward(q, k, v, o, do, lse, ctx.causal, ctx.scale)
-        return dq, dk, dv, None, None
+        dq, dk, dv = backward(q, k, v, o, do, lse, ctx.causal, ctx.scale, dq_mode=ctx.dq_mode)
+        return dq, dk, dv, None, None, None
 
 
-def attention(q, k, v, causal=False, scale: float | None = None):
-    """Autograd-aware exact attention over [B, H, N, d] tensors (causal: False, True or "bottom_right")."""
+def attention(q, k, v, causal=False, scale: float | None = None, dq_mode="atomic"):
+    """Autograd-aware exact attention over [B, H, N, d] tensors (causal: False, True or "bottom_right";
+    dq_mode: "atomic", "deterministic" or "auto")."""
     scale = (1.0 / q.shape[-1] ** 0.5) if scale is None else scale
-    return _AttnFunction.apply(q, k, v, causal, scale)
+    return _AttnFunction.apply(q, k, v, causal, scale, dq_mode)

@@ -207,6 +207,59 @@ attn_status attn_bwd_strided(const void* Q, attn_strides q_strides, const void* 
                              void* stream);
 
 /*
+ * How the backward produces dQ (attn_bwd_ex, attn_bwd_strided_ex).
+ *   ATTN_DQ_ATOMIC         every key/value block adds its dQ contribution into
+ *                          an fp32 accumulator (copy-engine reduce-adds at
+ *                          d = 128, vector reductions at d = 64); the order
+ *                          of the additions varies, so dQ may differ between
+ *                          runs in its last bits.  This is attn_bwd.
+ *   ATTN_DQ_DETERMINISTIC  the key/value blocks produce dK and dV only; a
+ *                          second kernel, parallel over 128-row query tiles,
+ *                          recomputes S, P, dP and dS for each key tile the
+ *                          tile sees, in increasing key order, and accumulates
+ *                          dQ on chip.  dQ, dK and dV are the same bits on
+ *                          every run; S and dP are computed twice (seven
+ *                          tile products per key/query tile pair instead of
+ *                          five).
+ *   ATTN_DQ_AUTO           the faster of the two for the shape.  The StreamKL
+ *                          summary (backward, kernel fusion) picks atomics
+ *                          while the buffer fits in L2 and separate kernels
+ *                          when contention on it grows.  On GB300 the
+ *                          reductions beat the separate kernel on every shape
+ *                          measured: fp32 accumulators from 4 MiB to four
+ *                          times the L2 size, causal and not, and one head
+ *                          whose 256 key blocks all add into the same rows at
+ *                          once.  So AUTO resolves to ATTN_DQ_ATOMIC;
+ *                          determinism is the only reason to ask for the
+ *                          other mode.
+ * SparkAttention Figure 9 adds dQ across thread blocks atomically.
+ */
+typedef enum {
+  ATTN_DQ_ATOMIC = 0,
+  ATTN_DQ_DETERMINISTIC = 1,
+  ATTN_DQ_AUTO = 2
+} attn_dq_mode;
+
+/*
+ * attn_bwd with a dQ mode (attn_dq_mode; other values are
+ * ATTN_ERR_INVALID_ARG).  The workspace is sized by attn_bwd_workspace_size
+ * for every mode (the deterministic mode leaves the accumulator part unused).
+ */
+attn_status attn_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                        const float* LSE, void* dQ, void* dK, void* dV,
+                        int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                        attn_dtype dtype, int dq_mode, void* workspace, size_t workspace_bytes, void* stream);
+
+/* attn_bwd_strided with a dQ mode (see attn_bwd_ex). */
+attn_status attn_bwd_strided_ex(const void* Q, attn_strides q_strides, const void* K, attn_strides k_strides,
+                                const void* V, attn_strides v_strides, const void* O, attn_strides o_strides,
+                                const void* dO, attn_strides do_strides, const float* LSE, void* dQ,
+                                attn_strides dq_strides, void* dK, attn_strides dk_strides, void* dV,
+                                attn_strides dv_strides, int B, int H, int Nq, int Nk, int d, int causal,
+                                float scale, attn_dtype dtype, int dq_mode, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
  * The three steps attn_bwd launches, callable one at a time (same arguments
  * and validation as attn_bwd; attn_bwd is exactly these three in this order on
  * `stream`, sharing `workspace`):

@@ -162,3 +162,12 @@ def test_splitkv_rejects_bad_arguments(lib):
     assert call(4, ws=None) == 6
     assert call(4, nbytes=need - 1) == 6
     assert call(4, ws=FAKE + 16) == 3
+
+
+def test_bwd_ex_rejects_unknown_dq_mode(lib):
+    p = [ctypes.c_void_p(FAKE)] * 9
+    need = lib.attn_bwd_workspace_size(1, 1, 128, 64)
+    for mode in (-1, 3, 17):
+        assert lib.attn_bwd_ex(*p, 1, 1, 128, 128, 64, 0, 0.125, 0, mode, ctypes.c_void_p(FAKE), need, None) == 1
+    # a valid mode still stops at the misaligned workspace, before any launch
+    assert lib.attn_bwd_ex(*p, 1, 1, 128, 128, 64, 0, 0.125, 0, 1, ctypes.c_void_p(FAKE + 16), need, None) == 3
