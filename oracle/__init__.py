@@ -20,6 +20,12 @@ Definitions (cited in ``attn_oracle.c``):
     dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q -- SparkAttention,
     Figure 9 / Equation 4 (equation body not printed; exact gradient written out).
 
+Attention KL divergence (StreamKL summary, Methodology 1-2): a teacher (1) and a
+student (2) distribution P_t = softmax(scale Q_t K_t^T), KL_q = sum_k P1 (log P1 -
+log P2) with log P_t = S_t - LSE_t, and the gradients of sum_q g_q KL_q for the
+student (setting 1: dS2 = g (P2 - P1)) or the teacher (setting 2: dS1 = g P1
+(log P1 - log P2 - KL)), dQ_t = scale dS_t K_t, dK_t = scale dS_t^T Q_t.
+
 Every function here is pinned by tests that do not re-type the formula:
 closed forms, invariants, finite differences and a library special case
 (torch's fp64 CPU scaled_dot_product_attention).
@@ -69,8 +75,15 @@ def _load():
             lib.oracle_attn_dq_rows.argtypes = [dp, dp, dp, dp, I, I, L, L, I, I, D, L, lp, dp, dp]
             lib.oracle_attn_dkdv_cols.argtypes = [dp, dp, dp, dp, I, I, L, L, I, I, D, L, lp, dp, dp]
             lib.oracle_attn_probs.argtypes = [dp, dp, L, L, I, I, D, dp, dp]
+            lib.oracle_kl_fwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, I, I, L, L, I, I, D]
+            lib.oracle_kl_bwd.argtypes = [dp, dp, dp, dp, dp, I, dp, dp, I, I, L, L, I, I, D]
+            lib.oracle_kl_fwd_rows.argtypes = [dp, dp, dp, dp, I, I, L, L, I, I, D, L, lp, dp, dp, dp]
+            lib.oracle_kl_dq_rows.argtypes = [dp, dp, dp, dp, dp, I, I, I, L, L, I, I, D, L, lp, dp]
+            lib.oracle_kl_dk_cols.argtypes = [dp, dp, dp, dp, dp, I, I, I, L, L, I, I, D, L, lp, dp]
             for f in (lib.oracle_attn_fwd, lib.oracle_attn_bwd, lib.oracle_attn_fwd_rows,
-                      lib.oracle_attn_dq_rows, lib.oracle_attn_dkdv_cols, lib.oracle_attn_probs):
+                      lib.oracle_attn_dq_rows, lib.oracle_attn_dkdv_cols, lib.oracle_attn_probs,
+                      lib.oracle_kl_fwd, lib.oracle_kl_bwd, lib.oracle_kl_fwd_rows, lib.oracle_kl_dq_rows,
+                      lib.oracle_kl_dk_cols):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -189,3 +202,81 @@ def attn_probs(qh, kh, causal, scale: float):
     lse = np.zeros(Nq)
     _load().oracle_attn_probs(_ptr(qh), _ptr(kh), Nq, Nk, d, _mask(causal), float(scale), _ptr(p), _ptr(lse))
     return p, lse
+
+
+# ---------------------------------------------------------------- attention KL divergence
+
+def _kl_shape(q1, k1, q2, k2):
+    B, H, Nq, Nk, d = _shape(q1, k1)
+    if q2.shape != q1.shape or k2.shape != k1.shape:
+        raise ValueError("teacher and student tensors disagree in shape")
+    return B, H, Nq, Nk, d
+
+
+def _setting(setting) -> int:
+    if setting not in (1, 2):
+        raise ValueError("setting must be 1 (student trained) or 2 (teacher trained)")
+    return int(setting)
+
+
+def kl_fwd(q1, k1, q2, k2, causal, scale: float):
+    """KL [B,H,Nq] of the student (q2, k2) from the teacher (q1, k1), and LSE1, LSE2 [B,H,Nq]."""
+    q1, k1, q2, k2 = _f64(q1), _f64(k1), _f64(q2), _f64(k2)
+    B, H, Nq, Nk, d = _kl_shape(q1, k1, q2, k2)
+    kl, lse1, lse2 = (np.zeros((B, H, Nq)) for _ in range(3))
+    rc = _load().oracle_kl_fwd(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(kl), _ptr(lse1), _ptr(lse2),
+                               B, H, Nq, Nk, d, _mask(causal), float(scale))
+    if rc != 0:
+        raise MemoryError("oracle_kl_fwd failed")
+    return kl, lse1, lse2
+
+
+def kl_bwd(q1, k1, q2, k2, g, setting, causal, scale: float):
+    """(dQ, dK) of sum_q g_q KL_q for the student (setting 1) or the teacher (setting 2)."""
+    q1, k1, q2, k2, g = _f64(q1), _f64(k1), _f64(q2), _f64(k2), _f64(g)
+    B, H, Nq, Nk, d = _kl_shape(q1, k1, q2, k2)
+    dq, dk = np.zeros((B, H, Nq, d)), np.zeros((B, H, Nk, d))
+    rc = _load().oracle_kl_bwd(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(g), _setting(setting), _ptr(dq),
+                               _ptr(dk), B, H, Nq, Nk, d, _mask(causal), float(scale))
+    if rc != 0:
+        raise MemoryError("oracle_kl_bwd failed")
+    return dq, dk
+
+
+def kl_fwd_rows(q1, k1, q2, k2, causal, scale: float, rows):
+    """KL, LSE1, LSE2 of chosen rows; rows[i] = (b*H + h)*Nq + q."""
+    q1, k1, q2, k2 = _f64(q1), _f64(k1), _f64(q2), _f64(k2)
+    B, H, Nq, Nk, d = _kl_shape(q1, k1, q2, k2)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    kl, lse1, lse2 = (np.zeros(len(rows)) for _ in range(3))
+    rc = _load().oracle_kl_fwd_rows(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), B, H, Nq, Nk, d, _mask(causal),
+                                    float(scale), len(rows), _lptr(rows), _ptr(kl), _ptr(lse1), _ptr(lse2))
+    if rc != 0:
+        raise MemoryError("oracle_kl_fwd_rows failed")
+    return kl, lse1, lse2
+
+
+def kl_dq_rows(q1, k1, q2, k2, g, setting, causal, scale: float, rows):
+    """dQ of the trained distribution for chosen rows; rows[i] = (b*H + h)*Nq + q."""
+    q1, k1, q2, k2, g = _f64(q1), _f64(k1), _f64(q2), _f64(k2), _f64(g)
+    B, H, Nq, Nk, d = _kl_shape(q1, k1, q2, k2)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    dq = np.zeros((len(rows), d))
+    rc = _load().oracle_kl_dq_rows(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(g), _setting(setting), B, H, Nq,
+                                   Nk, d, _mask(causal), float(scale), len(rows), _lptr(rows), _ptr(dq))
+    if rc != 0:
+        raise MemoryError("oracle_kl_dq_rows failed")
+    return dq
+
+
+def kl_dk_cols(q1, k1, q2, k2, g, setting, causal, scale: float, cols):
+    """dK of the trained distribution for chosen key rows; cols[i] = (b*H + h)*Nk + k."""
+    q1, k1, q2, k2, g = _f64(q1), _f64(k1), _f64(q2), _f64(k2), _f64(g)
+    B, H, Nq, Nk, d = _kl_shape(q1, k1, q2, k2)
+    cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+    dk = np.zeros((len(cols), d))
+    rc = _load().oracle_kl_dk_cols(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(g), _setting(setting), B, H, Nq,
+                                   Nk, d, _mask(causal), float(scale), len(cols), _lptr(cols), _ptr(dk))
+    if rc != 0:
+        raise MemoryError("oracle_kl_dk_cols failed")
+    return dk

@@ -305,3 +305,225 @@ int oracle_attn_probs(const double* Qh, const double* Kh, long Nq, long Nk, int 
   for (long q = 0; q < Nq; ++q) row_probs(Qh, Kh, Nk, d, q, causal, off, scale, P + (size_t)q * Nk, &lse[q]);
   return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Attention KL divergence (StreamKL summary, gist.science 2606.20005).
+ *
+ * Two attention distributions over the same keys positions, a teacher (1) and
+ * a student (2), each from its own queries and keys:
+ *   S_t = scale Q_t K_t^T (visible keys only), P_t = softmax_row(S_t),
+ *   LSE_t = m_t + ln sum_k exp(S_t - m_t)                  (Methodology 1)
+ * and the row-wise divergence of the student from the teacher
+ *   KL_q = sum_k P1_qk (log P1_qk - log P2_qk),  log P_t = S_t - LSE_t.
+ * Gradients of L = sum_q g_q KL_q (Methodology 2, P regenerated from LSE):
+ *   setting 1 (teacher fixed, the student is trained):
+ *     dS2_qk = g_q (P2_qk - P1_qk)
+ *   setting 2 (student fixed, the teacher is trained):
+ *     dS1_qk = g_q P1_qk ((S1_qk - LSE1_q) - (S2_qk - LSE2_q) - KL_q)
+ *   then dQ_t = scale dS_t K_t and dK_t = scale dS_t^T Q_t for the trained
+ *   distribution t.  The masks are those of the attention oracle above; a row
+ *   that sees no key has KL = 0, LSE_t = -inf and zero gradients.
+ * ------------------------------------------------------------------------ */
+
+/* Both distributions of one row; returns the number of visible keys. */
+static long kl_row(const double* Q1h, const double* K1h, const double* Q2h, const double* K2h, long Nk, int d,
+                   long q, int causal, long off, double scale, double* P1, double* P2, double* lse1, double* lse2,
+                   double* kl) {
+  long n = row_probs(Q1h, K1h, Nk, d, q, causal, off, scale, P1, lse1);
+  row_probs(Q2h, K2h, Nk, d, q, causal, off, scale, P2, lse2);
+  double acc = 0.0;
+  for (long k = 0; k < Nk && n > 0; ++k) {
+    if (!key_visible(q, k, causal, off) || P1[k] == 0.0) continue;
+    const double s1 = scale * dot(Q1h + (size_t)q * d, K1h + (size_t)k * d, d);
+    const double s2 = scale * dot(Q2h + (size_t)q * d, K2h + (size_t)k * d, d);
+    acc += P1[k] * ((s1 - *lse1) - (s2 - *lse2));
+  }
+  *kl = n > 0 ? acc : 0.0;
+  return n;
+}
+
+/* KL, LSE1, LSE2 [B][H][Nq]. */
+int oracle_kl_fwd(const double* Q1, const double* K1, const double* Q2, const double* K2, double* KL, double* LSE1,
+                  double* LSE2, int B, int H, long Nq, long Nk, int d, int causal, double scale) {
+  const long off = mask_offset(causal, Nq, Nk);
+  double* P1 = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  double* P2 = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  if (!P1 || !P2) {
+    free(P1);
+    free(P2);
+    return -1;
+  }
+  for (long bh = 0; bh < (long)B * H; ++bh) {
+    const size_t qo = (size_t)bh * Nq * d, ko = (size_t)bh * Nk * d;
+    for (long q = 0; q < Nq; ++q) {
+      const size_t r = (size_t)bh * Nq + q;
+      kl_row(Q1 + qo, K1 + ko, Q2 + qo, K2 + ko, Nk, d, q, causal, off, scale, P1, P2, &LSE1[r], &LSE2[r], &KL[r]);
+    }
+  }
+  free(P1);
+  free(P2);
+  return 0;
+}
+
+/* dS of one row for the trained distribution (setting 1: student, 2: teacher); dS [Nk]. */
+static void kl_row_ds(const double* Q1h, const double* K1h, const double* Q2h, const double* K2h, long Nk, int d,
+                      long q, int causal, long off, double scale, double g, int setting, double* P1, double* P2,
+                      double* dS) {
+  double lse1, lse2, kl;
+  long n = kl_row(Q1h, K1h, Q2h, K2h, Nk, d, q, causal, off, scale, P1, P2, &lse1, &lse2, &kl);
+  for (long k = 0; k < Nk; ++k) {
+    dS[k] = 0.0;
+    if (n == 0 || !key_visible(q, k, causal, off)) continue;
+    if (setting == 1) {
+      dS[k] = g * (P2[k] - P1[k]);
+    } else {
+      const double s1 = scale * dot(Q1h + (size_t)q * d, K1h + (size_t)k * d, d);
+      const double s2 = scale * dot(Q2h + (size_t)q * d, K2h + (size_t)k * d, d);
+      dS[k] = g * P1[k] * ((s1 - lse1) - (s2 - lse2) - kl);
+    }
+  }
+}
+
+/*
+ * Gradients of sum_q G_q KL_q for the trained distribution: dQ [B][H][Nq][d] and dK [B][H][Nk][d] of the
+ * student (setting 1) or of the teacher (setting 2).  G [B][H][Nq].
+ */
+int oracle_kl_bwd(const double* Q1, const double* K1, const double* Q2, const double* K2, const double* G,
+                  int setting, double* dQ, double* dK, int B, int H, long Nq, long Nk, int d, int causal,
+                  double scale) {
+  if (setting != 1 && setting != 2) return -2;
+  const long off = mask_offset(causal, Nq, Nk);
+  double* P1 = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  double* P2 = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  double* dS = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  if (!P1 || !P2 || !dS) {
+    free(P1);
+    free(P2);
+    free(dS);
+    return -1;
+  }
+  for (long bh = 0; bh < (long)B * H; ++bh) {
+    const size_t qo = (size_t)bh * Nq * d, ko = (size_t)bh * Nk * d;
+    const double* Qt = (setting == 1 ? Q2 : Q1) + qo;
+    const double* Kt = (setting == 1 ? K2 : K1) + ko;
+    double* dKh = dK + ko;
+    memset(dKh, 0, sizeof(double) * (size_t)Nk * d);
+    for (long q = 0; q < Nq; ++q) {
+      kl_row_ds(Q1 + qo, K1 + ko, Q2 + qo, K2 + ko, Nk, d, q, causal, off, scale, G[(size_t)bh * Nq + q], setting,
+                P1, P2, dS);
+      double* dqrow = dQ + qo + (size_t)q * d;
+      for (int c = 0; c < d; ++c) dqrow[c] = 0.0;
+      for (long k = 0; k < Nk; ++k) {
+        if (dS[k] == 0.0) continue;
+        for (int c = 0; c < d; ++c) {
+          dqrow[c] += scale * dS[k] * Kt[(size_t)k * d + c];
+          dKh[(size_t)k * d + c] += scale * dS[k] * Qt[(size_t)q * d + c];
+        }
+      }
+    }
+  }
+  free(P1);
+  free(P2);
+  free(dS);
+  return 0;
+}
+
+/* KL, LSE1, LSE2 of chosen rows (rows[i] = bh * Nq + q). */
+int oracle_kl_fwd_rows(const double* Q1, const double* K1, const double* Q2, const double* K2, int B, int H, long Nq,
+                       long Nk, int d, int causal, double scale, long nrows, const long* rows, double* KL,
+                       double* LSE1, double* LSE2) {
+  (void)B;
+  (void)H;
+  const long off = mask_offset(causal, Nq, Nk);
+  double* P1 = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  double* P2 = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  if (!P1 || !P2) {
+    free(P1);
+    free(P2);
+    return -1;
+  }
+  for (long i = 0; i < nrows; ++i) {
+    const long bh = rows[i] / Nq, q = rows[i] % Nq;
+    const size_t qo = (size_t)bh * Nq * d, ko = (size_t)bh * Nk * d;
+    kl_row(Q1 + qo, K1 + ko, Q2 + qo, K2 + ko, Nk, d, q, causal, off, scale, P1, P2, &LSE1[i], &LSE2[i], &KL[i]);
+  }
+  free(P1);
+  free(P2);
+  return 0;
+}
+
+/* dQ of the trained distribution for chosen rows (rows[i] = bh * Nq + q); dQ_rows [nrows][d]. */
+int oracle_kl_dq_rows(const double* Q1, const double* K1, const double* Q2, const double* K2, const double* G,
+                      int setting, int B, int H, long Nq, long Nk, int d, int causal, double scale, long nrows,
+                      const long* rows, double* dQ_rows) {
+  (void)B;
+  (void)H;
+  if (setting != 1 && setting != 2) return -2;
+  const long off = mask_offset(causal, Nq, Nk);
+  double* P1 = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  double* P2 = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  double* dS = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  if (!P1 || !P2 || !dS) {
+    free(P1);
+    free(P2);
+    free(dS);
+    return -1;
+  }
+  for (long i = 0; i < nrows; ++i) {
+    const long bh = rows[i] / Nq, q = rows[i] % Nq;
+    const size_t qo = (size_t)bh * Nq * d, ko = (size_t)bh * Nk * d;
+    const double* Kt = (setting == 1 ? K2 : K1) + ko;
+    kl_row_ds(Q1 + qo, K1 + ko, Q2 + qo, K2 + ko, Nk, d, q, causal, off, scale, G[(size_t)bh * Nq + q], setting,
+              P1, P2, dS);
+    double* dqrow = dQ_rows + (size_t)i * d;
+    for (int c = 0; c < d; ++c) dqrow[c] = 0.0;
+    for (long k = 0; k < Nk; ++k) {
+      if (dS[k] == 0.0) continue;
+      for (int c = 0; c < d; ++c) dqrow[c] += scale * dS[k] * Kt[(size_t)k * d + c];
+    }
+  }
+  free(P1);
+  free(P2);
+  free(dS);
+  return 0;
+}
+
+/* dK of the trained distribution for chosen key rows (cols[i] = bh * Nk + k); dK_cols [ncols][d]. */
+int oracle_kl_dk_cols(const double* Q1, const double* K1, const double* Q2, const double* K2, const double* G,
+                      int setting, int B, int H, long Nq, long Nk, int d, int causal, double scale, long ncols,
+                      const long* cols, double* dK_cols) {
+  if (setting != 1 && setting != 2) return -2;
+  const long off = mask_offset(causal, Nq, Nk);
+  double* P1 = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  double* P2 = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  double* dS = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+  if (!P1 || !P2 || !dS) {
+    free(P1);
+    free(P2);
+    free(dS);
+    return -1;
+  }
+  memset(dK_cols, 0, sizeof(double) * (size_t)ncols * d);
+  for (long bh = 0; bh < (long)B * H; ++bh) {
+    long kmin = -1;
+    for (long i = 0; i < ncols; ++i)
+      if (cols[i] / Nk == bh && (kmin < 0 || cols[i] % Nk < kmin)) kmin = cols[i] % Nk;
+    if (kmin < 0) continue;
+    const size_t qo = (size_t)bh * Nq * d, ko = (size_t)bh * Nk * d;
+    const double* Qt = (setting == 1 ? Q2 : Q1) + qo;
+    for (long q = (causal && kmin - off > 0) ? kmin - off : 0; q < Nq; ++q) {
+      kl_row_ds(Q1 + qo, K1 + ko, Q2 + qo, K2 + ko, Nk, d, q, causal, off, scale, G[(size_t)bh * Nq + q], setting,
+                P1, P2, dS);
+      for (long i = 0; i < ncols; ++i) {
+        if (cols[i] / Nk != bh) continue;
+        const long k = cols[i] % Nk;
+        if (dS[k] == 0.0) continue;
+        for (int c = 0; c < d; ++c) dK_cols[(size_t)i * d + c] += scale * dS[k] * Qt[(size_t)q * d + c];
+      }
+    }
+  }
+  free(P1);
+  free(P2);
+  free(dS);
+  return 0;
+}
