@@ -569,3 +569,109 @@ extern "C" attn_status attn_fwd_splitkv_strided(const void* Q, attn_strides q_st
   return fwd_split_impl(Q, qs, K, ks, V, vs, O, os, LSE, B, H, Nq, Nk, d, causal, scale, dtype, num_splits,
                         workspace, workspace_bytes, stream);
 }
+
+// ----------------------------------------------------------------- attention KL divergence
+
+namespace {
+
+attn_status kl_common(const void* Q1, const void* K1, const void* Q2, const void* K2, int B, int H, int Nq, int Nk,
+                      int d, int causal, float scale, attn_dtype dtype, KlArgs* a, DeviceState** ds) {
+  attn_status st = check_common(B, H, Nq, Nk, d, causal, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if ((Nq + kTileRows - 1) / kTileRows > 65535) return ATTN_ERR_INVALID_ARG;
+  if (!Q1 || !K1 || !Q2 || !K2) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(Q1) || !aligned16(K1) || !aligned16(Q2) || !aligned16(K2)) return ATTN_ERR_MISALIGNED;
+  if ((st = device_state(ds)) != ATTN_OK) return st;
+  std::memset(a, 0, sizeof(*a));
+  const bool bf16 = dtype == ATTN_BF16;
+  const RowStrides qs = contiguous(H, Nq, d), ks = contiguous(H, Nk, d);
+  CUresult r;
+  if ((r = encode_map(&a->tm_qa, Q1, bf16, B, H, Nq, d, qs)) != CUDA_SUCCESS ||
+      (r = encode_map(&a->tm_ka, K1, bf16, B, H, Nk, d, ks)) != CUDA_SUCCESS ||
+      (r = encode_map(&a->tm_qb, Q2, bf16, B, H, Nq, d, qs)) != CUDA_SUCCESS ||
+      (r = encode_map(&a->tm_kb, K2, bf16, B, H, Nk, d, ks)) != CUDA_SUCCESS)
+    return driver_fail("cuTensorMapEncodeTiled", r);
+  a->err_word = (*ds)->err_word;
+  a->bh_count = B * H;
+  a->heads = H;
+  a->Nq = Nq;
+  a->Nk = Nk;
+  a->d = d;
+  a->causal = causal != ATTN_MASK_NONE;
+  a->causal_off = causal_offset(causal, Nq, Nk);
+  a->bf16 = bf16;
+  a->scale = scale;
+  a->timeout_ns = wait_timeout_ns();
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" attn_status attn_kl_fwd(const void* Q1, const void* K1, const void* Q2, const void* K2, float* KL,
+                                   float* LSE1, float* LSE2, int B, int H, int Nq, int Nk, int d, int causal,
+                                   float scale, attn_dtype dtype, void* stream) {
+  if (!KL || !LSE1 || !LSE2) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(KL) || !aligned16(LSE1) || !aligned16(LSE2)) return ATTN_ERR_MISALIGNED;
+  KlArgs a;
+  DeviceState* ds = nullptr;
+  attn_status st = kl_common(Q1, K1, Q2, K2, B, H, Nq, Nk, d, causal, scale, dtype, &a, &ds);
+  if (st != ATTN_OK) return st;
+  a.kl = KL;
+  a.lse1 = LSE1;
+  a.lse2 = LSE2;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return finish(launch_kl_fwd(a, s), s);
+}
+
+extern "C" attn_status attn_kl_bwd(const void* Q1, const void* K1, const void* Q2, const void* K2, const float* KL,
+                                   const float* LSE1, const float* LSE2, const float* G, int setting, void* dQ,
+                                   void* dK, int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                                   attn_dtype dtype, void* stream) {
+  if (setting != 1 && setting != 2) return ATTN_ERR_INVALID_ARG;
+  if (!KL || !LSE1 || !LSE2 || !G || !dQ || !dK) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(KL) || !aligned16(LSE1) || !aligned16(LSE2) || !aligned16(G) || !aligned16(dQ) || !aligned16(dK))
+    return ATTN_ERR_MISALIGNED;
+  KlArgs a;
+  DeviceState* ds = nullptr;
+  attn_status st = kl_common(Q1, K1, Q2, K2, B, H, Nq, Nk, d, causal, scale, dtype, &a, &ds);
+  if (st != ATTN_OK) return st;
+  const bool bf16 = dtype == ATTN_BF16;
+  CUresult r;
+  if ((r = encode_map(&a.tm_dk, dK, bf16, B, H, Nk, d, contiguous(H, Nk, d))) != CUDA_SUCCESS)
+    return driver_fail("cuTensorMapEncodeTiled", r);
+  a.kl = const_cast<float*>(KL);
+  a.lse1 = const_cast<float*>(LSE1);
+  a.lse2 = const_cast<float*>(LSE2);
+  a.g = G;
+  a.op = setting == 1 ? kPairKlStudent : kPairKlTeacher;
+  // dQ over query tiles (teacher a, student b)
+  PairDqArgs p;
+  std::memset(&p, 0, sizeof(p));
+  p.tm_qa = a.tm_qa;
+  p.tm_ka = a.tm_ka;
+  p.tm_qb = a.tm_qb;
+  p.tm_kb = a.tm_kb;
+  if ((r = encode_map(&p.tm_dq, dQ, bf16, B, H, Nq, d, contiguous(H, Nq, d))) != CUDA_SUCCESS)
+    return driver_fail("cuTensorMapEncodeTiled", r);
+  p.rv[0] = LSE1;
+  p.rv[1] = LSE2;
+  p.rv[2] = KL;
+  p.rv[3] = G;
+  p.rv_stride = Nq;
+  p.err_word = a.err_word;
+  p.bh_count = a.bh_count;
+  p.heads = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.d = d;
+  p.causal = a.causal;
+  p.bf16 = bf16;
+  p.causal_off = a.causal_off;
+  p.scale = scale;
+  p.op = a.op;
+  p.timeout_ns = a.timeout_ns;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_pair_dq(p, s);
+  if (e == cudaSuccess) e = launch_kl_dk(a, s);
+  return finish(e, s);
+}

@@ -66,6 +66,44 @@ struct SplitArgs {
   uint64_t timeout_ns;
 };
 
+// Query-tile gradient kernel: for one 128-row query tile, over the key tiles it sees in increasing order,
+//   S_a = Q_a K_a^T, S_b = Q_b K_b^T, dS = f(S_a, S_b, per-row values), dQ += dS K_dq,
+// with dQ accumulated on chip and stored once (times scale): the same bits on every run.  Used by the
+// attention backward's deterministic mode (a = (Q, K), b = (dO, V), K_dq = K) and by the attention-KL
+// backward (a = teacher, b = student, K_dq = the trained distribution's keys).
+constexpr int kPairAttn = 0, kPairKlStudent = 1, kPairKlTeacher = 2;
+
+struct PairDqArgs {
+  CUtensorMap tm_qa, tm_ka, tm_qb, tm_kb, tm_dq;
+  // per-row values, [B*H][rv_stride]: attention: base-2 LSE, D; KL: LSE1, LSE2, KL, upstream gradient g
+  const float* rv[4];
+  int rv_stride;
+  uint32_t* err_word;
+  int bh_count, heads, Nq, Nk, d;
+  bool causal, bf16;
+  int causal_off;
+  float scale;
+  int op;  // kPairAttn, kPairKlStudent, kPairKlTeacher
+  uint64_t timeout_ns;
+};
+
+// Attention KL divergence (teacher a = (Q1, K1), student b = (Q2, K2)).
+struct KlArgs {
+  CUtensorMap tm_qa, tm_ka, tm_qb, tm_kb;  // 4-D maps as in FwdArgs
+  CUtensorMap tm_dk;                       // backward: dK of the trained distribution
+  float* kl;                               // [B*H][Nq]: forward output, backward input
+  float* lse1;                             // [B*H][Nq]
+  float* lse2;                             // [B*H][Nq]
+  const float* g;                          // [B*H][Nq]: upstream gradient (backward)
+  uint32_t* err_word;
+  int bh_count, heads, Nq, Nk, d;
+  bool causal, bf16;
+  int causal_off;
+  float scale;
+  int op;  // backward: kPairKlStudent or kPairKlTeacher
+  uint64_t timeout_ns;
+};
+
 // Backward steps (bit mask for launch_bwd).  The atomic dQ mode runs pre, main, convert; the
 // deterministic mode (dq_acc == nullptr) runs pre, main (dK and dV only), then the dQ kernel.
 constexpr int kBwdPre = 1, kBwdMain = 2, kBwdConvert = 4, kBwdAll = 7, kBwdDq = 8;
@@ -79,5 +117,8 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_split(const SplitArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, int steps, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_pair_dq(const PairDqArgs& a, cudaStream_t stream);
+cudaError_t launch_kl_fwd(const KlArgs& a, cudaStream_t stream);
+cudaError_t launch_kl_dk(const KlArgs& a, cudaStream_t stream);
 
 }  // namespace exattn

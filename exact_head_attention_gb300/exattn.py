@@ -80,6 +80,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_bwd_strided_ex.argtypes = [vp, st, vp, st, vp, st, vp, st, vp, st, vp, vp, st, vp, st, vp, st,
                                                 i, i, i, i, i, i, f, i, i, vp, sz, vp]
             lib.attn_bwd_strided_ex.restype = i
+            lib.attn_kl_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+            lib.attn_kl_fwd.restype = i
+            lib.attn_kl_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, f, i, vp]
+            lib.attn_kl_bwd.restype = i
             lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
             lib.attn_bwd_workspace_size.restype = sz
             for name in ("attn_bwd",) + BWD_STEPS:
@@ -312,3 +316,66 @@ def attention(q, k, v, causal=False, scale: float | None = None, dq_mode="atomic
     dq_mode: "atomic", "deterministic" or "auto")."""
     scale = (1.0 / q.shape[-1] ** 0.5) if scale is None else scale
     return _AttnFunction.apply(q, k, v, causal, scale, dq_mode)
+
+
+# ------------------------------------------------------------------ attention KL divergence
+
+KL_SETTINGS = {"student": 1, "teacher": 2, 1: 1, 2: 2}
+
+
+def kl_fwd_raw(q1, k1, q2, k2, kl, lse1, lse2, causal, scale: float, stream=None) -> int:
+    """Calls attn_kl_fwd on caller-provided contiguous tensors; returns the status code."""
+    B, H, Nq, Nk, d = _dims(q1, k1)
+    return load().attn_kl_fwd(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(kl), _ptr(lse1), _ptr(lse2), B, H, Nq,
+                              Nk, d, mask_code(causal), float(scale), _dtype_code(q1), _stream(stream))
+
+
+def kl_bwd_raw(q1, k1, q2, k2, kl, lse1, lse2, g, setting, dq, dk, causal, scale: float, stream=None) -> int:
+    """Calls attn_kl_bwd on caller-provided contiguous tensors; returns the status code."""
+    B, H, Nq, Nk, d = _dims(q1, k1)
+    return load().attn_kl_bwd(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(kl), _ptr(lse1), _ptr(lse2), _ptr(g),
+                              KL_SETTINGS[setting], _ptr(dq), _ptr(dk), B, H, Nq, Nk, d, mask_code(causal),
+                              float(scale), _dtype_code(q1), _stream(stream))
+
+
+def kl_forward(q1, k1, q2, k2, causal=False, scale: float | None = None, stream=None):
+    """Row-wise KL(P1 || P2) of the student (q2, k2) from the teacher (q1, k1): (KL, LSE1, LSE2) [B,H,Nq] fp32."""
+    B, H, Nq, Nk, d = _dims(q1, k1)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    kl, lse1, lse2 = (torch.empty((B, H, Nq), dtype=torch.float32, device=q1.device) for _ in range(3))
+    _check(kl_fwd_raw(q1, k1, q2, k2, kl, lse1, lse2, causal, scale, stream), "attn_kl_fwd")
+    return kl, lse1, lse2
+
+
+def kl_backward(q1, k1, q2, k2, kl, lse1, lse2, g, train="student", causal=False, scale: float | None = None,
+                stream=None):
+    """(dQ, dK) of sum(g * KL) for the trained distribution ("student": Q2, K2; "teacher": Q1, K1)."""
+    B, H, Nq, Nk, d = _dims(q1, k1)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    dq, dk = torch.empty_like(q1), torch.empty_like(k1)
+    _check(kl_bwd_raw(q1, k1, q2, k2, kl, lse1, lse2, g.contiguous().float(), train, dq, dk, causal, scale, stream),
+           "attn_kl_bwd")
+    return dq, dk
+
+
+class _KlFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q1, k1, q2, k2, causal, scale, train):
+        kl, lse1, lse2 = kl_forward(q1, k1, q2, k2, causal, scale)
+        ctx.save_for_backward(q1, k1, q2, k2, kl, lse1, lse2)
+        ctx.causal, ctx.scale, ctx.train = causal, scale, train
+        return kl
+
+    @staticmethod
+    def backward(ctx, g):
+        q1, k1, q2, k2, kl, lse1, lse2 = ctx.saved_tensors
+        dq, dk = kl_backward(q1, k1, q2, k2, kl, lse1, lse2, g, ctx.train, ctx.causal, ctx.scale)
+        if KL_SETTINGS[ctx.train] == 1:
+            return None, None, dq, dk, None, None, None
+        return dq, dk, None, None, None, None, None
+
+
+def attention_kl(q1, k1, q2, k2, causal=False, scale: float | None = None, train="student"):
+    """Autograd-aware row-wise KL(P1 || P2) [B,H,Nq]; gradients flow to the trained distribution only."""
+    scale = (1.0 / q1.shape[-1] ** 0.5) if scale is None else scale
+    return _KlFunction.apply(q1, k1, q2, k2, causal, scale, train)

@@ -42,7 +42,7 @@ class Workload:
     sigma_qk: float = 1.0
     sigma_v: float = 1.0
     sigma_do: float = 1.0
-    kind: str = "train"  # "train": forward + backward; "decode": forward only (split-KV)
+    kind: str = "train"  # "train": forward + backward; "decode": forward only (split-KV); "kl": attention KL
 
     @property
     def scale(self) -> float:
@@ -73,7 +73,12 @@ WORKLOADS = {
                                           "bottom_right", kind="decode"),
     "chunk_q64_kv16k_d64_fp16": Workload("chunk_q64_kv16k_d64_fp16", 8, 4, 16, 64, 16384, 64, "fp16",
                                          "bottom_right", kind="decode"),
+    # attention KL divergence (teacher and student attention of one layer)
+    "kl8k_causal_bf16": Workload("kl8k_causal_bf16", 9, 1, 12, 8192, 8192, 128, "bf16", True, kind="kl"),
 }
+
+# Student queries and keys of the KL workloads: the teacher's plus noise of this standard deviation.
+KL_STUDENT_NOISE = 0.5
 
 # The workload the throughput metric is quoted on.
 HEADLINE = "long8k_causal_bf16"
@@ -100,6 +105,22 @@ def make_inputs(w: Workload, seed_offset: int = 0, with_grad_out: bool = True) -
     if with_grad_out:
         out["do"] = _normal((w.B, w.H, w.Nq, w.d), base + 3, w.sigma_do, dt)
     return out
+
+
+def make_kl_inputs(w: Workload, seed_offset: int = 0) -> dict:
+    """CPU tensors q1, k1 (teacher), q2, k2 (student) in the workload dtype and the upstream gradient g (fp32).
+
+    The student's queries and keys are the teacher's plus independent noise (a student close to its
+    teacher, as in attention distillation), drawn before rounding to the dtype.  Tensor indices: q1=0,
+    k1=1, noise of q2=2, noise of k2=3, g=4."""
+    base = 1000 * w.index + seed_offset
+    dt = w.torch_dtype
+    q1 = _normal((w.B, w.H, w.Nq, w.d), base + 0, w.sigma_qk, torch.float32)
+    k1 = _normal((w.B, w.H, w.Nk, w.d), base + 1, w.sigma_qk, torch.float32)
+    q2 = q1 + _normal((w.B, w.H, w.Nq, w.d), base + 2, KL_STUDENT_NOISE, torch.float32)
+    k2 = k1 + _normal((w.B, w.H, w.Nk, w.d), base + 3, KL_STUDENT_NOISE, torch.float32)
+    g = _normal((w.B, w.H, w.Nq), base + 4, 1.0, torch.float32)
+    return {"q1": q1.to(dt), "k1": k1.to(dt), "q2": q2.to(dt), "k2": k2.to(dt), "g": g}
 
 
 def custom(B: int, H: int, Nq: int, Nk: int, d: int, dtype: str = "bf16", causal: bool | str = False,

@@ -165,6 +165,41 @@ int attn_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int d, int sm_coun
 size_t attn_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
 
 /*
+ * Attention KL divergence (the StreamKL summary, Methodology 1): a teacher
+ * distribution P1 = softmax(scale Q1 K1^T) and a student P2 = softmax(scale
+ * Q2 K2^T) over the same key positions (and the same attn_mask), and the
+ * row-wise divergence of the student from the teacher
+ *   KL_q = sum_k P1_qk (log P1_qk - log P2_qk)
+ * computed in one pass with five running scalars per row, without forming
+ * either distribution.  Q1, Q2 [B,H,Nq,d] and K1, K2 [B,H,Nk,d] 16-bit,
+ * contiguous; outputs KL, LSE1, LSE2 [B,H,Nq] fp32 (LSE_t in natural-log
+ * units, as attn_fwd).  A row that sees no key gets KL = 0 and LSE = -inf.
+ * Errors as attn_fwd.
+ */
+attn_status attn_kl_fwd(const void* Q1, const void* K1, const void* Q2, const void* K2, float* KL, float* LSE1,
+                        float* LSE2, int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                        attn_dtype dtype, void* stream);
+
+/*
+ * Gradients of sum_q G_q KL_q (Methodology 2: probabilities regenerated from
+ * the stored LSEs) for one distribution:
+ *   setting 1, the student is trained (teacher fixed):
+ *     dS = G (P2 - P1);                 dQ, dK are gradients w.r.t. Q2, K2
+ *   setting 2, the teacher is trained (student fixed):
+ *     dS = G P1 (log P1 - log P2 - KL); dQ, dK are gradients w.r.t. Q1, K1
+ * with dQ = scale dS K and dK = scale dS^T Q of that distribution.  KL, LSE1,
+ * LSE2 as written by attn_kl_fwd; G [B,H,Nq] fp32; dQ [B,H,Nq,d] and dK
+ * [B,H,Nk,d] 16-bit outputs.  Two launches: dQ over query tiles and dK over
+ * key tiles, each visiting every (query tile, key tile) pair once, no atomics:
+ * the same bits on every run.  Errors as attn_fwd, plus ATTN_ERR_INVALID_ARG
+ * for a setting other than 1 or 2.
+ */
+attn_status attn_kl_bwd(const void* Q1, const void* K1, const void* Q2, const void* K2, const float* KL,
+                        const float* LSE1, const float* LSE2, const float* G, int setting, void* dQ, void* dK,
+                        int B, int H, int Nq, int Nk, int d, int causal, float scale, attn_dtype dtype,
+                        void* stream);
+
+/*
  * Bytes of device workspace attn_bwd needs for this shape: an fp32 dQ
  * accumulator [B,H,ceil(Nq/128)*128,d] plus two fp32 row vectors of the same
  * padded length (D = rowsum(dO o O) and the base-2 LSE).  Returns 0 for

@@ -171,3 +171,17 @@ def test_bwd_ex_rejects_unknown_dq_mode(lib):
         assert lib.attn_bwd_ex(*p, 1, 1, 128, 128, 64, 0, 0.125, 0, mode, ctypes.c_void_p(FAKE), need, None) == 1
     # a valid mode still stops at the misaligned workspace, before any launch
     assert lib.attn_bwd_ex(*p, 1, 1, 128, 128, 64, 0, 0.125, 0, 1, ctypes.c_void_p(FAKE + 16), need, None) == 3
+
+
+def test_kl_rejects_bad_arguments(lib):
+    p4 = [ctypes.c_void_p(FAKE)] * 4
+    f3 = [ctypes.c_void_p(FAKE)] * 3
+    assert lib.attn_kl_fwd(*p4, *f3, 0, 1, 128, 128, 64, 0, 0.125, 0, None) == 1
+    assert lib.attn_kl_fwd(*p4, *f3, 1, 1, 128, 128, 96, 0, 0.125, 0, None) == 2
+    assert lib.attn_kl_fwd(*p4, ctypes.c_void_p(FAKE + 4), *f3[1:], 1, 1, 128, 128, 64, 0, 0.125, 0, None) == 3
+    assert lib.attn_kl_fwd(*p4, *f3, 1, 1, 128, 128, 64, 3, 0.125, 0, None) == 1
+    g = [ctypes.c_void_p(FAKE)] * 4  # KL, LSE1, LSE2, G
+    out = [ctypes.c_void_p(FAKE)] * 2
+    for setting in (0, 3, -1):
+        assert lib.attn_kl_bwd(*p4, *g, setting, *out, 1, 1, 128, 128, 64, 0, 0.125, 0, None) == 1
+    assert lib.attn_kl_bwd(*p4, *g, 1, ctypes.c_void_p(FAKE + 2), out[1], 1, 1, 128, 128, 64, 0, 0.125, 0, None) == 3
