@@ -18,6 +18,11 @@ runs an independent replica of the workload (no collective on the data path).
 --impl reference times the CPU oracle (the plain fp64 definition) on the host
 cores instead, on bounded samples of the same workload.
 
+--workload kl8k_causal_bf16 times the attention KL divergence instead: one
+step is attn_kl_fwd and attn_kl_bwd (the student trained), at 2 + 4 tile
+products per (query tile, key tile) pair (the backward recomputes both score
+tiles in each of its two kernels: 6 executed).
+
 --workload NAME picks another workload.  A decoding workload (few queries over a
 long key/value cache) times one split-KV forward (attn_fwd_splitkv: the slice
 kernel and the merge kernel) per step and reports the bandwidth of its
@@ -83,6 +88,8 @@ def config_dict(w, extra=None) -> dict:
          "dtype": w.dtype, "sigma_qk": w.sigma_qk}
     if w.kind == "decode":
         c.update(kind="decode", bytes_per_step=decode_bytes(w), flops_per_step=4.0 * w.B * w.H * w.d * visible_pairs(w))
+    elif w.kind == "kl":
+        c.update(kind="kl", flops_per_step=sum(kl_flops(w)))
     else:
         c["flops_per_step"] = sum(step_flops(w))
     if extra:
@@ -417,6 +424,189 @@ def run_decode(args, w, rank: int, world: int) -> None:
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ attention KL workloads
+
+KL_METRIC = "attention KL divergence fwd+bwd TFLOPS (causal-adjusted; 2 forward + 4 backward score-sized products)"
+
+
+def kl_flops(w) -> tuple[float, float]:
+    one = 2.0 * w.B * w.H * w.Nq * w.Nk * w.d * (0.5 if w.causal else 1.0)  # one score-sized product
+    return 2 * one, 4 * one
+
+
+def _oracle_kl_step(x, w, n: int) -> float:
+    import oracle
+    sel = {k: v[:1, :1, :n] for k, v in x.items()}  # head (0, 0), first n rows (and keys)
+    t = time.perf_counter()
+    oracle.kl_fwd(sel["q1"], sel["k1"], sel["q2"], sel["k2"], w.causal, w.scale)
+    oracle.kl_bwd(sel["q1"], sel["k1"], sel["q2"], sel["k2"], sel["g"], 1, w.causal, w.scale)
+    return time.perf_counter() - t
+
+
+def _kl_sample_flops(w, n: int) -> float:
+    return 6.0 * 2.0 * n * n * w.d * (0.5 if w.causal else 1.0)
+
+
+def _kl_pick_n(x, w, budget_s: float) -> int:
+    import oracle
+    oracle.build()
+    n0 = min(256, w.Nq, w.Nk)
+    t0 = max(_oracle_kl_step(x, w, n0), 1e-4)
+    n = int(n0 * math.sqrt(budget_s / t0))
+    n = max(64, min(n, w.Nq, w.Nk))
+    return n - n % 64 if n >= 128 else n
+
+
+def run_kl(args, w, rank: int, world: int) -> None:
+    from exact_head_attention_gb300 import workloads
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        x = workloads.make_kl_inputs(w)
+        n = _kl_pick_n(x, w, max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup))))
+        for _ in range(args.warmup):
+            _oracle_kl_step(x, w, n)
+        mean = statistics.mean(_oracle_kl_step(x, w, n) for _ in range(args.steps))
+        value = _kl_sample_flops(w, n) / mean / 1e12
+        sample = f"per step: fp64 oracle KL forward + student backward of head (0,0), first {n} queries and keys, 1 thread"
+        print(json.dumps({
+            "impl": "reference", "metric": KL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w, {"sample_n": n}),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
+
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from exact_head_attention_gb300 import build as _build
+    from exact_head_attention_gb300 import exattn
+    _build.build()
+    exattn.load()
+
+    x = workloads.make_kl_inputs(w, seed_offset=10 * rank)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = _kl_pick_n(x, w, 15.0)
+        dt = _oracle_kl_step(x, w, n)
+        cpu = {"value": _kl_sample_flops(w, n) / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"fp64 oracle KL forward + student backward of head (0,0), first {n} queries and keys, "
+                         f"{dt:.1f} s on 1 thread (host has {len(os.sched_getaffinity(0))} cores available)"}
+
+    stream = torch.cuda.current_stream()
+    d = {k: v.to(dev) for k, v in x.items()}
+    kl, l1, l2 = (torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev) for _ in range(3))
+    dq, dk = torch.empty_like(d["q2"]), torch.empty_like(d["k2"])
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def launch(ev=None):
+        s1 = exattn.kl_fwd_raw(d["q1"], d["k1"], d["q2"], d["k2"], kl, l1, l2, w.causal, w.scale)
+        if ev:
+            ev[1].record(stream)
+        s2 = exattn.kl_bwd_raw(d["q1"], d["k1"], d["q2"], d["k2"], kl, l1, l2, d["g"], "student", dq, dk, w.causal,
+                               w.scale)
+        if ev:
+            ev[2].record(stream)
+        if s1 or s2:
+            raise RuntimeError(f"C-ABI status {(s1, s2)}: {exattn.last_error()}")
+
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    if exattn.check_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+    props = torch.cuda.get_device_properties(dev)
+    sampler = ClockSampler(getattr(props, "uuid", None) and f"GPU-{props.uuid}")
+    for _ in range(args.warmup):
+        launch()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record(stream)
+        launch(evs[i])
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    if exattn.check_device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    ms_per_step = max_over_ranks(fwd_ms + bwd_ms, dist, dev)
+
+    # end to end: pinned host Q1, K1, Q2, K2, g -> device -> forward + backward -> host KL, dQ2, dK2
+    h = {k: v.pin_memory() for k, v in x.items()}
+    hkl = torch.empty(kl.shape, dtype=torch.float32).pin_memory()
+    hdq, hdk = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk))
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = sum(t.numel() * t.element_size() for t in (hkl, hdq, hdk))
+
+    def e2e_step():
+        for k_ in d:
+            d[k_].copy_(h[k_], non_blocking=True)
+        launch()
+        hkl.copy_(kl, non_blocking=True)
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ms = []
+    for i in range(args.e2e_steps):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e_ms.append(a.elapsed_time(b))
+    sampler.stop()
+    e2e_ms = max_over_ranks(statistics.mean(e_ms) if e_ms else float("nan"), dist, dev)
+
+    ff, bf = kl_flops(w)
+    pk = peaks()
+    achieved = bf / (bwd_ms * 1e-3) / 1e12
+    line = {
+        "metric": KL_METRIC, "value": world * (ff + bf) / (ms_per_step * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "fp16",
+        "data": "synthetic: seeded normal teacher Q,K (sigma 1); student = teacher + noise (sigma %.2g); g ~ N(0,1)"
+                % workloads.KL_STUDENT_NOISE,
+        "config": config_dict(w, {"kind": "kl", "train": "student", "flops_per_step": ff + bf,
+                                  "parallelism": "replicas" if world > 1 else "single GPU",
+                                  "l2": "256 MiB flush write between timed steps, outside the CUDA events"}),
+        "kernels_ms": {"kl_fwd": fwd_ms, "kl_bwd (dQ + dK kernels)": bwd_ms},
+        "fwd_tflops": ff / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": achieved,
+        "roofline": {"kernel": "pair_dq_kernel + kl_dk_kernel (attn_kl_bwd)", "bound": "tensor", "achieved": achieved,
+                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                     "traffic": None, "peak_kind": f"bf16 dense burst ({pk['source']})"},
+        "cpu_baseline": cpu,
+        "e2e": ({"value": world * (ff + bf) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms} if e_ms else None),
+        "gpu_launches": 3 * args.steps,
+        "clocks": sampler.summary(t_wall0, t_wall1),
+        "wall_s_timed_region": t_wall1 - t_wall0,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
 def main() -> None:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -435,6 +625,9 @@ def main() -> None:
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if w.kind == "decode":
         run_decode(args, w, rank, world)
+        return
+    if w.kind == "kl":
+        run_kl(args, w, rank, world)
         return
 
     if args.impl == "reference":
