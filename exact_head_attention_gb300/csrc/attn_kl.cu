@@ -73,6 +73,73 @@ struct KlFwdBars {
 // exp2(x - m) with m = -inf (a row without a visible key so far) treated as 0; masked x are -inf.
 __device__ __forceinline__ float base_of(float m) { return m == -INFINITY ? 0.f : m; }
 
+// One key tile of the five-scalar update for this thread's query row: reads the tile's raw teacher and
+// student scores from TMEM twice (tile maxima, then sums), rescales l_a, acc (by the teacher's max
+// change) and l_b (the student's), and adds
+//     l_a += sum exp2(s_a c - m_a),  l_b += sum exp2(s_b c - m_b),  acc += sum exp2(s_a c - m_a) (s_a - s_b)
+// (c = scale log2 e; acc in raw score units).  With MASKED, columns at or past `lim` take no part.  The
+// two distributions' exponent arguments and sums travel as fp32 pairs.
+template <bool MASKED>
+__device__ __forceinline__ void kl_tile(uint32_t tA, uint32_t tB, int lim, float c_log2, float& ma, float& mb,
+                                        float& la, float& lb, float& acc) {
+  float xa[2] = {-INFINITY, -INFINITY}, xb[2] = {-INFINITY, -INFINITY};
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t va[32], vb[32];
+    tmem_ld32(tA + c * 32, va);
+    tmem_ld32(tB + c * 32, vb);
+    tmem_wait_ld();
+    reg_fence32(va);
+    reg_fence32(vb);
+    if constexpr (MASKED) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (c * 32 + i >= lim) va[i] = vb[i] = __float_as_uint(-INFINITY);
+    }
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+      xa[p & 1] = max3(xa[p & 1], __uint_as_float(va[2 * p]), __uint_as_float(va[2 * p + 1]));
+      xb[p & 1] = max3(xb[p & 1], __uint_as_float(vb[2 * p]), __uint_as_float(vb[2 * p + 1]));
+    }
+  }
+  const float na = fmaxf(ma, fmaxf(xa[0], xa[1]) * c_log2), nb = fmaxf(mb, fmaxf(xb[0], xb[1]) * c_log2);
+  const float alpha_a = na == ma ? 1.f : ex2_approx(ma - na), alpha_b = nb == mb ? 1.f : ex2_approx(mb - nb);
+  la *= alpha_a;
+  acc *= alpha_a;
+  lb *= alpha_b;
+  ma = na;
+  mb = nb;
+  const uint64_t c2 = f2_pack(c_log2, c_log2), nbase = f2_pack(-base_of(ma), -base_of(mb));
+  uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};  // (l_a, l_b) partial sums
+  float ac2[2] = {0.f, 0.f};
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t va[32], vb[32];
+    tmem_ld32(tA + c * 32, va);
+    tmem_ld32(tB + c * 32, vb);
+    tmem_wait_ld();
+    reg_fence32(va);
+    reg_fence32(vb);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float sa = __uint_as_float(va[i]), sb = __uint_as_float(vb[i]);
+      float xa2, xb2;
+      f2_unpack(f2_fma(f2_pack(sa, sb), c2, nbase), xa2, xb2);
+      float ea = ex2_approx(xa2), eb = ex2_approx(xb2), df = sa - sb;
+      if constexpr (MASKED) {
+        if (c * 32 + i >= lim) ea = eb = df = 0.f;
+      }
+      sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(ea, eb));
+      ac2[i & 1] = fmaf(ea, df, ac2[i & 1]);
+    }
+  }
+  float sa_, sb_;
+  f2_unpack(f2_add(sum2[0], sum2[1]), sa_, sb_);
+  la += sa_;
+  lb += sb_;
+  acc += ac2[0] + ac2[1];
+}
+
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(kKlFwdThreads, 1) kl_fwd_kernel(const __grid_constant__ KlArgs a) {
   using C = KlFwdCfg<D>;
@@ -201,57 +268,12 @@ __global__ void __launch_bounds__(kKlFwdThreads, 1) kl_fwd_kernel(const __grid_c
       const bool need_mask =
           ((j + 1) * kTileRows > a.Nk) || (CAUSAL && j * kTileRows + kTileRows - 1 > q0 + coff);
       const int lim = need_mask ? (CAUSAL ? min(a.Nk, row + coff + 1) : a.Nk) - j * kTileRows : kTileRows;
-      // pass 1: tile maxima
-      float xa = -INFINITY, xb = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t va[32], vb[32];
-        tmem_ld32(tA + c * 32, va);
-        tmem_ld32(tB + c * 32, vb);
-        tmem_wait_ld();
-        reg_fence32(va);
-        reg_fence32(vb);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const bool keep = !need_mask || c * 32 + i < lim;
-          xa = keep ? fmaxf(xa, __uint_as_float(va[i])) : xa;
-          xb = keep ? fmaxf(xb, __uint_as_float(vb[i])) : xb;
-        }
-      }
-      const float na = fmaxf(ma, xa * c_log2), nb = fmaxf(mb, xb * c_log2);
-      const float alpha_a = na == ma ? 1.f : ex2_approx(ma - na), alpha_b = nb == mb ? 1.f : ex2_approx(mb - nb);
-      la *= alpha_a;
-      acc *= alpha_a;
-      lb *= alpha_b;
-      ma = na;
-      mb = nb;
-      const float ba = base_of(ma), bb = base_of(mb);
-      // pass 2: sums and the weighted logit difference (two independent chains each)
-      float sa2[2] = {0.f, 0.f}, sb2[2] = {0.f, 0.f}, ac2[2] = {0.f, 0.f};
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t va[32], vb[32];
-        tmem_ld32(tA + c * 32, va);
-        tmem_ld32(tB + c * 32, vb);
-        tmem_wait_ld();
-        reg_fence32(va);
-        reg_fence32(vb);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float sa = __uint_as_float(va[i]), sb = __uint_as_float(vb[i]);
-          float ea = ex2_approx(fmaf(sa, c_log2, -ba)), eb = ex2_approx(fmaf(sb, c_log2, -bb));
-          float df = sa - sb;
-          if (need_mask && c * 32 + i >= lim) ea = eb = df = 0.f;
-          sa2[i & 1] += ea;
-          sb2[i & 1] += eb;
-          ac2[i & 1] = fmaf(ea, df, ac2[i & 1]);
-        }
-      }
+      if (need_mask)
+        kl_tile<true>(tA, tB, lim, c_log2, ma, mb, la, lb, acc);
+      else
+        kl_tile<false>(tA, tB, lim, c_log2, ma, mb, la, lb, acc);
       tc_fence_before();
-      mbar_arrive(bars.s_free(t));  // both score tiles are in registers no more: the buffer may be refilled
-      la += sa2[0] + sa2[1];
-      lb += sb2[0] + sb2[1];
-      acc += ac2[0] + ac2[1];
+      mbar_arrive(bars.s_free(t));  // both score tiles were read: the buffer may be refilled
     }
 
     // ------------------------------------------------------------ merge the two warpgroups' states
