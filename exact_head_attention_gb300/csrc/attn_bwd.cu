@@ -32,7 +32,8 @@
 //   Y  = [128,256)  dQ_i (d = 64: lane = query row) or dQ_i^T (d = 128: lane = d)
 //   dV = [256,256+d), dK = [384,384+d)
 // Shared memory: K_j, V_j, dS^T (the dQ MMA's operand), the Q/dO ring.
-// Per tile i the MMA issue order is dV_i, dK_i, S_{i+1}, dQ_i, dP_{i+1}: the
+// Per tile i the MMA issue order is dV_i, dK_i, S_{i+1}, dQ_i, dP_{i+1}: dV_i
+// starts as soon as P^T_i is in TMEM and overlaps the forming of dS^T_i, the
 // exponentials of tile i+1 overlap dQ_i and dP_{i+1}, and the dQ_i reduction
 // (issued by the compute warps after they hand over tile i+1) overlaps the
 // next tile's MMAs.
@@ -68,8 +69,8 @@ struct BwdCfg {
   static constexpr uint32_t ROWV_BYTES = 2 * 128 * 4;
   static constexpr uint32_t OFF_BAR = OFF_ROWV + 2 * ROWV_BYTES;
   // kv_full, ring_full[NR], ring_empty[NR], s_full, s_used, dp_full, pd_ready, ds_empty,
-  // dq_full, dq_empty, done, mma_done, rowv_full[2], rowv_empty[2], dss_ready, dstile_free
-  static constexpr int NBAR = 1 + 2 * NR + 15;
+  // dq_full, dq_empty, done, mma_done, rowv_full[2], rowv_empty[2], dss_ready, dstile_free, p_ready
+  static constexpr int NBAR = 1 + 2 * NR + 16;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   // The operand tiles need 1024-byte alignment; the dynamic shared memory base is checked at entry
@@ -92,6 +93,7 @@ struct BwdBars {
   __device__ uint32_t dss_ready() const { return at(13); } // dS^T in shared memory
   // d = 128: the copy engine has read warpgroup 1's dQ rows out of the dS^T tile
   __device__ uint32_t dstile_free() const { return at(14); }
+  __device__ uint32_t p_ready() const { return at(15); }   // P^T packed in TMEM X (dV may go)
   __device__ uint32_t ds_empty() const { return at(4); }
   __device__ uint32_t dq_full() const { return at(5); }
   __device__ uint32_t dq_empty() const { return at(6); }
@@ -145,6 +147,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     mbar_init(bars.s_used(), 256);
     mbar_init(bars.dp_full(), 1);
     mbar_init(bars.pd_ready(), 256);
+    mbar_init(bars.p_ready(), 256);
     mbar_init(bars.dss_ready(), 256);
     mbar_init(bars.dstile_free(), 1);
     mbar_init(bars.ds_empty(), 1);
@@ -258,7 +261,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       if (ok) ok = issue_S(0);
       if (ok) ok = issue_dP(0);
       for (int it = 0; ok && it < n; ++it) {
-        if (!(ok = mbar_wait(bars.pd_ready(), it & 1, wc))) break;
+        // dV_i needs only P^T: it runs while the compute warps form dS^T
+        if (!(ok = mbar_wait(bars.p_ready(), it & 1, wc))) break;
         tc_fence_after();
         const uint32_t q_lo = ring_mn + slot_of(2 * it) * kTileLo;
         const uint32_t do_lo = ring_mn + slot_of(2 * it + 1) * kTileLo;
@@ -268,6 +272,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
 #pragma unroll
         for (int k = 1; k < 128 / 16; ++k) mma_ts_lo<true>(tdV, tX + packed_col(k, 0), do_lo + k * (2048 >> 4), idG);
         mma_commit(bars.ring_empty(slot_of(2 * it + 1)));
+        if (!(ok = mbar_wait(bars.pd_ready(), it & 1, wc))) break;
+        tc_fence_after();
         // dK += dS^T Q_i   (A: dS^T packed in TMEM X; B: Q_i [query][d] MN-major)
         mma_ts_lo_rt(tdK, tX + packed_col(0, 32), q_lo, idG, acc0);
 #pragma unroll
@@ -425,6 +431,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       reg_fence32(s[1]);
       // P^T into this half's first 32 columns of X: its dP^T values are in registers now.
       tmem_st32(tX + lane_bits + h * 64, pp);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bars.p_ready());  // dV_i may go
       // dS^T = P^T o (dP^T - D), into the half's next 32 columns of X and into the shared dS^T tile.
       uint32_t pk[32];
 #pragma unroll
@@ -445,7 +454,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       tmem_st32(tX + lane_bits + h * 64 + 32, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bars.pd_ready());  // dV_i, dK_i and S_{i+1} may go
+      mbar_arrive(bars.pd_ready());  // dK_i and S_{i+1} may go
       if constexpr (!DQ) continue;
       if (it > 0 && !(ok = mbar_wait_warp(bars.ds_empty(), (it - 1) & 1, wc))) break;
       if constexpr (D == 128) {
