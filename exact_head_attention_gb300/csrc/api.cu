@@ -14,6 +14,7 @@
 
 #include "../../include/exattn.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace exattn {
 namespace {
@@ -674,4 +675,41 @@ extern "C" attn_status attn_kl_bwd(const void* Q1, const void* K1, const void* Q
   cudaError_t e = launch_pair_dq(p, s);
   if (e == cudaSuccess) e = launch_kl_dk(a, s);
   return finish(e, s);
+}
+
+// ----------------------------------------------------------------- bounded-wait self-test
+
+namespace exattn {
+namespace {
+
+// One block; its first thread waits on an mbarrier that nothing arrives at, through the same bounded
+// wait the attention kernels use.  The wait gives up after timeout_ns, records the timeout in the error
+// word and the kernel returns normally.
+__global__ void selftest_wait_kernel(uint32_t* err_word, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_word;
+  if (threadIdx.x == 0) {
+    abort_word = 0u;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtx wc{&abort_word, err_word, timeout_ns};
+  if (threadIdx.x == 0) (void)mbar_wait(smem_u32(&bar), 0, wc);
+  __syncthreads();
+}
+
+}  // namespace
+}  // namespace exattn
+
+extern "C" attn_status attn_selftest_wait_timeout(int timeout_ms, void* stream) {
+  if (timeout_ms < 1 || timeout_ms > 10000) return ATTN_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  attn_status st = device_state(&ds);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  selftest_wait_kernel<<<1, 32, 0, s>>>(ds->err_word, static_cast<uint64_t>(timeout_ms) * 1000000ull);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail("kernel launch", e);
+  return attn_check_device_error(stream);
 }

@@ -84,6 +84,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_kl_fwd.restype = i
             lib.attn_kl_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, f, i, vp]
             lib.attn_kl_bwd.restype = i
+            lib.attn_selftest_wait_timeout.argtypes = [i, vp]
+            lib.attn_selftest_wait_timeout.restype = i
             lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
             lib.attn_bwd_workspace_size.restype = sz
             for name in ("attn_bwd",) + BWD_STEPS:
@@ -287,6 +289,12 @@ def backward(q, k, v, o, do, lse, causal=False, scale: float | None = None, work
         _check(bwd_strided_raw(q, k, v, o, do, lse, dq, dk, dv, causal, scale, workspace, stream),
                "attn_bwd_strided")
     return dq, dk, dv
+
+
+def selftest_wait_timeout(timeout_ms: int = 20, stream=None) -> int:
+    """Runs attn_selftest_wait_timeout: a bounded device wait that nothing satisfies.  Returns the status
+    (ATTN_ERR_TIMEOUT = 5 when the timeout path works)."""
+    return int(load().attn_selftest_wait_timeout(int(timeout_ms), _stream(stream)))
 
 
 def check_device_error(stream=None) -> int:

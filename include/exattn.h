@@ -323,6 +323,20 @@ attn_status attn_bwd_dq_convert(const void* Q, const void* K, const void* V, con
                                 attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Self-test of the bounded device waits.  Launches one block whose thread
+ * waits, through the same bounded wait the attention kernels use on their
+ * pipelines, on a shared-memory barrier that nothing ever arrives at.  After
+ * timeout_ms milliseconds the wait gives up, the kernel records
+ * ATTN_ERR_TIMEOUT in the device error word and returns normally: no fault,
+ * no trap, and the context stays usable.  The call then synchronises `stream`
+ * and returns what attn_check_device_error reports, so a working library
+ * returns ATTN_ERR_TIMEOUT (and clears the error word).  timeout_ms must be
+ * in [1, 10000] (ATTN_ERR_INVALID_ARG otherwise).  The pages have no
+ * counterpart: this is a check of the library's own failure detection.
+ */
+attn_status attn_selftest_wait_timeout(int timeout_ms, void* stream);
+
+/*
  * Backward for callers that cannot allocate device memory -- for example a
  * plugin inside an engine that owns all device memory and forbids allocation
  * while it runs, or a latency-bound loop that cannot risk an allocator call

@@ -185,3 +185,8 @@ def test_kl_rejects_bad_arguments(lib):
     for setting in (0, 3, -1):
         assert lib.attn_kl_bwd(*p4, *g, setting, *out, 1, 1, 128, 128, 64, 0, 0.125, 0, None) == 1
     assert lib.attn_kl_bwd(*p4, *g, 1, ctypes.c_void_p(FAKE + 2), out[1], 1, 1, 128, 128, 64, 0, 0.125, 0, None) == 3
+
+
+def test_selftest_rejects_bad_timeout(lib):
+    for ms in (0, -5, 10001):
+        assert lib.attn_selftest_wait_timeout(ms, None) == 1
