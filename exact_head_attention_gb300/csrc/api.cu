@@ -713,3 +713,54 @@ extern "C" attn_status attn_selftest_wait_timeout(int timeout_ms, void* stream) 
   if (e != cudaSuccess) return cuda_fail("kernel launch", e);
   return attn_check_device_error(stream);
 }
+
+// ----------------------------------------------------------------- attention KL: split-K forward
+
+namespace {
+
+size_t kl_split_workspace(int B, int H, int Nq, int splits) {
+  return align256(static_cast<size_t>(5) * splits * B * H * Nq * sizeof(float));
+}
+
+}  // namespace
+
+extern "C" size_t attn_kl_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128) || num_splits < 0 || num_splits > kMaxSplits)
+    return 0;
+  if (num_splits == 0) {
+    num_splits = attn_fwd_splitkv_num_splits(B, H, Nq, Nk, d, 0);
+    if (num_splits <= 1) return 0;
+  }
+  return kl_split_workspace(B, H, Nq, num_splits);
+}
+
+extern "C" attn_status attn_kl_fwd_splitkv(const void* Q1, const void* K1, const void* Q2, const void* K2, float* KL,
+                                           float* LSE1, float* LSE2, int B, int H, int Nq, int Nk, int d, int causal,
+                                           float scale, attn_dtype dtype, int num_splits, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  if (num_splits < 0 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  if (!KL || !LSE1 || !LSE2) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(KL) || !aligned16(LSE1) || !aligned16(LSE2)) return ATTN_ERR_MISALIGNED;
+  if (num_splits == 0) {
+    attn_status st = check_common(B, H, Nq, Nk, d, causal, scale, dtype);
+    if (st != ATTN_OK) return st;
+    const int sms = device_sm_count();
+    num_splits = choose_splits(static_cast<long long>(B) * H, Nq, Nk, sms > 0 ? sms : 1);
+    if (num_splits == 1)
+      return attn_kl_fwd(Q1, K1, Q2, K2, KL, LSE1, LSE2, B, H, Nq, Nk, d, causal, scale, dtype, stream);
+  }
+  if (!workspace || workspace_bytes < kl_split_workspace(B, H, Nq, num_splits)) return ATTN_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_MISALIGNED;
+  KlArgs a;
+  DeviceState* ds = nullptr;
+  attn_status st = kl_common(Q1, K1, Q2, K2, B, H, Nq, Nk, d, causal, scale, dtype, &a, &ds);
+  if (st != ATTN_OK) return st;
+  if (static_cast<long long>(B) * H * Nq > 0x7fffffffLL * 255LL) return ATTN_ERR_INVALID_ARG;
+  a.kl = KL;
+  a.lse1 = LSE1;
+  a.lse2 = LSE2;
+  a.part = static_cast<float*>(workspace);
+  a.splits = num_splits;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return finish(launch_kl_fwd(a, s), s);
+}

@@ -140,7 +140,10 @@ __device__ __forceinline__ void kl_tile(uint32_t tA, uint32_t tB, int lim, float
   acc += ac2[0] + ac2[1];
 }
 
-template <int D, bool CAUSAL, bool BF16>
+// SPLIT: the grid's z dimension divides the key tiles a query tile sees into a.splits contiguous
+// slices (the summary's split-K variant for few query rows); each block writes its slice's merged five
+// scalars to a.part and kl_combine_kernel forms KL and the LSEs.
+template <int D, bool CAUSAL, bool BF16, bool SPLIT>
 __global__ void __launch_bounds__(kKlFwdThreads, 1) kl_fwd_kernel(const __grid_constant__ KlArgs a) {
   using C = KlFwdCfg<D>;
   constexpr int NS = C::NS;
@@ -162,11 +165,15 @@ __global__ void __launch_bounds__(kKlFwdThreads, 1) kl_fwd_kernel(const __grid_c
   const int q0 = qt * kTileRows;
   const int nkv = (a.Nk + kTileRows - 1) / kTileRows;
   const int coff = CAUSAL ? a.causal_off : 0;
-  int n = nkv;
+  int nvis = nkv;  // key tiles this query tile sees
   if (CAUSAL) {
     const int last_key = q0 + kTileRows - 1 + coff;
-    n = last_key < 0 ? 0 : min(nkv, last_key / kTileRows + 1);
+    nvis = last_key < 0 ? 0 : min(nkv, last_key / kTileRows + 1);
   }
+  // this block's key tiles [j0, j0 + n): all of them, or one slice (slices differ by at most one tile)
+  const int split = SPLIT ? static_cast<int>(blockIdx.z) : 0, nsplit = SPLIT ? a.splits : 1;
+  const int j0 = static_cast<int>(static_cast<long long>(split) * nvis / nsplit);
+  const int n = static_cast<int>(static_cast<long long>(split + 1) * nvis / nsplit) - j0;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
@@ -212,8 +219,9 @@ __global__ void __launch_bounds__(kKlFwdThreads, 1) kl_fwd_kernel(const __grid_c
         mbar_arrive_expect_tx(bars.k_full(s), 2 * C::TILE);
         const uint32_t dst = sRing + s * 2 * C::TILE;
         for (int c = 0; c < C::NCH; ++c) {
-          tma_load_4d(dst + c * kChunkBytes, &a.tm_ka, c * 64, j * kTileRows, head, batch, bars.k_full(s));
-          tma_load_4d(dst + C::TILE + c * kChunkBytes, &a.tm_kb, c * 64, j * kTileRows, head, batch, bars.k_full(s));
+          tma_load_4d(dst + c * kChunkBytes, &a.tm_ka, c * 64, (j0 + j) * kTileRows, head, batch, bars.k_full(s));
+          tma_load_4d(dst + C::TILE + c * kChunkBytes, &a.tm_kb, c * 64, (j0 + j) * kTileRows, head, batch,
+                      bars.k_full(s));
         }
         ++issued;
       }
@@ -265,9 +273,10 @@ __global__ void __launch_bounds__(kKlFwdThreads, 1) kl_fwd_kernel(const __grid_c
     for (int j = t; ok && j < n; j += 2) {
       if (!(ok = mbar_wait_warp(bars.s_full(t), (j >> 1) & 1, wc))) break;
       tc_fence_after();
+      const int jg = j0 + j;  // key tile index
       const bool need_mask =
-          ((j + 1) * kTileRows > a.Nk) || (CAUSAL && j * kTileRows + kTileRows - 1 > q0 + coff);
-      const int lim = need_mask ? (CAUSAL ? min(a.Nk, row + coff + 1) : a.Nk) - j * kTileRows : kTileRows;
+          ((jg + 1) * kTileRows > a.Nk) || (CAUSAL && jg * kTileRows + kTileRows - 1 > q0 + coff);
+      const int lim = need_mask ? (CAUSAL ? min(a.Nk, row + coff + 1) : a.Nk) - jg * kTileRows : kTileRows;
       if (need_mask)
         kl_tile<true>(tA, tB, lim, c_log2, ma, mb, la, lb, acc);
       else
@@ -292,7 +301,16 @@ __global__ void __launch_bounds__(kKlFwdThreads, 1) kl_fwd_kernel(const __grid_c
       const float v0 = mb == -INFINITY ? 0.f : ex2_approx(mb - Mb), v1 = mb1 == -INFINITY ? 0.f : ex2_approx(mb1 - Mb);
       const float L_a = la * w0 + la1 * w1, L_b = lb * v0 + lb1 * v1, A = acc * w0 + ac1 * w1;
       const size_t o = static_cast<size_t>(bh) * a.Nq + row;
-      if (L_a > 0.f) {
+      if constexpr (SPLIT) {
+        // the slice's state: maxima (base 2), sums and acc, one plane each
+        const size_t plane = static_cast<size_t>(a.splits) * a.bh_count * a.Nq;
+        const size_t e = static_cast<size_t>(split) * a.bh_count * a.Nq + o;
+        a.part[e] = Ma;
+        a.part[plane + e] = Mb;
+        a.part[2 * plane + e] = L_a;
+        a.part[3 * plane + e] = L_b;
+        a.part[4 * plane + e] = A;
+      } else if (L_a > 0.f) {
         const float lse_a = (Ma + __log2f(L_a)) * 0.6931471805599453f;
         const float lse_b = (Mb + __log2f(L_b)) * 0.6931471805599453f;
         a.lse1[o] = lse_a;
@@ -589,16 +607,57 @@ __global__ void __launch_bounds__(kKlDkThreads, 1) kl_dk_kernel(const __grid_con
   }
 }
 
+// Merge of the slices' five scalars, one thread per query row:
+//   M_t = max_s m_t,s,  l_t = sum_s l_t,s 2^(m_t,s - M_t),  acc = sum_s acc_s 2^(m_a,s - M_a),
+// then LSE_t = (M_t + log2 l_t) ln 2 and KL = scale acc / l_a + LSE_b - LSE_a.
+__global__ void __launch_bounds__(256) kl_combine_kernel(const __grid_constant__ KlArgs a) {
+  const size_t rows = static_cast<size_t>(a.bh_count) * a.Nq;
+  const size_t o = static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x;
+  if (o >= rows) return;
+  const size_t plane = static_cast<size_t>(a.splits) * rows;
+  float Ma = -INFINITY, Mb = -INFINITY;
+  for (int s = 0; s < a.splits; ++s) {
+    Ma = fmaxf(Ma, a.part[s * rows + o]);
+    Mb = fmaxf(Mb, a.part[plane + s * rows + o]);
+  }
+  float La = 0.f, Lb = 0.f, A = 0.f;
+  for (int s = 0; s < a.splits; ++s) {
+    const size_t e = s * rows + o;
+    const float ma = a.part[e], mb = a.part[plane + e];
+    if (ma != -INFINITY) {
+      const float w = ex2_approx(ma - Ma);
+      La = fmaf(a.part[2 * plane + e], w, La);
+      A = fmaf(a.part[4 * plane + e], w, A);
+    }
+    if (mb != -INFINITY) Lb = fmaf(a.part[3 * plane + e], ex2_approx(mb - Mb), Lb);
+  }
+  if (La > 0.f) {
+    const float lse_a = (Ma + __log2f(La)) * 0.6931471805599453f;
+    const float lse_b = (Mb + __log2f(Lb)) * 0.6931471805599453f;
+    a.lse1[o] = lse_a;
+    a.lse2[o] = lse_b;
+    a.kl[o] = a.scale * A / La + lse_b - lse_a;
+  } else {
+    a.lse1[o] = -INFINITY;
+    a.lse2[o] = -INFINITY;
+    a.kl[o] = 0.f;
+  }
+}
+
 // ====================================================================== launchers
 
 template <int D, bool CAUSAL, bool BF16>
 cudaError_t launch_kl_fwd_t(const KlArgs& a, cudaStream_t stream) {
   using C = KlFwdCfg<D>;
-  auto kern = kl_fwd_kernel<D, CAUSAL, BF16>;
+  const bool split = a.splits > 1;
+  auto kern = split ? kl_fwd_kernel<D, CAUSAL, BF16, true> : kl_fwd_kernel<D, CAUSAL, BF16, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.bh_count, (a.Nq + kTileRows - 1) / kTileRows, 1);
+  dim3 grid(a.bh_count, (a.Nq + kTileRows - 1) / kTileRows, split ? a.splits : 1);
   kern<<<grid, kKlFwdThreads, C::BYTES, stream>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess || !split) return e;
+  const size_t rows = static_cast<size_t>(a.bh_count) * a.Nq;
+  kl_combine_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -95,6 +95,8 @@ struct KlArgs {
   float* lse1;                             // [B*H][Nq]
   float* lse2;                             // [B*H][Nq]
   const float* g;                          // [B*H][Nq]: upstream gradient (backward)
+  float* part;                             // forward, splits > 1: [5][splits][B*H][Nq] per-slice state
+  int splits;                              // forward: key slices per query tile (1: none)
   uint32_t* err_word;
   int bh_count, heads, Nq, Nk, d;
   bool causal, bf16;

@@ -86,6 +86,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_kl_bwd.restype = i
             lib.attn_selftest_wait_timeout.argtypes = [i, vp]
             lib.attn_selftest_wait_timeout.restype = i
+            lib.attn_kl_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, sz, vp]
+            lib.attn_kl_fwd_splitkv.restype = i
+            lib.attn_kl_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i, i]
+            lib.attn_kl_fwd_splitkv_workspace_size.restype = sz
             lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
             lib.attn_bwd_workspace_size.restype = sz
             for name in ("attn_bwd",) + BWD_STEPS:
@@ -352,6 +356,20 @@ def kl_forward(q1, k1, q2, k2, causal=False, scale: float | None = None, stream=
     scale = (1.0 / d ** 0.5) if scale is None else scale
     kl, lse1, lse2 = (torch.empty((B, H, Nq), dtype=torch.float32, device=q1.device) for _ in range(3))
     _check(kl_fwd_raw(q1, k1, q2, k2, kl, lse1, lse2, causal, scale, stream), "attn_kl_fwd")
+    return kl, lse1, lse2
+
+
+def kl_forward_splitkv(q1, k1, q2, k2, causal=False, scale: float | None = None, num_splits: int = 0, stream=None):
+    """kl_forward for few query rows with the key dimension divided across blocks (0: library's choice)."""
+    B, H, Nq, Nk, d = _dims(q1, k1)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    kl, lse1, lse2 = (torch.empty((B, H, Nq), dtype=torch.float32, device=q1.device) for _ in range(3))
+    nb = int(load().attn_kl_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, num_splits))
+    ws = torch.empty(nb, dtype=torch.uint8, device=q1.device) if nb else None
+    st = load().attn_kl_fwd_splitkv(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(kl), _ptr(lse1), _ptr(lse2), B, H,
+                                    Nq, Nk, d, mask_code(causal), float(scale), _dtype_code(q1), int(num_splits),
+                                    *_workspace(ws), _stream(stream))
+    _check(st, "attn_kl_fwd_splitkv")
     return kl, lse1, lse2
 
 

@@ -181,6 +181,28 @@ attn_status attn_kl_fwd(const void* Q1, const void* K1, const void* Q2, const vo
                         attn_dtype dtype, void* stream);
 
 /*
+ * attn_kl_fwd for few query rows (the StreamKL summary's split-K variant, GPU
+ * kernel optimisations): the key tiles each query tile sees are divided into
+ * num_splits contiguous slices processed by separate blocks; each writes its
+ * slice's five running scalars and a second kernel merges them (maxima
+ * combined, sums and the weighted logit difference rescaled to the common
+ * maxima).  Same results as attn_kl_fwd up to fp32 rounding.  num_splits:
+ * 1..256, or 0 for the library's choice (attn_fwd_splitkv_num_splits; when it
+ * is 1 this is exactly attn_kl_fwd and needs no workspace).  workspace: at
+ * least attn_kl_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, num_splits) bytes,
+ * 256-byte aligned, contents on entry irrelevant.  Errors as attn_kl_fwd, plus
+ * ATTN_ERR_INVALID_ARG for num_splits outside [0, 256] and ATTN_ERR_WORKSPACE
+ * for a missing or small workspace.
+ */
+attn_status attn_kl_fwd_splitkv(const void* Q1, const void* K1, const void* Q2, const void* K2, float* KL,
+                                float* LSE1, float* LSE2, int B, int H, int Nq, int Nk, int d, int causal,
+                                float scale, attn_dtype dtype, int num_splits, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of attn_kl_fwd_splitkv for num_splits (0: the library's choice, which may need none). */
+size_t attn_kl_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
+
+/*
  * Gradients of sum_q G_q KL_q (Methodology 2: probabilities regenerated from
  * the stored LSEs) for one distribution:
  *   setting 1, the student is trained (teacher fixed):

@@ -190,3 +190,16 @@ def test_kl_rejects_bad_arguments(lib):
 def test_selftest_rejects_bad_timeout(lib):
     for ms in (0, -5, 10001):
         assert lib.attn_selftest_wait_timeout(ms, None) == 1
+
+
+def test_kl_splitkv_rejects_bad_arguments(lib):
+    p = [ctypes.c_void_p(FAKE)] * 7
+    need = lib.attn_kl_fwd_splitkv_workspace_size(1, 2, 1, 1000, 64, 4)
+    assert need == ((5 * 4 * 2 * 1 * 4 + 255) // 256) * 256
+    call = lambda splits, ws=FAKE, nbytes=need: lib.attn_kl_fwd_splitkv(  # noqa: E731
+        *p, 1, 2, 1, 1000, 64, 0, 0.125, 0, splits, ctypes.c_void_p(ws) if ws else None, nbytes, None)
+    assert call(-1) == 1
+    assert call(300) == 1
+    assert call(4, ws=None) == 6
+    assert call(4, nbytes=need - 1) == 6
+    assert call(4, ws=FAKE + 8) == 3

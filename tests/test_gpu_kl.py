@@ -119,3 +119,22 @@ def test_kl_workload_full_size_sampled():
             assert rel_l2(dq[b, h, rows[:24]], rq) <= GRAD_TOL, f"{train} dQ rows head {h}"
             rk = oracle.kl_dk_cols(*args, sel(x["g"]), setting, w.causal, w.scale, cols)
             assert rel_l2(dk[b, h, cols], rk) <= GRAD_TOL, f"{train} dK rows head {h}"
+
+
+@pytest.mark.parametrize("shape,splits", [
+    ((2, 3, 1, 3000, 128, "bf16", "bottom_right"), 4),    # one query per head (decoding)
+    ((1, 2, 64, 2000, 64, "fp16", "bottom_right"), 3),
+    ((1, 1, 200, 700, 128, "bf16", True), 5),            # top-left: the second query tile sees one more tile
+    ((1, 1, 1, 200, 64, "bf16", False), 8),              # two key tiles over eight slices: empty slices
+    ((1, 1, 300, 100, 128, "fp16", "bottom_right"), 2),  # rows and a query tile without keys
+    ((2, 2, 5, 4099, 64, "bf16", False), 0),             # the library's slice count
+], ids=lambda v: str(v))
+def test_kl_splitkv_parity(shape, splits):
+    w = workloads.custom(*shape)
+    x = workloads.make_kl_inputs(w)
+    d = _dev(x)
+    kl, l1, l2 = exattn.kl_forward_splitkv(d["q1"], d["k1"], d["q2"], d["k2"], w.causal, w.scale, num_splits=splits)
+    torch.cuda.synchronize()
+    assert exattn.check_device_error() == 0
+    ref = oracle.kl_fwd(x["q1"], x["k1"], x["q2"], x["k2"], w.causal, w.scale)
+    _check_fwd(kl.cpu().numpy(), l1.cpu().numpy(), l2.cpu().numpy(), ref, f"{w.name} splits={splits}")
