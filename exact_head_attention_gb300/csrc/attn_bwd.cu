@@ -13,9 +13,13 @@
 //        dP^T = V_j dO_i^T, dS^T = P^T o (dP^T - D_i)
 //        dV_j += P^T dO_i,  dK_j += dS^T Q_i,  dQ_i += dS K_j
 //    (StreamKL summary, Methodology 2: P regenerated tile by tile from the
-//    stored LSE), accumulating dK_j, dV_j in TMEM and reducing dQ_i into the
-//    fp32 accumulator with atomics (SparkAttention: dQ is atomically added
-//    across thread blocks; StreamKL: atomics while the buffer fits in L2).
+//    stored LSE), accumulating dK_j, dV_j in TMEM and adding dQ_i into the
+//    fp32 accumulator in L2 (SparkAttention: dQ is atomically added across
+//    thread blocks; StreamKL: atomics while the buffer fits in L2).  At
+//    d = 128 the adds are copy-engine bulk reduce-adds of a shared-memory
+//    tile; at d = 64 vector reductions from registers.  A template flag drops
+//    the dQ work entirely for the deterministic mode, where the query-tile
+//    kernel (attn_bwd_dq.cu) produces dQ instead.
 // 3. bwd_dq_convert_kernel: dQ = scale * dQacc rounded to the input dtype.
 //
 // Main-kernel warp roles (320 threads):

@@ -240,9 +240,12 @@ size_t attn_bwd_workspace_size(int B, int H, int Nq, int d);
  *   D = rowsum(dO o O) ("dPsum"); per key/value block (parallel over blocks
  *   of columns of the attention matrix) recompute P = exp(S - LSE),
  *   dV += P^T dO, dP = dO V^T, dS = P o (dP - D), dK += scale dS^T Q, and
- *   dQ += scale dS K accumulated across blocks with fp32 atomics.
+ *   dQ += scale dS K accumulated across blocks by fp32 reductions into the
+ *   workspace (ATTN_DQ_ATOMIC of attn_bwd_ex).
  * The dQ summation order across key blocks is not fixed, so dQ may differ
- * between runs by fp32 rounding.
+ * between runs by fp32 rounding; attn_bwd_ex with ATTN_DQ_DETERMINISTIC
+ * gives the same bits on every run.  dK and dV are the same bits on every
+ * run in either mode.
  */
 attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                      const float* LSE, void* dQ, void* dK, void* dV,
