@@ -755,6 +755,13 @@ def main() -> None:
         "kernels_ms": kern_ms,
         "fwd_tflops": fwd_f / (kern_ms["fwd"] * 1e-3) / 1e12,
         "bwd_tflops": bwd_f / (sum(kern_ms[n] for n in ("bwd_preprocess", "bwd_kv_blocks", "bwd_dq_convert")) * 1e-3) / 1e12,
+        # each rate as a fraction of the measured bf16 tensor peak
+        "frac_of_peak": {
+            "fwd": fwd_f / (kern_ms["fwd"] * 1e-3) / 1e12 / pk["bf16_tflops"],
+            "bwd": bwd_f / (sum(kern_ms[n] for n in ("bwd_preprocess", "bwd_kv_blocks", "bwd_dq_convert")) * 1e-3)
+                   / 1e12 / pk["bf16_tflops"],
+            "fwd_bwd": flops / (ms_per_step * 1e-3) / 1e12 / pk["bf16_tflops"],
+        },
         "roofline": {"kernel": "bwd_main_kernel (attn_bwd_kv_blocks)", "bound": "tensor", "achieved": achieved,
                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
                      "traffic": traffic_from_profile(f"{dominant}:{w.name}"),
