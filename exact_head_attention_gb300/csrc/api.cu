@@ -115,6 +115,18 @@ CUresult encode_map(CUtensorMap* map, const void* ptr, bool bf16, int B, int H, 
   return r;
 }
 
+// 2-D fp32 map over the backward's dQ accumulator [rows][d]: box = 32 columns (128 bytes) x 128 rows,
+// 128-byte swizzle; the d = 64 kernel reduce-adds [128 query][32 d] boxes into it.
+CUresult encode_acc_map(CUtensorMap* map, float* acc, size_t rows, int d) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 4};
+  const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kTileRows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, acc, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 RowStrides contiguous(int H, int n, int d) {
   return RowStrides{static_cast<long long>(H) * n * d, static_cast<long long>(n) * d, d};
 }
@@ -301,6 +313,8 @@ attn_status bwd_steps(const void* Q, const void* K, const void* V, const void* O
   if (dq_mode == ATTN_DQ_DETERMINISTIC) {
     a.dq_acc = nullptr;  // no accumulator: dK, dV from the key/value blocks, dQ from the query-tile kernel
     steps = kBwdDeterministic;
+  } else if (d == 64 && (r = encode_acc_map(&a.tm_dqacc, a.dq_acc, rows, d)) != CUDA_SUCCESS) {
+    return driver_fail("cuTensorMapEncodeTiled(dQ accumulator)", r);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return finish(launch_bwd(a, steps, s), s);

@@ -61,8 +61,10 @@ struct BwdCfg {
   // Q/dO ring slots.  d = 128 gives one slot to the dQ staging tile: reducing dQ with the copy
   // engine from shared memory is far cheaper than per-thread atomics, which outweighs the shallower ring.
   static constexpr int NR = (D == 64) ? 6 : 3;
-  // fp32 dQ staging for d = 128: 64 query rows x 128 d, the accumulator's own row-major layout
-  static constexpr uint32_t STAGE_BYTES = (D == 128) ? 64 * 128 * 4 : 0;
+  // fp32 dQ staging, 32 KB: d = 128, 64 query rows x 128 d in the accumulator's row-major layout (one
+  // half per warpgroup in turn with the dS^T tile); d = 64, two [128 query][32 d] boxes (one per
+  // warpgroup) in the 128-byte-swizzled layout of the accumulator's tensor map.
+  static constexpr uint32_t STAGE_BYTES = 32768;
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + TILE;
   static constexpr uint32_t OFF_DS = OFF_V + TILE;
@@ -360,19 +362,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
           tma_store_commit();
         }
       } else {
-        // dQ_i: lane = query row; this warpgroup reduces d columns [32h, 32h + 32).
+        // dQ_i: lane = query row; this warpgroup reduces d columns [32h, 32h + 32).  Its box [128
+        // query][32 d] (128 bytes per row) goes into its half of the staging tile with the 128-byte
+        // swizzle of the accumulator's tensor map (a thread writes one row: no bank conflicts), and one
+        // thread has the copy engine add the box into the accumulator (a tensor reduce-add).
         uint32_t v[32];
         tmem_ld32(tY + lane_bits + h * 32, v);
         tmem_wait_ld();
         reg_fence32(v);
         tc_fence_before();
         mbar_arrive(bars.dq_empty());
-        const size_t row = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows + r;
-        float* dst = a.dq_acc + row * D + h * 32;
+        const uint32_t box = sbase + C::OFF_STAGE + h * (C::STAGE_BYTES / 2);
+        if (r == 0) tma_store_wait_read_all();  // this half's previous reduction has read the box
+        named_bar_sync(1 + h, 128);
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          red_add_v4(dst + u * 4, __uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]), __uint_as_float(v[4 * u + 2]),
-                     __uint_as_float(v[4 * u + 3]));
+        for (int u = 0; u < 8; ++u) st_shared_v4(box + sw128_offset(r, u), v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(1 + h, 128);
+        if (r == 0) {
+          tma_reduce_add_2d(&a.tm_dqacc, box, 32 * h, bh * a.Nq_pad + (i_start + it) * kTileRows);
+          tma_store_commit();
+        }
       }
       return true;
     };

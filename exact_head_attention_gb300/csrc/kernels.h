@@ -33,6 +33,7 @@ struct FwdArgs {
 
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv, tm_dq;
+  CUtensorMap tm_dqacc;  // d = 64: 2-D fp32 map {d, B*H*Nq_pad} over dq_acc, box {32, 128}, 128-byte swizzle
   const void* o;       // [B][H][Nq][d] 16-bit, strides so
   const void* dout;    // [B][H][Nq][d] 16-bit, strides sdo
   const float* lse;    // [B*H][Nq]

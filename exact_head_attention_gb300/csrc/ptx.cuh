@@ -176,6 +176,15 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t src, u
                : "memory");
 }
 
+// 2-D tensor reduce-add (fp32 add) of a shared-memory box into global memory through a tensor map, by
+// the copy engine; tracked by the issuing thread's bulk groups like a tensor store.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_store_wait_read_all() {
