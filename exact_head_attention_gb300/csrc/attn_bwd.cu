@@ -15,9 +15,10 @@
 //    (StreamKL summary, Methodology 2: P regenerated tile by tile from the
 //    stored LSE), accumulating dK_j, dV_j in TMEM and adding dQ_i into the
 //    fp32 accumulator in L2 (SparkAttention: dQ is atomically added across
-//    thread blocks; StreamKL: atomics while the buffer fits in L2).  At
-//    d = 128 the adds are copy-engine bulk reduce-adds of a shared-memory
-//    tile; at d = 64 vector reductions from registers.  A template flag drops
+//    thread blocks; StreamKL: atomics while the buffer fits in L2).  The
+//    adds are copy-engine reduce-adds of a shared-memory tile: flat bulk
+//    copies of dQ^T's row-major halves at d = 128, 2-D tensor copies of
+//    128-byte-swizzled [128 query][32 d] boxes at d = 64.  A template flag drops
 //    the dQ work entirely for the deterministic mode, where the query-tile
 //    kernel (attn_bwd_dq.cu) produces dQ instead.
 // 3. bwd_dq_convert_kernel: dQ = scale * dQacc rounded to the input dtype.
