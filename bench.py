@@ -38,6 +38,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -248,9 +249,14 @@ def traffic_from_profile(kernel_key: str) -> float | None:
 
 
 def kernel_source_sha() -> str:
+    """Hash of the headline kernels' sources with comments and blank lines removed (a comment edit
+    leaves the compiled kernels, and so the profiled traffic, unchanged)."""
     h = hashlib.sha256()
     for f in ("attn_fwd.cu", "attn_bwd.cu", "ptx.cuh", "kernels.h", "softmax.cuh"):
-        h.update(open(os.path.join(ROOT, "exact_head_attention_gb300", "csrc", f), "rb").read())
+        src = open(os.path.join(ROOT, "exact_head_attention_gb300", "csrc", f)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update("\n".join(ln.rstrip() for ln in src.splitlines() if ln.strip()).encode())
     return h.hexdigest()[:16]
 
 
