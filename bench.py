@@ -234,6 +234,77 @@ def job_throughput(flops_per_rank_step: float, world: int, ms_per_step: float) -
     return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
 
 
+def pipelined_e2e(steps: int, slots: list, h2d, compute, d2h, flush) -> tuple[float, float]:
+    """End to end through the public API: pinned host inputs -> device -> one step -> pinned host results.
+
+    Returns (ms per step with steps pipelined, ms of one step on its own).
+
+    Pipelined: step i's host-to-device copies run on a copy-in stream, its kernels on a compute stream
+    and its result copies on a copy-out stream.  Steps alternate between the device buffer sets in
+    `slots`, so step i+1's inputs and step i-1's results cross the host link while step i computes.
+    Events order the reuse of a set: its inputs are overwritten only after the compute that read them
+    has finished, and its results only after the copy-out that read them has finished.  The time runs
+    from the first copy-in to the last copy-out and includes filling and draining the pipeline.
+
+    On its own: the same calls on one stream, one step at a time, each after an L2 flush (outside the
+    events).  `h2d(slot)` and `d2h(slot)` issue copies on the current stream; `compute(slot, stream)`
+    launches the step on `stream`."""
+    import torch
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    n_sl = len(slots)
+
+    def run(n: int) -> float:
+        cmp_done, out_done = [None] * n, [None] * n
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        start.record(s_in)
+        for i in range(n):
+            sl = slots[i % n_sl]
+            if i >= n_sl:
+                s_in.wait_event(cmp_done[i - n_sl])
+            with torch.cuda.stream(s_in):
+                h2d(sl)
+            in_done = torch.cuda.Event()
+            in_done.record(s_in)
+            s_cmp.wait_event(in_done)
+            if i >= n_sl:
+                s_cmp.wait_event(out_done[i - n_sl])
+            compute(sl, s_cmp)
+            cmp_done[i] = torch.cuda.Event()
+            cmp_done[i].record(s_cmp)
+            s_out.wait_event(cmp_done[i])
+            with torch.cuda.stream(s_out):
+                d2h(sl)
+            out_done[i] = torch.cuda.Event()
+            out_done[i].record(s_out)
+        end.record(s_out)
+        end.synchronize()
+        return start.elapsed_time(end) / n
+
+    run(3)
+    pipe_ms = run(steps)
+    alone = []
+    for i in range(max(3, steps // 3)):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s_cmp)
+        with torch.cuda.stream(s_cmp):
+            h2d(slots[0])
+        compute(slots[0], s_cmp)
+        with torch.cuda.stream(s_cmp):
+            d2h(slots[0])
+        b.record(s_cmp)
+        b.synchronize()
+        alone.append(a.elapsed_time(b))
+    return pipe_ms, statistics.mean(alone)
+
+
+E2E_NOTE = ("pipelined over steps on three CUDA streams (copy-in, compute, copy-out) with two device buffer sets; "
+            "no L2 flush (each step's inputs arrive by host-to-device copy); alone_ms_per_step: one step by itself "
+            "on one stream after an L2 flush")
+
+
 # ------------------------------------------------------------------ main
 
 def traffic_from_profile(kernel_key: str) -> float | None:
@@ -380,28 +451,27 @@ def run_decode(args, w, rank: int, world: int) -> None:
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = sum(t.numel() * t.element_size() for t in (ho, hlse))
 
-    def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        launch()
-        ho.copy_(o, non_blocking=True)
-        hlse.copy_(lse, non_blocking=True)
+    slots = [{"q": q, "k": k, "v": v, "o": o, "lse": lse, "ws": ws}]
+    slots.append({n: torch.empty_like(t) for n, t in slots[0].items()})
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e_ms = []
-    for i in range(args.e2e_steps):
-        flush.fill_(i & 0xFF)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_step()
-        b.record(stream)
-        b.synchronize()
-        e_ms.append(a.elapsed_time(b))
+    def h2d_(sl):
+        for n, ht in (("q", hq), ("k", hk), ("v", hv)):
+            sl[n].copy_(ht, non_blocking=True)
+
+    def compute_(sl, s):
+        st = exattn.fwd_splitkv_raw(sl["q"], sl["k"], sl["v"], sl["o"], sl["lse"], w.causal, w.scale, splits, sl["ws"],
+                                    stream=s)
+        if st:
+            raise RuntimeError(f"C-ABI status {st}: {exattn.last_error()}")
+
+    def d2h_(sl):
+        ho.copy_(sl["o"], non_blocking=True)
+        hlse.copy_(sl["lse"], non_blocking=True)
+
+    e2e_ms, alone_ms = pipelined_e2e(args.e2e_steps, slots, h2d_, compute_, d2h_, flush) if args.e2e_steps else (0, 0)
     sampler.stop()
-    e2e_ms = max_over_ranks(statistics.mean(e_ms) if e_ms else float("nan"), dist, dev)
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    alone_ms = max_over_ranks(alone_ms, dist, dev)
 
     nbytes = decode_bytes(w)
     pk = peaks()
@@ -419,7 +489,8 @@ def run_decode(args, w, rank: int, world: int) -> None:
                      "traffic": None, "peak_kind": f"HBM copy bandwidth ({pk['source']})"},
         "cpu_baseline": cpu,
         "e2e": ({"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms} if e_ms else None),
+                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "alone_ms_per_step": alone_ms,
+                 "timing": E2E_NOTE} if args.e2e_steps else None),
         "gpu_launches": 2 * args.steps,
         "clocks": sampler.summary(t_wall0, t_wall1),
         "wall_s_timed_region": t_wall1 - t_wall0,
@@ -559,28 +630,30 @@ def run_kl(args, w, rank: int, world: int) -> None:
     h2d = sum(t.numel() * t.element_size() for t in h.values())
     d2h = sum(t.numel() * t.element_size() for t in (hkl, hdq, hdk))
 
-    def e2e_step():
-        for k_ in d:
-            d[k_].copy_(h[k_], non_blocking=True)
-        launch()
-        hkl.copy_(kl, non_blocking=True)
-        hdq.copy_(dq, non_blocking=True)
-        hdk.copy_(dk, non_blocking=True)
+    slots = [dict(d, kl=kl, l1=l1, l2=l2, dq=dq, dk=dk)]
+    slots.append({n: torch.empty_like(t) for n, t in slots[0].items()})
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e_ms = []
-    for i in range(args.e2e_steps):
-        flush.fill_(i & 0xFF)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_step()
-        b.record(stream)
-        b.synchronize()
-        e_ms.append(a.elapsed_time(b))
+    def h2d_(sl):
+        for k_ in d:
+            sl[k_].copy_(h[k_], non_blocking=True)
+
+    def compute_(sl, s):
+        s1 = exattn.kl_fwd_raw(sl["q1"], sl["k1"], sl["q2"], sl["k2"], sl["kl"], sl["l1"], sl["l2"], w.causal, w.scale,
+                               stream=s)
+        s2 = exattn.kl_bwd_raw(sl["q1"], sl["k1"], sl["q2"], sl["k2"], sl["kl"], sl["l1"], sl["l2"], sl["g"], "student",
+                               sl["dq"], sl["dk"], w.causal, w.scale, stream=s)
+        if s1 or s2:
+            raise RuntimeError(f"C-ABI status {(s1, s2)}: {exattn.last_error()}")
+
+    def d2h_(sl):
+        hkl.copy_(sl["kl"], non_blocking=True)
+        hdq.copy_(sl["dq"], non_blocking=True)
+        hdk.copy_(sl["dk"], non_blocking=True)
+
+    e2e_ms, alone_ms = pipelined_e2e(args.e2e_steps, slots, h2d_, compute_, d2h_, flush) if args.e2e_steps else (0, 0)
     sampler.stop()
-    e2e_ms = max_over_ranks(statistics.mean(e_ms) if e_ms else float("nan"), dist, dev)
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    alone_ms = max_over_ranks(alone_ms, dist, dev)
 
     ff, bf = kl_flops(w)
     pk = peaks()
@@ -602,7 +675,8 @@ def run_kl(args, w, rank: int, world: int) -> None:
                      "traffic": None, "peak_kind": f"bf16 dense burst ({pk['source']})"},
         "cpu_baseline": cpu,
         "e2e": ({"value": world * (ff + bf) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms} if e_ms else None),
+                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                 "alone_ms_per_step": alone_ms, "timing": E2E_NOTE} if args.e2e_steps else None),
         "gpu_launches": 3 * args.steps,
         "clocks": sampler.summary(t_wall0, t_wall1),
         "wall_s_timed_region": t_wall1 - t_wall0,
@@ -716,32 +790,28 @@ def main() -> None:
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
 
-    def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        do.copy_(hdo, non_blocking=True)
-        s1 = exattn.fwd_raw(q, k, v, o, lse, w.causal, w.scale)
-        s2 = exattn.bwd_raw(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, ws)
-        for hd, dd in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
-            hd.copy_(dd, non_blocking=True)
+    slots = [{"q": q, "k": k, "v": v, "do": do, "o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv, "ws": ws}]
+    slots.append({n: torch.empty_like(t) for n, t in slots[0].items()})
+
+    def h2d_(sl):
+        for n, ht in (("q", hq), ("k", hk), ("v", hv), ("do", hdo)):
+            sl[n].copy_(ht, non_blocking=True)
+
+    def compute_(sl, s):
+        s1 = exattn.fwd_raw(sl["q"], sl["k"], sl["v"], sl["o"], sl["lse"], w.causal, w.scale, stream=s)
+        s2 = exattn.bwd_raw(sl["q"], sl["k"], sl["v"], sl["o"], sl["do"], sl["lse"], sl["dq"], sl["dk"], sl["dv"],
+                            w.causal, w.scale, sl["ws"], stream=s)
         if s1 or s2:
             raise RuntimeError(exattn.last_error())
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e_ms = []
-    for i in range(args.e2e_steps):
-        flush.fill_(i & 0xFF)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_step()
-        b.record(stream)
-        b.synchronize()
-        e_ms.append(a.elapsed_time(b))
+    def d2h_(sl):
+        for ht, n in ((ho, "o"), (hlse, "lse"), (hdq, "dq"), (hdk, "dk"), (hdv, "dv")):
+            ht.copy_(sl[n], non_blocking=True)
+
+    e2e_ms, alone_ms = pipelined_e2e(args.e2e_steps, slots, h2d_, compute_, d2h_, flush) if args.e2e_steps else (0, 0)
     sampler.stop()
-    e2e_ms = max_over_ranks(statistics.mean(e_ms) if e_ms else float("nan"), dist, dev)
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    alone_ms = max_over_ranks(alone_ms, dist, dev)
 
     fwd_f, bwd_f = step_flops(w)
     flops = fwd_f + bwd_f
@@ -774,7 +844,8 @@ def main() -> None:
                      "peak_kind": f"bf16 dense burst ({pk['source']})"},
         "cpu_baseline": ({k_: v_ for k_, v_ in cpu.items() if k_ != "seconds"} if cpu else None),
         "e2e": ({"value": job_throughput(flops, world, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms} if e_ms else None),
+                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "alone_ms_per_step": alone_ms,
+                 "timing": E2E_NOTE} if args.e2e_steps else None),
         "gpu_launches": 4 * args.steps,
         "clocks": sampler.summary(t_wall0, t_wall1),
         "wall_s_timed_region": t_wall1 - t_wall0,
