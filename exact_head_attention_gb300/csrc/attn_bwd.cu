@@ -32,13 +32,16 @@
 //   warp  9     MMA issuer (one thread) and TMEM owner
 // Tensor memory (512 columns):
 //   X  = [0,128)    S^T_i, then dP^T_i; then each compute warpgroup h packs its
-//                   P^T half into [64h, 64h+32) and its dS^T half into
-//                   [64h+32, 64h+64) -- the A operands of the dV and dK MMAs
-//   Y  = [128,256)  dQ_i (d = 64: lane = query row) or dQ_i^T (d = 128: lane = d)
+//                   dS^T half into [64h+32, 64h+64) -- the A operand of the dK MMA
+//   Y  = [128,256)  dQ_i (d = 64: lane = query row, 64 columns) or dQ_i^T (d = 128:
+//                   lane = d), and the packed P^T (the dV MMA's A operand), written
+//                   as soon as the exponentials are done: d = 128 into the columns
+//                   each warpgroup has just read dQ_{i-1}^T from, d = 64 into the
+//                   64 columns dQ leaves free
 //   dV = [256,256+d), dK = [384,384+d)
 // Shared memory: K_j, V_j, dS^T (the dQ MMA's operand), the Q/dO ring.
 // Per tile i the MMA issue order is dV_i, dK_i, S_{i+1}, dQ_i, dP_{i+1}: dV_i
-// starts as soon as P^T_i is in TMEM and overlaps the forming of dS^T_i, the
+// queues behind dP^T_i (P^T_i is in Y by then) and overlaps the forming of dS^T_i, the
 // exponentials of tile i+1 overlap dQ_i and dP_{i+1}, and the dQ_i reduction
 // (issued by the compute warps after they hand over tile i+1) overlaps the
 // next tile's MMAs.
@@ -110,9 +113,20 @@ struct BwdBars {
   __device__ uint32_t rowv_empty(int s) const { return at(11 + s); }
 };
 
-// TMEM column of K step k (16 query columns) of the packed P^T (off = 0) or dS^T (off = 32) operand:
-// query columns [0, 64) sit in [off, off + 32), query columns [64, 128) in [64 + off, 64 + off + 32).
-__device__ __forceinline__ uint32_t packed_col(int k, int off) { return (k < 4 ? k * 8 : 64 + (k - 4) * 8) + off; }
+// TMEM column of K step k (16 query columns) of the packed dS^T operand in X: query columns [0, 64)
+// sit in [32, 64), query columns [64, 128) in [96, 128).
+__device__ __forceinline__ uint32_t ds_col(int k) { return (k < 4 ? k * 8 : 64 + (k - 4) * 8) + 32; }
+
+// The packed P^T operand lives in Y, so that it can be written before dP^T lands in X.  Query half h
+// (32 packed columns) starts at column p_base<D>() + h * p_stride<D>() of Y: d = 128, the first 32
+// columns of the half of dQ_{i-1}^T that warpgroup h has just read out; d = 64, the 64 columns of Y
+// that dQ (64 columns) leaves free.
+template <int D>
+__device__ __forceinline__ constexpr uint32_t p_base() { return D == 64 ? 64u : 0u; }
+template <int D>
+__device__ __forceinline__ constexpr uint32_t p_stride() { return D == 64 ? 32u : 64u; }
+template <int D>
+__device__ __forceinline__ uint32_t p_col(int k) { return p_base<D>() + (k < 4 ? k * 8 : p_stride<D>() + (k - 4) * 8); }
 
 // DQ = false: dK and dV only (the deterministic mode computes dQ in bwd_dq_kernel instead); the dQ
 // MMA, the dS^T tile in shared memory and the reductions are left out.
@@ -268,25 +282,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       if (ok) ok = issue_S(0);
       if (ok) ok = issue_dP(0);
       for (int it = 0; ok && it < n; ++it) {
-        // dV_i needs only P^T: it runs while the compute warps form dS^T
+        // dV_i needs only P^T, which is in Y before dP^T_i lands: it queues behind dP^T_i and runs while
+        // the compute warps form dS^T.
         if (!(ok = mbar_wait(bars.p_ready(), it & 1, wc))) break;
         tc_fence_after();
         const uint32_t q_lo = ring_mn + slot_of(2 * it) * kTileLo;
         const uint32_t do_lo = ring_mn + slot_of(2 * it + 1) * kTileLo;
         const uint32_t acc0 = it > 0 ? 1u : 0u;
-        // dV += P^T dO_i   (A: P^T packed in TMEM X; B: dO_i [query][d] MN-major, 16 query rows per K step)
-        mma_ts_lo_rt(tdV, tX + packed_col(0, 0), do_lo, idG, acc0);
+        // dV += P^T dO_i   (A: P^T packed in TMEM Y; B: dO_i [query][d] MN-major, 16 query rows per K step)
+        mma_ts_lo_rt(tdV, tY + p_col<D>(0), do_lo, idG, acc0);
 #pragma unroll
-        for (int k = 1; k < 128 / 16; ++k) mma_ts_lo<true>(tdV, tX + packed_col(k, 0), do_lo + k * (2048 >> 4), idG);
+        for (int k = 1; k < 128 / 16; ++k) mma_ts_lo<true>(tdV, tY + p_col<D>(k), do_lo + k * (2048 >> 4), idG);
         mma_commit(bars.ring_empty(slot_of(2 * it + 1)));
         if (!(ok = mbar_wait(bars.pd_ready(), it & 1, wc))) break;
         tc_fence_after();
         // dK += dS^T Q_i   (A: dS^T packed in TMEM X; B: Q_i [query][d] MN-major)
-        mma_ts_lo_rt(tdK, tX + packed_col(0, 32), q_lo, idG, acc0);
+        mma_ts_lo_rt(tdK, tX + ds_col(0), q_lo, idG, acc0);
 #pragma unroll
-        for (int k = 1; k < 128 / 16; ++k) mma_ts_lo<true>(tdK, tX + packed_col(k, 32), q_lo + k * (2048 >> 4), idG);
+        for (int k = 1; k < 128 / 16; ++k) mma_ts_lo<true>(tdK, tX + ds_col(k), q_lo + k * (2048 >> 4), idG);
         mma_commit(bars.ring_empty(slot_of(2 * it)));
-        // S^T_{i+1} overwrites X after dV_i, dK_i have read it (MMAs of one thread run in order).
+        // S^T_{i+1} overwrites X after dK_i has read it, and dQ_i overwrites Y after dV_i has read it
+        // (MMAs of one thread run in order).
         if (it + 1 < n && !(ok = issue_S(it + 1))) break;
         if constexpr (!DQ) {
           if (it + 1 < n && !(ok = issue_dP(it + 1))) break;
@@ -329,40 +345,57 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
 
     // dQ_i from TMEM Y -> fp32 reductions into the accumulator; Y is released as soon as the
     // values are in registers.
-    auto drain_dq = [&](int it) -> bool {
+    // d = 128: dQ_i^T: lane = d, column = query row.  This warpgroup reduces query rows [64h, 64h + 64):
+    // it writes them row-major (the accumulator's layout; a warp's 32 lanes are 32 consecutive floats of
+    // a row) into a 32 KB buffer and one thread has the copy engine add that contiguous block into the
+    // accumulator.  Warpgroup 0 owns the staging tile (its previous reduction was issued a whole tile
+    // ago); warpgroup 1 uses the dS^T tile, free from the end of the dQ_i MMA until the next dS^T store,
+    // which waits for this reduction's read (see dstile_free).  The rows come out of TMEM 32 at a time;
+    // with `pp`, this warpgroup's P^T of the next tile goes into the first 32 columns once they are read.
+    auto drain128 = [&](int it, bool with_p, const uint32_t (&pp)[32]) -> bool {
       if (!mbar_wait_warp(bars.dq_full(), it & 1, wc)) return false;
       tc_fence_after();
-      if constexpr (D == 128) {
-        // dQ_i^T: lane = d, column = query row.  This warpgroup reduces query rows [64h, 64h + 64):
-        // it writes them row-major (the accumulator's layout; a warp's 32 lanes are 32 consecutive
-        // floats of a row) into a 32 KB buffer and one thread has the copy engine add that contiguous
-        // block into the accumulator.  Warpgroup 0 owns the staging tile (its previous reduction was
-        // issued a whole tile ago); warpgroup 1 uses the dS^T tile, free from the end of the dQ_i MMA
-        // until the next dS^T store, which waits for this reduction's read (see dstile_free).
-        uint32_t v[2][32];
-        tmem_ld32(tY + lane_bits + h * 64, v[0]);
-        tmem_ld32(tY + lane_bits + h * 64 + 32, v[1]);
-        tmem_wait_ld();
-        reg_fence32(v[0]);
-        reg_fence32(v[1]);
+      uint32_t v[32];
+      tmem_ld32(tY + lane_bits + h * 64, v);
+      tmem_wait_ld();
+      reg_fence32(v);
+      if (with_p) {
+        tmem_st32(tY + lane_bits + p_base<D>() + h * p_stride<D>(), pp);
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bars.dq_empty());
-        const uint32_t buf_off = h ? C::OFF_DS : C::OFF_STAGE;
-        if (h == 0) {
-          if (r == 0) tma_store_wait_read_all();  // the previous reduction from the staging tile
-          named_bar_sync(1, 128);
-        }
-        float* buf = reinterpret_cast<float*>(gbase + buf_off);
+        mbar_arrive(bars.p_ready());  // dV of the next tile may go
+      }
+      const uint32_t buf_off = h ? C::OFF_DS : C::OFF_STAGE;
+      if (h == 0) {
+        if (r == 0) tma_store_wait_read_all();  // the previous reduction from the staging tile
+        named_bar_sync(1, 128);
+      }
+      float* buf = reinterpret_cast<float*>(gbase + buf_off);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) buf[c * D + r] = __uint_as_float(v[c >> 5][c & 31]);
-        fence_proxy_async_smem();
-        named_bar_sync(1 + h, 128);
-        if (r == 0) {
-          const size_t row0 = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows + h * 64;
-          bulk_reduce_add_f32(a.dq_acc + row0 * D, sbase + buf_off, C::STAGE_BYTES);
-          tma_store_commit();
-        }
+      for (int c = 0; c < 32; ++c) buf[c * D + r] = __uint_as_float(v[c]);
+      tmem_ld32(tY + lane_bits + h * 64 + 32, v);
+      tmem_wait_ld();
+      reg_fence32(v);
+      tc_fence_before();
+      mbar_arrive(bars.dq_empty());
+#pragma unroll
+      for (int c = 0; c < 32; ++c) buf[(32 + c) * D + r] = __uint_as_float(v[c]);
+      fence_proxy_async_smem();
+      named_bar_sync(1 + h, 128);
+      if (r == 0) {
+        const size_t row0 = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows + h * 64;
+        bulk_reduce_add_f32(a.dq_acc + row0 * D, sbase + buf_off, C::STAGE_BYTES);
+        tma_store_commit();
+      }
+      return true;
+    };
+    auto drain_dq = [&](int it) -> bool {
+      if constexpr (D == 128) {
+        const uint32_t none[32] = {};
+        if (!drain128(it, false, none)) return false;
       } else {
+        if (!mbar_wait_warp(bars.dq_full(), it & 1, wc)) return false;
+        tc_fence_after();
         // dQ_i: lane = query row; this warpgroup reduces d columns [32h, 32h + 32).  Its box [128
         // query][32 d] (128 bytes per row) goes into its half of the staging tile with the 128-byte
         // swizzle of the accumulator's tensor map (a thread writes one row: no bank conflicts), and one
@@ -433,9 +466,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
 #pragma unroll
       for (int i = 0; i < 32; ++i) pp[i] = pack2<BF16>(p[2 * i], p[2 * i + 1]);
 
-      // d = 128: dQ of the previous tile completes just before this tile's dP^T; staging it for the
-      // copy engine fits in that window.
-      if (DQ && D == 128 && it > 0 && !(ok = drain_dq(it - 1))) break;
+      // P^T into Y, before dP^T_i lands: at d = 128 once this warpgroup has read dQ_{i-1}^T out of its
+      // half of Y (dQ_{i-1} runs just before dP^T_i), at d = 64 straight away.  dV_i then queues behind
+      // dP^T_i.  Staging dQ_{i-1} for the copy engine fits before dP^T_i lands.
+      if (DQ && D == 128 && it > 0) {
+        if (!(ok = drain128(it - 1, true, pp))) break;
+      } else {
+        tmem_st32(tY + lane_bits + p_base<D>() + h * p_stride<D>(), pp);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bars.p_ready());  // dV_i may go
+      }
 
       if (!(ok = mbar_wait_warp(bars.dp_full(), it & 1, wc))) break;
       tc_fence_after();
@@ -444,12 +485,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       tmem_wait_ld();
       reg_fence32(s[0]);
       reg_fence32(s[1]);
-      // P^T into this half's first 32 columns of X: its dP^T values are in registers now.
-      tmem_st32(tX + lane_bits + h * 64, pp);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bars.p_ready());  // dV_i may go
-      // dS^T = P^T o (dP^T - D), into the half's next 32 columns of X and into the shared dS^T tile.
+      // dS^T = P^T o (dP^T - D), into the half's last 32 columns of X and into the shared dS^T tile.
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
