@@ -523,7 +523,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       fence_proxy_async_smem();
       mbar_arrive(bars.dss_ready());  // dQ_i may go
 
-      // d = 64: the previous tile's per-thread reductions run after this tile is handed over.
+      // d = 64: the previous tile's dQ is staged and handed to the copy engine after this tile is handed over.
       if (DQ && D == 64 && it > 0 && !(ok = drain_dq(it - 1))) break;
     }
     if (DQ && ok && n > 0) ok = drain_dq(n - 1);
