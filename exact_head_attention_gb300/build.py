@@ -13,7 +13,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libexattn.so")
-SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_dq.cu", "attn_splitkv.cu", "attn_kl.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_dq.cu", "attn_splitkv.cu", "attn_kl.cu", "attn_kl_bwd.cu", "noalloc.cu"]
 HEADERS = ["ptx.cuh", "kernels.h", "softmax.cuh", "ds_ops.cuh"]
 
 NVCC_FLAGS = [

@@ -638,14 +638,27 @@ extern "C" attn_status attn_kl_fwd(const void* Q1, const void* K1, const void* Q
   return finish(launch_kl_fwd(a, s), s);
 }
 
-extern "C" attn_status attn_kl_bwd(const void* Q1, const void* K1, const void* Q2, const void* K2, const float* KL,
-                                   const float* LSE1, const float* LSE2, const float* G, int setting, void* dQ,
-                                   void* dK, int B, int H, int Nq, int Nk, int d, int causal, float scale,
-                                   attn_dtype dtype, void* stream) {
+extern "C" size_t attn_kl_bwd_workspace_size(int B, int H, int Nq, int d) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || (d != 64 && d != 128)) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * padded_rows(Nq);
+  return align256(rows * d * sizeof(float)) + align256(3 * rows * sizeof(float));
+}
+
+namespace {
+
+attn_status kl_bwd_impl(const void* Q1, const void* K1, const void* Q2, const void* K2, const float* KL,
+                        const float* LSE1, const float* LSE2, const float* G, int setting, void* dQ, void* dK, int B,
+                        int H, int Nq, int Nk, int d, int causal, float scale, attn_dtype dtype, int dq_mode,
+                        void* workspace, size_t workspace_bytes, void* stream) {
   if (setting != 1 && setting != 2) return ATTN_ERR_INVALID_ARG;
+  if (dq_mode != ATTN_DQ_ATOMIC && dq_mode != ATTN_DQ_DETERMINISTIC && dq_mode != ATTN_DQ_AUTO)
+    return ATTN_ERR_INVALID_ARG;
   if (!KL || !LSE1 || !LSE2 || !G || !dQ || !dK) return ATTN_ERR_INVALID_ARG;
+  const bool fused = dq_mode != ATTN_DQ_DETERMINISTIC;  // AUTO: the one-pass kernel, as for attention
+  if (fused && (!workspace || workspace_bytes < attn_kl_bwd_workspace_size(B, H, Nq, d))) return ATTN_ERR_WORKSPACE;
   if (!aligned16(KL) || !aligned16(LSE1) || !aligned16(LSE2) || !aligned16(G) || !aligned16(dQ) || !aligned16(dK))
     return ATTN_ERR_MISALIGNED;
+  if (fused && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTN_ERR_MISALIGNED;
   KlArgs a;
   DeviceState* ds = nullptr;
   attn_status st = kl_common(Q1, K1, Q2, K2, B, H, Nq, Nk, d, causal, scale, dtype, &a, &ds);
@@ -659,7 +672,40 @@ extern "C" attn_status attn_kl_bwd(const void* Q1, const void* K1, const void* Q
   a.lse2 = const_cast<float*>(LSE2);
   a.g = G;
   a.op = setting == 1 ? kPairKlStudent : kPairKlTeacher;
-  // dQ over query tiles (teacher a, student b)
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (fused) {
+    // One pass over key tiles: dK, and dQ added into the fp32 accumulator; then dQ = scale * accumulator.
+    const size_t rows = static_cast<size_t>(B) * H * padded_rows(Nq);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.dq_acc = reinterpret_cast<float*>(ws);
+    a.rowv = reinterpret_cast<float*>(ws + align256(rows * d * sizeof(float)));
+    a.Nq_pad = padded_rows(Nq);
+    if (d == 64 && (r = encode_acc_map(&a.tm_dqacc, a.dq_acc, rows, d)) != CUDA_SUCCESS)
+      return driver_fail("cuTensorMapEncodeTiled (accumulator)", r);
+    cudaError_t e = launch_kl_bwd_fused(a, s);
+    if (e == cudaSuccess) {
+      BwdArgs c;
+      std::memset(&c, 0, sizeof(c));
+      c.dq = dQ;
+      c.sdq = contiguous(H, Nq, d);
+      c.dq_acc = a.dq_acc;
+      c.err_word = a.err_word;
+      c.bh_count = a.bh_count;
+      c.heads = H;
+      c.Nq = Nq;
+      c.Nq_pad = a.Nq_pad;
+      c.Nk = Nk;
+      c.d = d;
+      c.causal = a.causal;
+      c.bf16 = bf16;
+      c.scale = scale;
+      c.timeout_ns = a.timeout_ns;
+      e = launch_bwd(c, kBwdConvert, s);
+    }
+    return finish(e, s);
+  }
+  // dQ over query tiles (teacher a, student b), then dK over key tiles: no atomics, the same bits on
+  // every run.
   PairDqArgs p;
   std::memset(&p, 0, sizeof(p));
   p.tm_qa = a.tm_qa;
@@ -685,10 +731,28 @@ extern "C" attn_status attn_kl_bwd(const void* Q1, const void* K1, const void* Q
   p.scale = scale;
   p.op = a.op;
   p.timeout_ns = a.timeout_ns;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_pair_dq(p, s);
   if (e == cudaSuccess) e = launch_kl_dk(a, s);
   return finish(e, s);
+}
+
+}  // namespace
+
+extern "C" attn_status attn_kl_bwd(const void* Q1, const void* K1, const void* Q2, const void* K2, const float* KL,
+                                   const float* LSE1, const float* LSE2, const float* G, int setting, void* dQ,
+                                   void* dK, int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                                   attn_dtype dtype, void* stream) {
+  return kl_bwd_impl(Q1, K1, Q2, K2, KL, LSE1, LSE2, G, setting, dQ, dK, B, H, Nq, Nk, d, causal, scale, dtype,
+                     ATTN_DQ_DETERMINISTIC, nullptr, 0, stream);
+}
+
+extern "C" attn_status attn_kl_bwd_ex(const void* Q1, const void* K1, const void* Q2, const void* K2, const float* KL,
+                                      const float* LSE1, const float* LSE2, const float* G, int setting, void* dQ,
+                                      void* dK, int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                                      attn_dtype dtype, int dq_mode, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+  return kl_bwd_impl(Q1, K1, Q2, K2, KL, LSE1, LSE2, G, setting, dQ, dK, B, H, Nq, Nk, d, causal, scale, dtype,
+                     dq_mode, workspace, workspace_bytes, stream);
 }
 
 // ----------------------------------------------------------------- bounded-wait self-test

@@ -98,6 +98,12 @@ struct KlArgs {
   const float* g;                          // [B*H][Nq]: upstream gradient (backward)
   float* part;                             // forward, splits > 1: [5][splits][B*H][Nq] per-slice state
   int splits;                              // forward: key slices per query tile (1: none)
+  // fused backward (atomic dQ): fp32 accumulator [B*H][Nq_pad][d], its 2-D map (d = 64, as in
+  // BwdArgs), and three planes of per-row values [3][B*H][Nq_pad]
+  float* dq_acc;
+  CUtensorMap tm_dqacc;
+  float* rowv;
+  int Nq_pad;
   uint32_t* err_word;
   int bh_count, heads, Nq, Nk, d;
   bool causal, bf16;
@@ -123,5 +129,8 @@ cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_pair_dq(const PairDqArgs& a, cudaStream_t stream);
 cudaError_t launch_kl_fwd(const KlArgs& a, cudaStream_t stream);
 cudaError_t launch_kl_dk(const KlArgs& a, cudaStream_t stream);
+// Row values + zeroed accumulator, then the one-pass key-tile kernel (dK and the dQ reduce-adds); the
+// caller converts the accumulator with the attention backward's kBwdConvert step.
+cudaError_t launch_kl_bwd_fused(const KlArgs& a, cudaStream_t stream);
 
 }  // namespace exattn

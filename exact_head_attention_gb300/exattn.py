@@ -84,6 +84,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_kl_fwd.restype = i
             lib.attn_kl_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, f, i, vp]
             lib.attn_kl_bwd.restype = i
+            lib.attn_kl_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, f, i, i, vp,
+                                           sz, vp]
+            lib.attn_kl_bwd_ex.restype = i
+            lib.attn_kl_bwd_workspace_size.argtypes = [i, i, i, i]
+            lib.attn_kl_bwd_workspace_size.restype = sz
             lib.attn_selftest_wait_timeout.argtypes = [i, vp]
             lib.attn_selftest_wait_timeout.restype = i
             lib.attn_kl_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, sz, vp]
@@ -350,6 +355,21 @@ def kl_bwd_raw(q1, k1, q2, k2, kl, lse1, lse2, g, setting, dq, dk, causal, scale
                               float(scale), _dtype_code(q1), _stream(stream))
 
 
+def kl_bwd_workspace_size(B: int, H: int, Nq: int, d: int) -> int:
+    """Workspace bytes of the one-pass KL backward (attn_kl_bwd_workspace_size)."""
+    return int(load().attn_kl_bwd_workspace_size(B, H, Nq, d))
+
+
+def kl_bwd_ex_raw(q1, k1, q2, k2, kl, lse1, lse2, g, setting, dq, dk, causal, scale: float, dq_mode, workspace,
+                  stream=None) -> int:
+    """Calls attn_kl_bwd_ex (dQ mode, workspace) on caller-provided contiguous tensors; returns the status."""
+    B, H, Nq, Nk, d = _dims(q1, k1)
+    return load().attn_kl_bwd_ex(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(kl), _ptr(lse1), _ptr(lse2), _ptr(g),
+                                 KL_SETTINGS[setting], _ptr(dq), _ptr(dk), B, H, Nq, Nk, d, mask_code(causal),
+                                 float(scale), _dtype_code(q1), dq_mode_code(dq_mode), *_workspace(workspace),
+                                 _stream(stream))
+
+
 def kl_forward(q1, k1, q2, k2, causal=False, scale: float | None = None, stream=None):
     """Row-wise KL(P1 || P2) of the student (q2, k2) from the teacher (q1, k1): (KL, LSE1, LSE2) [B,H,Nq] fp32."""
     B, H, Nq, Nk, d = _dims(q1, k1)
@@ -374,34 +394,44 @@ def kl_forward_splitkv(q1, k1, q2, k2, causal=False, scale: float | None = None,
 
 
 def kl_backward(q1, k1, q2, k2, kl, lse1, lse2, g, train="student", causal=False, scale: float | None = None,
-                stream=None):
-    """(dQ, dK) of sum(g * KL) for the trained distribution ("student": Q2, K2; "teacher": Q1, K1)."""
+                stream=None, dq_mode="atomic", workspace=None):
+    """(dQ, dK) of sum(g * KL) for the trained distribution ("student": Q2, K2; "teacher": Q1, K1).
+
+    dq_mode: "atomic" / "auto" (one pass over key tiles, dQ added into an fp32 accumulator; `workspace`
+    is allocated if omitted) or "deterministic" (attn_kl_bwd: two launches, the same bits on every run)."""
     B, H, Nq, Nk, d = _dims(q1, k1)
     scale = (1.0 / d ** 0.5) if scale is None else scale
     dq, dk = torch.empty_like(q1), torch.empty_like(k1)
-    _check(kl_bwd_raw(q1, k1, q2, k2, kl, lse1, lse2, g.contiguous().float(), train, dq, dk, causal, scale, stream),
-           "attn_kl_bwd")
+    g = g.contiguous().float()
+    if dq_mode_code(dq_mode) == DQ_MODES["deterministic"]:
+        _check(kl_bwd_raw(q1, k1, q2, k2, kl, lse1, lse2, g, train, dq, dk, causal, scale, stream), "attn_kl_bwd")
+        return dq, dk
+    if workspace is None:
+        workspace = torch.empty(kl_bwd_workspace_size(B, H, Nq, d), dtype=torch.uint8, device=q1.device)
+    _check(kl_bwd_ex_raw(q1, k1, q2, k2, kl, lse1, lse2, g, train, dq, dk, causal, scale, dq_mode, workspace, stream),
+           "attn_kl_bwd_ex")
     return dq, dk
 
 
 class _KlFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q1, k1, q2, k2, causal, scale, train):
+    def forward(ctx, q1, k1, q2, k2, causal, scale, train, dq_mode):
         kl, lse1, lse2 = kl_forward(q1, k1, q2, k2, causal, scale)
         ctx.save_for_backward(q1, k1, q2, k2, kl, lse1, lse2)
-        ctx.causal, ctx.scale, ctx.train = causal, scale, train
+        ctx.causal, ctx.scale, ctx.train, ctx.dq_mode = causal, scale, train, dq_mode
         return kl
 
     @staticmethod
     def backward(ctx, g):
         q1, k1, q2, k2, kl, lse1, lse2 = ctx.saved_tensors
-        dq, dk = kl_backward(q1, k1, q2, k2, kl, lse1, lse2, g, ctx.train, ctx.causal, ctx.scale)
+        dq, dk = kl_backward(q1, k1, q2, k2, kl, lse1, lse2, g, ctx.train, ctx.causal, ctx.scale,
+                             dq_mode=ctx.dq_mode)
         if KL_SETTINGS[ctx.train] == 1:
-            return None, None, dq, dk, None, None, None
-        return dq, dk, None, None, None, None, None
+            return None, None, dq, dk, None, None, None, None
+        return dq, dk, None, None, None, None, None, None
 
 
-def attention_kl(q1, k1, q2, k2, causal=False, scale: float | None = None, train="student"):
+def attention_kl(q1, k1, q2, k2, causal=False, scale: float | None = None, train="student", dq_mode="atomic"):
     """Autograd-aware row-wise KL(P1 || P2) [B,H,Nq]; gradients flow to the trained distribution only."""
     scale = (1.0 / q1.shape[-1] ** 0.5) if scale is None else scale
-    return _KlFunction.apply(q1, k1, q2, k2, causal, scale, train)
+    return _KlFunction.apply(q1, k1, q2, k2, causal, scale, train, dq_mode)

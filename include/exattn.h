@@ -222,6 +222,35 @@ attn_status attn_kl_bwd(const void* Q1, const void* K1, const void* Q2, const vo
                         void* stream);
 
 /*
+ * Bytes of device workspace attn_kl_bwd_ex needs in the one-pass mode: an fp32
+ * dQ accumulator [B,H,ceil(Nq/128)*128,d] plus three fp32 row vectors of that
+ * padded length.  Returns 0 for invalid sizes.
+ */
+size_t attn_kl_bwd_workspace_size(int B, int H, int Nq, int d);
+
+/*
+ * attn_kl_bwd with a choice of how dQ is produced (dq_mode, an attn_dq_mode
+ * value).  ATTN_DQ_DETERMINISTIC is attn_kl_bwd: two launches, no atomics, the
+ * same bits on every run; the workspace is unused and may be NULL.
+ * ATTN_DQ_ATOMIC and ATTN_DQ_AUTO take the StreamKL summary's one-pass form
+ * (Methodology 2, fusion choice): one block per key tile recomputes both
+ * distributions' scores once, accumulates dK on chip and adds its dQ
+ * contribution into an fp32 accumulator in the workspace (copy-engine
+ * reduce-adds through L2); a last launch writes dQ = scale * accumulator.
+ * Four score-sized products per (query tile, key tile) pair instead of six.
+ * dK is the same bits on every run; dQ's summation order across key tiles is
+ * not fixed.  workspace: at least attn_kl_bwd_workspace_size(B,H,Nq,d) bytes,
+ * 256-byte aligned, contents on entry irrelevant.  Errors as attn_kl_bwd, plus
+ * ATTN_ERR_INVALID_ARG for an unknown dq_mode, ATTN_ERR_WORKSPACE for a
+ * missing or small workspace and ATTN_ERR_MISALIGNED for a workspace that is
+ * not 256-byte aligned (one-pass modes).
+ */
+attn_status attn_kl_bwd_ex(const void* Q1, const void* K1, const void* Q2, const void* K2, const float* KL,
+                           const float* LSE1, const float* LSE2, const float* G, int setting, void* dQ, void* dK,
+                           int B, int H, int Nq, int Nk, int d, int causal, float scale, attn_dtype dtype,
+                           int dq_mode, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Bytes of device workspace attn_bwd needs for this shape: an fp32 dQ
  * accumulator [B,H,ceil(Nq/128)*128,d] plus two fp32 row vectors of the same
  * padded length (D = rowsum(dO o O) and the base-2 LSE).  Returns 0 for

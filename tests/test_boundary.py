@@ -187,6 +187,26 @@ def test_kl_rejects_bad_arguments(lib):
     assert lib.attn_kl_bwd(*p4, *g, 1, ctypes.c_void_p(FAKE + 2), out[1], 1, 1, 128, 128, 64, 0, 0.125, 0, None) == 3
 
 
+def test_kl_bwd_ex_rejects_bad_arguments(lib):
+    B, H, Nq, Nk, d = 2, 3, 200, 300, 64
+    rows = B * H * 256  # Nq padded to whole 128-row tiles
+    align = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    need = lib.attn_kl_bwd_workspace_size(B, H, Nq, d)
+    assert need == align(rows * d * 4) + align(3 * rows * 4)
+    assert lib.attn_kl_bwd_workspace_size(0, H, Nq, d) == 0
+    assert lib.attn_kl_bwd_workspace_size(B, H, Nq, 96) == 0
+    p4, g, out = [ctypes.c_void_p(FAKE)] * 4, [ctypes.c_void_p(FAKE)] * 4, [ctypes.c_void_p(FAKE)] * 2
+    call = lambda mode, ws=FAKE, nbytes=need, setting=1: lib.attn_kl_bwd_ex(  # noqa: E731
+        *p4, *g, setting, *out, B, H, Nq, Nk, d, 0, 0.125, 0, mode, ctypes.c_void_p(ws) if ws else None, nbytes, None)
+    for mode in (-1, 3):
+        assert call(mode) == 1
+    assert call(0, setting=0) == 1
+    for mode in (0, 2):  # the one-pass modes need the workspace
+        assert call(mode, ws=None) == 6
+        assert call(mode, nbytes=need - 1) == 6
+        assert call(mode, ws=FAKE + 16) == 3
+
+
 def test_selftest_rejects_bad_timeout(lib):
     for ms in (0, -5, 10001):
         assert lib.attn_selftest_wait_timeout(ms, None) == 1
