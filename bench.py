@@ -582,14 +582,15 @@ def run_kl(args, w, rank: int, world: int) -> None:
     d = {k: v.to(dev) for k, v in x.items()}
     kl, l1, l2 = (torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev) for _ in range(3))
     dq, dk = torch.empty_like(d["q2"]), torch.empty_like(d["k2"])
+    kws = torch.empty(exattn.kl_bwd_workspace_size(w.B, w.H, w.Nq, w.d), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def launch(ev=None):
         s1 = exattn.kl_fwd_raw(d["q1"], d["k1"], d["q2"], d["k2"], kl, l1, l2, w.causal, w.scale)
         if ev:
             ev[1].record(stream)
-        s2 = exattn.kl_bwd_raw(d["q1"], d["k1"], d["q2"], d["k2"], kl, l1, l2, d["g"], "student", dq, dk, w.causal,
-                               w.scale)
+        s2 = exattn.kl_bwd_ex_raw(d["q1"], d["k1"], d["q2"], d["k2"], kl, l1, l2, d["g"], "student", dq, dk, w.causal,
+                                  w.scale, args.kl_dq_mode, kws)
         if ev:
             ev[2].record(stream)
         if s1 or s2:
@@ -630,7 +631,7 @@ def run_kl(args, w, rank: int, world: int) -> None:
     h2d = sum(t.numel() * t.element_size() for t in h.values())
     d2h = sum(t.numel() * t.element_size() for t in (hkl, hdq, hdk))
 
-    slots = [dict(d, kl=kl, l1=l1, l2=l2, dq=dq, dk=dk)]
+    slots = [dict(d, kl=kl, l1=l1, l2=l2, dq=dq, dk=dk, kws=kws)]
     slots.append({n: torch.empty_like(t) for n, t in slots[0].items()})
 
     def h2d_(sl):
@@ -640,8 +641,8 @@ def run_kl(args, w, rank: int, world: int) -> None:
     def compute_(sl, s):
         s1 = exattn.kl_fwd_raw(sl["q1"], sl["k1"], sl["q2"], sl["k2"], sl["kl"], sl["l1"], sl["l2"], w.causal, w.scale,
                                stream=s)
-        s2 = exattn.kl_bwd_raw(sl["q1"], sl["k1"], sl["q2"], sl["k2"], sl["kl"], sl["l1"], sl["l2"], sl["g"], "student",
-                               sl["dq"], sl["dk"], w.causal, w.scale, stream=s)
+        s2 = exattn.kl_bwd_ex_raw(sl["q1"], sl["k1"], sl["q2"], sl["k2"], sl["kl"], sl["l1"], sl["l2"], sl["g"],
+                                  "student", sl["dq"], sl["dk"], w.causal, w.scale, args.kl_dq_mode, sl["kws"], stream=s)
         if s1 or s2:
             raise RuntimeError(f"C-ABI status {(s1, s2)}: {exattn.last_error()}")
 
@@ -665,12 +666,14 @@ def run_kl(args, w, rank: int, world: int) -> None:
         "dtype": "bf16" if w.dtype == "bf16" else "fp16",
         "data": "synthetic: seeded normal teacher Q,K (sigma 1); student = teacher + noise (sigma %.2g); g ~ N(0,1)"
                 % workloads.KL_STUDENT_NOISE,
-        "config": config_dict(w, {"kind": "kl", "train": "student", "flops_per_step": ff + bf,
+        "config": config_dict(w, {"kind": "kl", "train": "student", "dq_mode": args.kl_dq_mode, "flops_per_step": ff + bf,
                                   "parallelism": "replicas" if world > 1 else "single GPU",
                                   "l2": "256 MiB flush write between timed steps, outside the CUDA events"}),
-        "kernels_ms": {"kl_fwd": fwd_ms, "kl_bwd (dQ + dK kernels)": bwd_ms},
+        "kernels_ms": {"kl_fwd": fwd_ms, "kl_bwd": bwd_ms},
         "fwd_tflops": ff / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": achieved,
-        "roofline": {"kernel": "pair_dq_kernel + kl_dk_kernel (attn_kl_bwd)", "bound": "tensor", "achieved": achieved,
+        "roofline": {"kernel": ("kl_bwd_fused_kernel with its pre and conversion launches (attn_kl_bwd_ex, one pass)"
+                                if args.kl_dq_mode == "atomic" else "pair_dq_kernel + kl_dk_kernel (attn_kl_bwd)"),
+                     "bound": "tensor", "achieved": achieved,
                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
                      "traffic": None, "peak_kind": f"bf16 dense burst ({pk['source']})"},
         "cpu_baseline": cpu,
@@ -696,6 +699,8 @@ def main() -> None:
     ap.add_argument("--workload", default=None)
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--kl-dq-mode", choices=("atomic", "deterministic"), default="atomic",
+                    help="attention-KL workloads: the one-pass backward (atomic dQ) or the repeatable two-kernel one")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
