@@ -320,13 +320,19 @@ def traffic_from_profile(kernel_key: str) -> float | None:
 
 
 def kernel_source_sha() -> str:
-    """Hash of the headline kernels' sources with comments and blank lines removed (a comment edit
-    leaves the compiled kernels, and so the profiled traffic, unchanged)."""
+    """Hash of what the headline kernels compile from, with comments and blank lines removed (a comment
+    edit leaves the compiled kernels, and so the profiled traffic, unchanged): their translation units,
+    the device headers they include, and from kernels.h the argument structs they take and the integer
+    constants (the other workloads' structs there do not change these kernels)."""
     h = hashlib.sha256()
     for f in ("attn_fwd.cu", "attn_bwd.cu", "ptx.cuh", "kernels.h", "softmax.cuh"):
         src = open(os.path.join(ROOT, "exact_head_attention_gb300", "csrc", f)).read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
         src = re.sub(r"//[^\n]*", "", src)
+        if f == "kernels.h":
+            parts = [m.group(0) for m in re.finditer(r"struct (RowStrides|FwdArgs|BwdArgs) \{.*?\};", src, flags=re.S)]
+            parts += re.findall(r"constexpr int [^;]*;", src)
+            src = "\n".join(parts)
         h.update("\n".join(ln.rstrip() for ln in src.splitlines() if ln.strip()).encode())
     return h.hexdigest()[:16]
 
