@@ -313,6 +313,8 @@ attn_status bwd_steps(const void* Q, const void* K, const void* V, const void* O
   if (dq_mode == ATTN_DQ_DETERMINISTIC) {
     a.dq_acc = nullptr;  // no accumulator: dK, dV from the key/value blocks, dQ from the query-tile kernel
     steps = kBwdDeterministic;
+  } else if (d == 64 && rows > 0x7fffffffull) {
+    return ATTN_ERR_INVALID_ARG;  // the accumulator map's row coordinate is a 32-bit integer
   } else if (d == 64 && (r = encode_acc_map(&a.tm_dqacc, a.dq_acc, rows, d)) != CUDA_SUCCESS) {
     return driver_fail("cuTensorMapEncodeTiled(dQ accumulator)", r);
   }
@@ -680,6 +682,7 @@ attn_status kl_bwd_impl(const void* Q1, const void* K1, const void* Q2, const vo
     a.dq_acc = reinterpret_cast<float*>(ws);
     a.rowv = reinterpret_cast<float*>(ws + align256(rows * d * sizeof(float)));
     a.Nq_pad = padded_rows(Nq);
+    if (d == 64 && rows > 0x7fffffffull) return ATTN_ERR_INVALID_ARG;  // 32-bit row coordinate of the map
     if (d == 64 && (r = encode_acc_map(&a.tm_dqacc, a.dq_acc, rows, d)) != CUDA_SUCCESS)
       return driver_fail("cuTensorMapEncodeTiled (accumulator)", r);
     cudaError_t e = launch_kl_bwd_fused(a, s);
