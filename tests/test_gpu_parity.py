@@ -115,6 +115,18 @@ def test_long_workloads_full_size_sampled(name):
     _check_invariants(w, x, got, name)
 
 
+@pytest.mark.parametrize("shape", [(1, 1, 200003, 200003, 64, "bf16", True),
+                                   (1, 1, 100001, 131075, 128, "bf16", "bottom_right")],
+                         ids=["q200003_d64_causal", "q100001_k131075_d128_bottom_right"])
+def test_very_long_sequences_sampled(shape):
+    """Sequences far past the workloads' 32k: tensor-map row coordinates above 2^17, ~1500 key blocks,
+    a ragged last tile; sampled rows and the last key rows against the oracle."""
+    w = workloads.custom(*shape, index=31)
+    x = workloads.make_inputs(w)
+    got = run_gpu(w, x)
+    _sampled_check(w, x, got, 24, [(0, 0)], seed=w.index)
+
+
 def test_outputs_written_everywhere():
     """Outputs pre-filled with NaN must be fully overwritten (ragged shapes included)."""
     from exact_head_attention_gb300 import exattn
