@@ -686,7 +686,8 @@ def run_kl(args, w, rank: int, world: int) -> None:
         "e2e": ({"value": world * (ff + bf) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                  "alone_ms_per_step": alone_ms, "timing": E2E_NOTE} if args.e2e_steps else None),
-        "gpu_launches": 3 * args.steps,
+        # forward, then pre + one-pass kernel + dQ conversion (atomic) or the dQ and dK kernels
+        "gpu_launches": (4 if args.kl_dq_mode == "atomic" else 3) * args.steps,
         "clocks": sampler.summary(t_wall0, t_wall1),
         "wall_s_timed_region": t_wall1 - t_wall0,
     }
