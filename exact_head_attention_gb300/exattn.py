@@ -149,9 +149,17 @@ def _all_contiguous(*ts) -> bool:
     return all(t.is_contiguous() for t in ts)
 
 
+# The current stream's raw handle without building a Stream object (several microseconds a call);
+# the public call is the fallback where this accessor is absent.
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    if _RAW_STREAM is not None:
+        return ctypes.c_void_p(_RAW_STREAM(torch.cuda.current_device()))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def _dims(q, k):
