@@ -461,15 +461,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-__device__ __forceinline__ void red_add_f32(float* gaddr, float a) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gaddr), "f"(a) : "memory");
-}
-
-__device__ __forceinline__ void red_add_v4(float* gaddr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gaddr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
 // Byte offset of 16-byte unit `u` (0..7) of row `r` inside a 128-row x
 // 128-byte chunk stored with the 128-byte swizzle (unit index XOR row % 8).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t u) {

@@ -298,8 +298,8 @@ attn_status attn_bwd_strided(const void* Q, attn_strides q_strides, const void* 
 /*
  * How the backward produces dQ (attn_bwd_ex, attn_bwd_strided_ex).
  *   ATTN_DQ_ATOMIC         every key/value block adds its dQ contribution into
- *                          an fp32 accumulator (copy-engine reduce-adds at
- *                          d = 128, vector reductions at d = 64); the order
+ *                          an fp32 accumulator (copy-engine reduce-adds of
+ *                          shared-memory tiles); the order
  *                          of the additions varies, so dQ may differ between
  *                          runs in its last bits.  This is attn_bwd.
  *   ATTN_DQ_DETERMINISTIC  the key/value blocks produce dK and dV only; a
