@@ -128,7 +128,7 @@ __device__ __forceinline__ constexpr uint32_t p_stride() { return D == 64 ? 32u 
 template <int D>
 __device__ __forceinline__ uint32_t p_col(int k) { return p_base<D>() + (k < 4 ? k * 8 : p_stride<D>() + (k - 4) * 8); }
 
-// DQ = false: dK and dV only (the deterministic mode computes dQ in bwd_dq_kernel instead); the dQ
+// DQ = false: dK and dV only (the deterministic mode computes dQ in pair_dq_kernel (attn_bwd_dq.cu) instead); the dQ
 // MMA, the dS^T tile in shared memory and the reductions are left out.
 template <int D, bool CAUSAL, bool BF16, bool DQ>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
@@ -659,7 +659,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int steps, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   if (steps & kBwdMain) {
-    // no accumulator: the deterministic mode, where bwd_dq_kernel produces dQ
+    // no accumulator: the deterministic mode, where pair_dq_kernel produces dQ
     auto kern = a.dq_acc ? bwd_main_kernel<D, CAUSAL, BF16, true> : bwd_main_kernel<D, CAUSAL, BF16, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
