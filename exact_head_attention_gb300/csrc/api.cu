@@ -247,6 +247,33 @@ extern "C" size_t attn_bwd_workspace_size(int B, int H, int Nq, int d) {
   return align256(rows * d * sizeof(float)) + 2 * align256(rows * sizeof(float));
 }
 
+// ATTN_DQ_AUTO.  The StreamKL summary (backward, kernel fusion) adds dQ atomically while the buffer fits
+// in L2 and uses separate kernels when contention grows.  What decides on GB300 is whether the key
+// blocks that add into the same head's rows find them still in L2.  Blocks are launched head-fastest,
+// so consecutive key blocks of one head run B*H blocks apart; with at least one head per SM they run in
+// different waves, and the whole accumulator passes through L2 between them.  Only then, with an
+// accumulator larger than L2, at least 8 key blocks per head, no causal mask to halve the revisits, and
+// d = 128 (the query-tile kernel is far slower at d = 64), did the query-tile kernel measure faster, by
+// 2-7 %; in every other measured case the reductions won, by up to 39 %.
+extern "C" int attn_bwd_auto_dq_mode(int B, int H, int Nq, int Nk, int d, int causal, int sm_count,
+                                     size_t l2_bytes) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return -1;
+  if (sm_count <= 0 || l2_bytes == 0) {
+    int dev = 0, sms = 0, l2 = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+      return ATTN_DQ_ATOMIC;
+    if (sm_count <= 0) sm_count = sms;
+    if (l2_bytes == 0) l2_bytes = static_cast<size_t>(l2);
+  }
+  const long long bh = static_cast<long long>(B) * H;
+  const size_t acc_bytes = static_cast<size_t>(bh) * padded_rows(Nq) * d * sizeof(float);
+  const bool deterministic =
+      d == 128 && causal == ATTN_MASK_NONE && bh >= sm_count && acc_bytes > l2_bytes && Nk >= 8 * kTileRows;
+  return deterministic ? ATTN_DQ_DETERMINISTIC : ATTN_DQ_ATOMIC;
+}
+
 namespace {
 
 // Tensor views of one backward call (element strides; d contiguous).
@@ -281,10 +308,7 @@ attn_status bwd_steps(const void* Q, const void* K, const void* V, const void* O
       (r = encode_map(&a.tm_dv, dV, bf16, B, H, Nk, d, vw.dv)) != CUDA_SUCCESS ||
       (r = encode_map(&a.tm_dq, dQ, bf16, B, H, Nq, d, vw.dq)) != CUDA_SUCCESS)
     return driver_fail("cuTensorMapEncodeTiled", r);
-  // ATTN_DQ_AUTO: the reductions into the fp32 accumulator were faster than the query-tile kernel on every
-  // shape measured on GB300 (accumulators up to four times the L2, one head whose key blocks all add into
-  // the same rows at once), so the choice resolves to them.
-  if (dq_mode == ATTN_DQ_AUTO) dq_mode = ATTN_DQ_ATOMIC;
+  if (dq_mode == ATTN_DQ_AUTO) dq_mode = attn_bwd_auto_dq_mode(B, H, Nq, Nk, d, causal, 0, 0);
   const int nq_pad = padded_rows(Nq);
   const size_t rows = static_cast<size_t>(bh) * nq_pad;
   uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -310,17 +310,13 @@ attn_status attn_bwd_strided(const void* Q, attn_strides q_strides, const void* 
  *                          every run; S and dP are computed twice (seven
  *                          tile products per key/query tile pair instead of
  *                          five).
- *   ATTN_DQ_AUTO           the faster of the two for the shape.  The StreamKL
+ *   ATTN_DQ_AUTO           the faster of the two for the shape, as
+ *                          attn_bwd_auto_dq_mode decides.  The StreamKL
  *                          summary (backward, kernel fusion) picks atomics
  *                          while the buffer fits in L2 and separate kernels
- *                          when contention on it grows.  On GB300 the
- *                          reductions beat the separate kernel on every shape
- *                          measured: fp32 accumulators from 4 MiB to four
- *                          times the L2 size, causal and not, and one head
- *                          whose 256 key blocks all add into the same rows at
- *                          once.  So AUTO resolves to ATTN_DQ_ATOMIC;
- *                          determinism is the only reason to ask for the
- *                          other mode.
+ *                          when contention on it grows; on GB300 the separate
+ *                          kernel wins only when the additions into a head's
+ *                          rows miss L2 (see attn_bwd_auto_dq_mode).
  * SparkAttention Figure 9 adds dQ across thread blocks atomically.
  */
 typedef enum {
@@ -328,6 +324,19 @@ typedef enum {
   ATTN_DQ_DETERMINISTIC = 1,
   ATTN_DQ_AUTO = 2
 } attn_dq_mode;
+
+/*
+ * The mode ATTN_DQ_AUTO resolves to for a backward of this shape (causal: an
+ * attn_mask value): ATTN_DQ_DETERMINISTIC when d = 128, there is no mask, B*H
+ * is at least sm_count (one head per SM or more, so the key blocks adding into
+ * one head's rows run in different waves), the fp32 accumulator
+ * (attn_bwd_workspace_size's first part) is larger than l2_bytes, and there are
+ * at least 8 key blocks per head (Nk >= 1024); ATTN_DQ_ATOMIC otherwise.  On
+ * GB300 that is where the query-tile kernel measured 2-7 % faster; everywhere
+ * else the reductions were faster, by up to 39 %.  sm_count <= 0 or
+ * l2_bytes = 0 take the current device's values.  Returns -1 for invalid sizes.
+ */
+int attn_bwd_auto_dq_mode(int B, int H, int Nq, int Nk, int d, int causal, int sm_count, size_t l2_bytes);
 
 /*
  * attn_bwd with a dQ mode (attn_dq_mode; other values are
