@@ -28,6 +28,8 @@ struct DeviceState {
   bool ready = false;
   bool supported = false;
   uint32_t* err_word = nullptr;  // device address of g_error_word on this device
+  size_t l2_bytes = 0;
+  int sm_count = 0;
 };
 
 std::mutex g_mutex;
@@ -78,6 +80,12 @@ attn_status device_state(DeviceState** out) {
       return cuda_fail("cudaDeviceGetAttribute", e);
     st.supported = (major == 10 && minor == 3);
     if (st.supported) {
+      int l2 = 0, sms = 0;
+      if ((e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return cuda_fail("cudaDeviceGetAttribute", e);
+      st.l2_bytes = static_cast<size_t>(l2);
+      st.sm_count = sms;
       void* p = nullptr;
       if ((e = cudaGetSymbolAddress(&p, g_error_word)) != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
       st.err_word = static_cast<uint32_t*>(p);
@@ -158,6 +166,8 @@ attn_status check_common(int B, int H, int Nq, int Nk, int d, int causal, float 
   if (bh > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   // grid.y limit of the forward (256 query rows per block) and of the backward (128 key rows per block)
   if ((Nq + 255) / 256 > 65535 || (Nk + 127) / 128 > 65535) return ATTN_ERR_INVALID_ARG;
+  // the key/value-block kernels number their B*H*ceil(Nk/128) blocks along grid.x in an int
+  if (bh * ((Nk + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
 
@@ -167,6 +177,26 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Diagonal offset of the causal mask: query q sees keys k <= q + offset.
 int causal_offset(int causal, int Nq, int Nk) { return causal == ATTN_MASK_CAUSAL_BOTTOM_RIGHT ? Nk - Nq : 0; }
+
+// Heads per launch group of the key/value-block kernels (kv_order.cuh) when they add dQ into an fp32
+// accumulator of acc_per_head bytes per head.  All heads in one group (heads fastest) while the whole
+// accumulator fits in a quarter of L2 with no mask, or in half of it under a causal mask (key block j
+// adds only into the rows at or after its own, and the heavy blocks of every head start first); the rest
+// of L2 holds the Q, dO, K and V tiles in flight.  Past that, groups whose accumulator rows take about a
+// sixteenth of L2, so each head's key blocks find its rows still in L2 (swept over 1 to 64 heads per
+// group on GB300, that size was within a few per cent of the best group on every shape).  Under a causal
+// mask the first key block of a head is the heaviest (it sees every query tile), and a group's first
+// blocks start only when that group does; a group of at least 2 * SMs / nkb heads has enough lighter
+// blocks to run beside them.
+int head_group(bool causal, long long bh, int Nk, size_t acc_per_head, const DeviceState* ds) {
+  if (static_cast<size_t>(bh) * acc_per_head <= (causal ? ds->l2_bytes / 2 : ds->l2_bytes / 4)) return static_cast<int>(bh);
+  long long g = std::max<long long>(1, static_cast<long long>(ds->l2_bytes / 16 / acc_per_head));
+  if (causal) {
+    const long long nkb = (Nk + kTileRows - 1) / kTileRows;
+    g = std::max(g, (2LL * ds->sm_count + nkb - 1) / nkb);
+  }
+  return static_cast<int>(std::min(g, bh));
+}
 
 attn_status finish(cudaError_t e, cudaStream_t stream) {
   if (e != cudaSuccess) return cuda_fail("kernel launch", e);
@@ -249,29 +279,13 @@ extern "C" size_t attn_bwd_workspace_size(int B, int H, int Nq, int d) {
 
 // ATTN_DQ_AUTO.  The StreamKL summary (backward, kernel fusion) adds dQ atomically while the buffer fits
 // in L2 and uses separate kernels when contention grows.  What decides on GB300 is whether the key
-// blocks that add into the same head's rows find them still in L2.  Blocks are launched head-fastest,
-// so consecutive key blocks of one head run B*H blocks apart; with at least one head per SM they run in
-// different waves, and the whole accumulator passes through L2 between them.  Only then, with an
-// accumulator larger than L2, at least 8 key blocks per head, no causal mask to halve the revisits, and
-// d = 128 (the query-tile kernel is far slower at d = 64), did the query-tile kernel measure faster, by
-// 2-7 %; in every other measured case the reductions won, by up to 39 %.
-extern "C" int attn_bwd_auto_dq_mode(int B, int H, int Nq, int Nk, int d, int causal, int sm_count,
-                                     size_t l2_bytes) {
+// blocks that add into the same head's rows find them still in L2, and the launch order
+// (head_group) sees to that: a head's blocks run close together whenever the accumulator as a whole
+// would not stay in L2.  The reductions then measured faster than the query-tile kernel on every
+// shape tried, by 1.3x to 1.6x, so the rule takes them for every shape; the mask is not needed.
+extern "C" int attn_bwd_auto_dq_mode(int B, int H, int Nq, int Nk, int d, int /*causal*/) {
   if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return -1;
-  if (sm_count <= 0 || l2_bytes == 0) {
-    int dev = 0, sms = 0, l2 = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
-      return ATTN_DQ_ATOMIC;
-    if (sm_count <= 0) sm_count = sms;
-    if (l2_bytes == 0) l2_bytes = static_cast<size_t>(l2);
-  }
-  const long long bh = static_cast<long long>(B) * H;
-  const size_t acc_bytes = static_cast<size_t>(bh) * padded_rows(Nq) * d * sizeof(float);
-  const bool deterministic =
-      d == 128 && causal == ATTN_MASK_NONE && bh >= sm_count && acc_bytes > l2_bytes && Nk >= 8 * kTileRows;
-  return deterministic ? ATTN_DQ_DETERMINISTIC : ATTN_DQ_ATOMIC;
+  return ATTN_DQ_ATOMIC;
 }
 
 namespace {
@@ -308,7 +322,7 @@ attn_status bwd_steps(const void* Q, const void* K, const void* V, const void* O
       (r = encode_map(&a.tm_dv, dV, bf16, B, H, Nk, d, vw.dv)) != CUDA_SUCCESS ||
       (r = encode_map(&a.tm_dq, dQ, bf16, B, H, Nq, d, vw.dq)) != CUDA_SUCCESS)
     return driver_fail("cuTensorMapEncodeTiled", r);
-  if (dq_mode == ATTN_DQ_AUTO) dq_mode = attn_bwd_auto_dq_mode(B, H, Nq, Nk, d, causal, 0, 0);
+  if (dq_mode == ATTN_DQ_AUTO) dq_mode = attn_bwd_auto_dq_mode(B, H, Nq, Nk, d, causal);
   const int nq_pad = padded_rows(Nq);
   const size_t rows = static_cast<size_t>(bh) * nq_pad;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -334,6 +348,9 @@ attn_status bwd_steps(const void* Q, const void* K, const void* V, const void* O
   a.bf16 = bf16;
   a.scale = scale;
   a.timeout_ns = wait_timeout_ns();
+  // deterministic mode: no accumulator, heads fastest
+  a.head_group = dq_mode == ATTN_DQ_DETERMINISTIC ? static_cast<int>(bh)
+                                                  : head_group(a.causal, bh, Nk, static_cast<size_t>(nq_pad) * d * sizeof(float), ds);
   if (dq_mode == ATTN_DQ_DETERMINISTIC) {
     a.dq_acc = nullptr;  // no accumulator: dK, dV from the key/value blocks, dQ from the query-tile kernel
     steps = kBwdDeterministic;
@@ -706,6 +723,7 @@ attn_status kl_bwd_impl(const void* Q1, const void* K1, const void* Q2, const vo
     a.dq_acc = reinterpret_cast<float*>(ws);
     a.rowv = reinterpret_cast<float*>(ws + align256(rows * d * sizeof(float)));
     a.Nq_pad = padded_rows(Nq);
+    a.head_group = head_group(a.causal, a.bh_count, Nk, static_cast<size_t>(a.Nq_pad) * d * sizeof(float), ds);
     if (d == 64 && rows > 0x7fffffffull) return ATTN_ERR_INVALID_ARG;  // 32-bit row coordinate of the map
     if (d == 64 && (r = encode_acc_map(&a.tm_dqacc, a.dq_acc, rows, d)) != CUDA_SUCCESS)
       return driver_fail("cuTensorMapEncodeTiled (accumulator)", r);

@@ -49,6 +49,7 @@
 #include <cuda_fp16.h>
 
 #include "kernels.h"
+#include "kv_order.cuh"
 #include "ptx.cuh"
 
 namespace exattn {
@@ -147,9 +148,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   const WaitCtx wc{abort_flag, a.err_word, a.timeout_ns};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
+  const int nkb = (a.Nk + kTileRows - 1) / kTileRows;
+  const KvBlock blk = kv_block(blockIdx.x, a.bh_count, a.head_group, nkb);
+  const int bh = blk.bh;
   const int head = bh % a.heads, batch = bh / a.heads;
-  const int jb = blockIdx.y;  // key block; causal work decreases with jb, so low jb are scheduled first
+  const int jb = blk.jb;  // key block; causal work decreases with jb
   const int k0 = jb * kTileRows;
   const int nq_tiles = (a.Nq + kTileRows - 1) / kTileRows;
   // Causal: query q sees key k iff k <= q + coff, so the first query tile to visit holds row k0 - coff.
@@ -663,8 +666,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int steps, cudaStream_t stream) {
     auto kern = a.dq_acc ? bwd_main_kernel<D, CAUSAL, BF16, true> : bwd_main_kernel<D, CAUSAL, BF16, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.bh_count, (a.Nk + kTileRows - 1) / kTileRows, 1);
-    kern<<<grid, kBwdThreads, C::SMEM_ALLOC, stream>>>(a);
+    const unsigned blocks = static_cast<unsigned>(a.bh_count) * ((a.Nk + kTileRows - 1) / kTileRows);
+    kern<<<blocks, kBwdThreads, C::SMEM_ALLOC, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

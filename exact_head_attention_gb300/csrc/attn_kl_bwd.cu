@@ -44,6 +44,7 @@
 #include <cuda_fp16.h>
 
 #include "kernels.h"
+#include "kv_order.cuh"
 #include "ptx.cuh"
 
 namespace exattn {
@@ -171,9 +172,11 @@ __global__ void __launch_bounds__(kKlBwdThreads, 1) kl_bwd_fused_kernel(const __
   const WaitCtx wc{abort_flag, a.err_word, a.timeout_ns};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
+  const int nkb = (a.Nk + kTileRows - 1) / kTileRows;
+  const KvBlock blk = kv_block(blockIdx.x, a.bh_count, a.head_group, nkb);  // launch order as in the attention backward
+  const int bh = blk.bh;
   const int head = bh % a.heads, batch = bh / a.heads;
-  const int jb = blockIdx.y;  // key tile; causal work decreases with jb, so low jb are scheduled first
+  const int jb = blk.jb;  // key tile; causal work decreases with jb
   const int k0 = jb * kTileRows;
   const int nq_tiles = (a.Nq + kTileRows - 1) / kTileRows;
   const int coff = CAUSAL ? a.causal_off : 0;
@@ -539,8 +542,8 @@ cudaError_t launch_kl_bwd_fused_t(const KlArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   auto kern = kl_bwd_fused_kernel<D, CAUSAL, BF16, OP>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES)) != cudaSuccess) return e;
-  dim3 grid(a.bh_count, (a.Nk + kTileRows - 1) / kTileRows, 1);
-  kern<<<grid, kKlBwdThreads, C::BYTES, stream>>>(a);
+  const unsigned blocks = static_cast<unsigned>(a.bh_count) * ((a.Nk + kTileRows - 1) / kTileRows);
+  kern<<<blocks, kKlBwdThreads, C::BYTES, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -45,6 +45,7 @@ struct BwdArgs {
   uint32_t* err_word;
   int bh_count, heads, Nq, Nq_pad, Nk, d;
   bool causal, bf16;
+  int head_group;  // heads per launch group of the key/value blocks (kv_order.cuh)
   int causal_off;
   float scale;
   uint64_t timeout_ns;
@@ -104,6 +105,7 @@ struct KlArgs {
   CUtensorMap tm_dqacc;
   float* rowv;
   int Nq_pad;
+  int head_group;  // as in BwdArgs
   uint32_t* err_word;
   int bh_count, heads, Nq, Nk, d;
   bool causal, bf16;

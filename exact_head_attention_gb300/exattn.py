@@ -95,7 +95,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_kl_fwd_splitkv.restype = i
             lib.attn_kl_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i, i]
             lib.attn_kl_fwd_splitkv_workspace_size.restype = sz
-            lib.attn_bwd_auto_dq_mode.argtypes = [i, i, i, i, i, i, i, sz]
+            lib.attn_bwd_auto_dq_mode.argtypes = [i, i, i, i, i, i]
             lib.attn_bwd_auto_dq_mode.restype = i
             lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
             lib.attn_bwd_workspace_size.restype = sz
@@ -268,11 +268,9 @@ def bwd_strided_raw(q, k, v, o, do, lse, dq, dk, dv, causal, scale: float, works
                                    float(scale), _dtype_code(q), *_workspace(workspace), _stream(stream))
 
 
-def auto_dq_mode(B: int, H: int, Nq: int, Nk: int, d: int, causal=False, sm_count: int = 0,
-                 l2_bytes: int = 0) -> str:
-    """The mode "auto" resolves to for this backward (attn_bwd_auto_dq_mode); sm_count / l2_bytes 0 take
-    the current device's values."""
-    code = int(load().attn_bwd_auto_dq_mode(B, H, Nq, Nk, d, mask_code(causal), sm_count, l2_bytes))
+def auto_dq_mode(B: int, H: int, Nq: int, Nk: int, d: int, causal=False) -> str:
+    """The mode "auto" resolves to for this backward (attn_bwd_auto_dq_mode)."""
+    code = int(load().attn_bwd_auto_dq_mode(B, H, Nq, Nk, d, mask_code(causal)))
     if code < 0:
         raise ValueError("invalid sizes")
     return {v: k for k, v in DQ_MODES.items()}[code]

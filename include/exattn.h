@@ -45,7 +45,9 @@ extern "C" {
 
 typedef enum {
   ATTN_OK = 0,
-  ATTN_ERR_INVALID_ARG = 1,     /* null pointer, non-positive size, bad scale, dtype, mask or strides */
+  ATTN_ERR_INVALID_ARG = 1,     /* null pointer, non-positive size, bad scale, dtype, mask or strides;
+                                   sizes past the launch limits: ceil(Nq/256) or ceil(Nk/128) above
+                                   65535, or B*H*ceil(Nk/128) above 2^31 - 1 */
   ATTN_ERR_UNSUPPORTED = 2,     /* d not in {64, 128}, or no sm_103a device */
   ATTN_ERR_MISALIGNED = 3,      /* a pointer is not 16-byte aligned */
   ATTN_ERR_CUDA = 4,            /* a CUDA runtime/driver call or launch failed */
@@ -301,7 +303,14 @@ attn_status attn_bwd_strided(const void* Q, attn_strides q_strides, const void* 
  *                          an fp32 accumulator (copy-engine reduce-adds of
  *                          shared-memory tiles); the order
  *                          of the additions varies, so dQ may differ between
- *                          runs in its last bits.  This is attn_bwd.
+ *                          runs in its last bits.  This is attn_bwd.  While
+ *                          the accumulator fits in half the L2 cache (a
+ *                          quarter with no mask) the key blocks are launched
+ *                          heads fastest (the heavy low causal blocks of
+ *                          every head start first); past that, in groups of
+ *                          a few heads, so the blocks adding into one head's
+ *                          rows run close together and find them still in
+ *                          L2.
  *   ATTN_DQ_DETERMINISTIC  the key/value blocks produce dK and dV only; a
  *                          second kernel, parallel over 128-row query tiles,
  *                          recomputes S, P, dP and dS for each key tile the
@@ -314,9 +323,10 @@ attn_status attn_bwd_strided(const void* Q, attn_strides q_strides, const void* 
  *                          attn_bwd_auto_dq_mode decides.  The StreamKL
  *                          summary (backward, kernel fusion) picks atomics
  *                          while the buffer fits in L2 and separate kernels
- *                          when contention on it grows; on GB300 the separate
- *                          kernel wins only when the additions into a head's
- *                          rows miss L2 (see attn_bwd_auto_dq_mode).
+ *                          when contention on it grows; with the launch order
+ *                          above, a head's additions stay in L2 whatever the
+ *                          accumulator's size, and on GB300 the reductions
+ *                          measured faster on every shape tried.
  * SparkAttention Figure 9 adds dQ across thread blocks atomically.
  */
 typedef enum {
@@ -327,16 +337,14 @@ typedef enum {
 
 /*
  * The mode ATTN_DQ_AUTO resolves to for a backward of this shape (causal: an
- * attn_mask value): ATTN_DQ_DETERMINISTIC when d = 128, there is no mask, B*H
- * is at least sm_count (one head per SM or more, so the key blocks adding into
- * one head's rows run in different waves), the fp32 accumulator
- * (attn_bwd_workspace_size's first part) is larger than l2_bytes, and there are
- * at least 8 key blocks per head (Nk >= 1024); ATTN_DQ_ATOMIC otherwise.  On
- * GB300 that is where the query-tile kernel measured 2-7 % faster; everywhere
- * else the reductions were faster, by up to 39 %.  sm_count <= 0 or
- * l2_bytes = 0 take the current device's values.  Returns -1 for invalid sizes.
+ * attn_mask value): ATTN_DQ_ATOMIC.  On GB300 the reductions measured 1.3x to
+ * 1.6x faster than the query-tile kernel on every shape tried (20 shapes with
+ * 16 MiB to 512 MiB of accumulator, causal and not, d = 64 and 128): the
+ * query-tile kernel recomputes S and dP, and with the launch order of
+ * ATTN_DQ_ATOMIC the reductions' working set stays in L2.  Returns -1 for
+ * invalid sizes.  Needs no device.
  */
-int attn_bwd_auto_dq_mode(int B, int H, int Nq, int Nk, int d, int causal, int sm_count, size_t l2_bytes);
+int attn_bwd_auto_dq_mode(int B, int H, int Nq, int Nk, int d, int causal);
 
 /*
  * attn_bwd with a dQ mode (attn_dq_mode; other values are

@@ -85,6 +85,10 @@ def test_bwd_rejects_bad_arguments(lib):
     assert _bwd(lib, ws_bytes=100) == 6
     assert _bwd(lib, ptrs=[FAKE] * 6 + [FAKE + 2] + [FAKE] * 2) == 3
     assert _bwd(lib, ws=FAKE + 16) == 3  # workspace must be 256-byte aligned
+    # launch limits: 65535 key blocks per head, and B*H*key blocks numbered in an int
+    assert _bwd(lib, Nk=65535 * 128 + 1) == 1
+    assert _bwd(lib, B=1 << 16, H=1 << 8, Nk=1 << 14) == 1
+    assert _bwd(lib, B=1 << 16, H=1 << 8, Nk=(1 << 14) - 128, ws=FAKE + 16) == 3  # one block fewer: size accepted
 
 
 @pytest.mark.parametrize("causal,code", [(3, 1), (-1, 1), (100, 1)])

@@ -107,9 +107,12 @@ def test_kl_autograd_routes_gradients():
     assert rel_l2(d["k2"].grad.float().cpu().numpy(), rdk) <= GRAD_TOL
 
 
-@pytest.mark.parametrize("mode", MODES)
-def test_kl_workload_full_size_sampled(mode):
-    w = workloads.WORKLOADS["kl8k_causal_bf16"]
+@pytest.mark.parametrize("mode,shape", [(m, None) for m in MODES] + [("atomic", (4, 16, 8192, 8192, 128, "bf16", True))],
+                         ids=lambda v: v if isinstance(v, str) else ("B{}H{}q{}k{}d{}{}{}".format(*v) if v else "kl8k"))
+def test_kl_workload_full_size_sampled(mode, shape):
+    """The 8k workload, and 64 heads whose 256 MiB dQ accumulator makes the one pass launch its key tiles
+    in groups of a few heads."""
+    w = workloads.WORKLOADS["kl8k_causal_bf16"] if shape is None else workloads.custom(*shape, index=33)
     x = workloads.make_kl_inputs(w)
     d = _dev(x)
     kl, l1, l2 = exattn.kl_forward(d["q1"], d["k1"], d["q2"], d["k2"], w.causal, w.scale)

@@ -115,6 +115,22 @@ def test_long_workloads_full_size_sampled(name):
     _check_invariants(w, x, got, name)
 
 
+def test_many_heads_causal_accumulator_beyond_l2_sampled():
+    """64 heads of 8192 causal rows: a 256 MiB dQ accumulator, twice the L2, so the key blocks are launched
+    in groups of a few heads instead of heads fastest (the last group taking the remainder); sampled rows
+    against the oracle."""
+    w = workloads.custom(4, 16, 8192, 8192, 128, "bf16", True, index=32)
+    x = workloads.make_inputs(w)
+    got = run_gpu(w, x)
+    for (b, h) in [(0, 0), (1, 7), (3, 15)]:
+        # the oracle sees one head at a time, so its row indices are the head's own
+        xs = {n: x[n][b:b + 1, h:h + 1] for n in ("q", "k", "v", "do")}
+        gs = {n: got[n][b:b + 1, h:h + 1] for n in ("o", "lse", "dq", "dk", "dv")}
+        ws = workloads.custom(1, 1, w.Nq, w.Nk, w.d, "bf16", True, index=32)
+        _sampled_check(ws, xs, gs, 32, [(0, 0)], seed=w.index + b * w.H + h)
+    _check_invariants(w, x, got, w.name)
+
+
 @pytest.mark.parametrize("shape", [(1, 1, 200003, 200003, 64, "bf16", True),
                                    (1, 1, 100001, 131075, 128, "bf16", "bottom_right")],
                          ids=["q200003_d64_causal", "q100001_k131075_d128_bottom_right"])
