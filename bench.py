@@ -752,7 +752,15 @@ def main() -> None:
     ws = torch.empty(exattn.workspace_size(w.B, w.H, w.Nq, w.d), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
+    def launch_step():
+        """One step as a caller runs it: the forward, then the whole backward in one call."""
+        st = (exattn.fwd_raw(q, k, v, o, lse, w.causal, w.scale),
+              exattn.bwd_raw(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, ws))
+        if any(st):
+            raise RuntimeError(f"C-ABI status {st}: {exattn.last_error()}")
+
     def launch(ev=None):
+        """The same step with each backward launch called on its own and an event after every kernel."""
         st = [exattn.fwd_raw(q, k, v, o, lse, w.causal, w.scale)]
         if ev:
             ev[1].record(stream)
@@ -764,6 +772,7 @@ def main() -> None:
             raise RuntimeError(f"C-ABI status {st}: {exattn.last_error()}")
 
     for _ in range(args.warmup):
+        launch_step()
         launch()
     torch.cuda.synchronize()
     if exattn.check_device_error() != 0:
@@ -772,28 +781,39 @@ def main() -> None:
     props = torch.cuda.get_device_properties(dev)
     sampler = ClockSampler(getattr(props, "uuid", None) and f"GPU-{props.uuid}")
     for _ in range(args.warmup):  # keep the GPU loaded while the sampler starts
-        launch()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+        launch_step()
+    # The timed region: whole steps, an event before and after each (the backward's three launches are
+    # dependent launches that overlap one another's edges, which events between them would prevent).
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
-        evs[i][0].record(stream)
-        launch(evs[i])
+        step_ev[i][0].record(stream)
+        launch_step()
+        step_ev[i][1].record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if dist:
         dist.barrier()
     if exattn.check_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
+    ms_per_step = statistics.mean(a.elapsed_time(b) for a, b in step_ev)
+    ms_per_step = max_over_ranks(ms_per_step, dist, dev)
+    # Per-kernel times, right after: the same steps with an event after every kernel.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record(stream)
+        launch(evs[i])
+    torch.cuda.synchronize()
+    if exattn.check_device_error() != 0:
+        raise RuntimeError("device error word set during the per-kernel pass")
     per = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)] for i in range(args.steps)]
-    step_ms = [sum(p) for p in per]
-    ms_per_step = statistics.mean(step_ms)
     kern_ms = {name: statistics.mean(p[j] for p in per)
                for j, name in enumerate(("fwd", "bwd_preprocess", "bwd_kv_blocks", "bwd_dq_convert"))}
-    ms_per_step = max_over_ranks(ms_per_step, dist, dev)
 
     # end to end through the C ABI: pinned host inputs -> device -> fwd + bwd -> host outputs
     hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "do"))
@@ -837,7 +857,10 @@ def main() -> None:
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "fp16",
         "data": "synthetic: seeded normal Q,K (sigma %.2g), V, dO (sigma 1)" % w.sigma_qk,
         "config": config_dict(w, {"parallelism": "replicas" if world > 1 else "single GPU",
-                                  "l2": "256 MiB flush write between timed steps, outside the CUDA events"}),
+                                  "l2": "256 MiB flush write between timed steps, outside the CUDA events",
+                                  "timing": "ms_per_step: CUDA events around each whole step (forward call, "
+                                            "backward call); kernels_ms: a second pass of the same steps with "
+                                            "an event after every kernel"}),
         "pct_of_peak": 100.0 * (flops / (ms_per_step * 1e-3) / 1e12) / pk["bf16_tflops"],
         "peak_tflops": pk["bf16_tflops"], "peak_source": pk["source"],
         "kernels_ms": kern_ms,

@@ -195,6 +195,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   const uint32_t tmem = *tmem_slot;
   const uint32_t tX = tmem, tY = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
 
+  // This kernel may start while the preprocess kernel finishes (dependent launch): K and V are not
+  // written by it, so their loads go first; everything else waits for it (LSE2, D, the zeroed
+  // accumulator, and through it every earlier kernel).
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n > 0) {
@@ -205,6 +208,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         tma_load_4d(sK + c * kChunkBytes, &a.tm_k, c * 64, k0, head, batch, bars.kv_full());
         tma_load_4d(sV + c * kChunkBytes, &a.tm_v, c * 64, k0, head, batch, bars.kv_full());
       }
+    }
+    griddep_wait();
+    griddep_launch_dependents();
+    if (lane == 0 && n > 0) {
       int issued = 0, issued_rowv = 0;
       for (int L = 0; L < 2 * n; ++L) {
         const int s = L % NR;
@@ -235,6 +242,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    griddep_wait();
     if (lane == 0 && n > 0) {
       constexpr uint32_t idS = idesc_f16(128, 128, BF16, false, false);   // K-major x K-major
       constexpr uint32_t idG = idesc_f16(128, D, BF16, false, true);      // dV, dK: A (TMEM) K-major, B MN-major
@@ -336,6 +344,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     }
   } else {
     // ------------------------------------------------------------ compute
+    griddep_wait();
     const int h = warp >> 2;             // query half: columns [64h, 64h + 64)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;   // TMEM lane: key row of S^T/dP^T; d (d = 128) or query row of dQ
@@ -586,6 +595,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
 // TPR threads per row, 8 elements (16 bytes) per thread.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ BwdArgs a) {
+  // O, dO and LSE may come from the kernels just before; the workspace may still be read by the
+  // previous backward's kernels.  Only after they are done may the main kernel start (its prologue
+  // then overlaps this kernel's tail).
+  griddep_wait();
+  griddep_launch_dependents();
   constexpr int TPR = D / 8;
   constexpr int RPB = 256 / TPR;
   const size_t row = static_cast<size_t>(blockIdx.x) * RPB + threadIdx.x / TPR;
@@ -631,6 +645,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
 // dQ = scale * dQacc, rounded to the input dtype; 8 elements per thread.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const __grid_constant__ BwdArgs a) {
+  griddep_wait();  // the accumulator is complete once the main kernel has finished
   const size_t e = (static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x) * 8;
   const size_t total = static_cast<size_t>(a.bh_count) * a.Nq * D;
   if (e >= total) return;
@@ -650,15 +665,33 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const __grid_consta
   *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + dst) = out;
 }
 
-// steps: bit 0 = preprocess, bit 1 = main, bit 2 = dQ conversion (launched in that order).
+// Launches `kern` with programmatic stream serialisation: it may start before the previous kernel on
+// the stream has finished, and waits for it with griddep_wait where it must.
+template <typename Kern>
+cudaError_t launch_dependent(Kern kern, dim3 grid, int threads, uint32_t smem, cudaStream_t stream, const BwdArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// steps: bit 0 = preprocess, bit 1 = main, bit 2 = dQ conversion (launched in that order, each as a
+// dependent launch).
 template <int D, bool CAUSAL, bool BF16>
 cudaError_t launch_bwd_t(const BwdArgs& a, int steps, cudaStream_t stream) {
   using C = BwdCfg<D>;
   if (steps & kBwdPre) {
     constexpr int RPB = 256 / (D / 8);
     const size_t rows = static_cast<size_t>(a.bh_count) * a.Nq_pad;
-    bwd_pre_kernel<D, BF16><<<static_cast<unsigned>((rows + RPB - 1) / RPB), 256, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dependent(bwd_pre_kernel<D, BF16>, dim3(static_cast<unsigned>((rows + RPB - 1) / RPB)), 256, 0,
+                                     stream, a);
     if (e != cudaSuccess) return e;
   }
   if (steps & kBwdMain) {
@@ -667,14 +700,13 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int steps, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     const unsigned blocks = static_cast<unsigned>(a.bh_count) * ((a.Nk + kTileRows - 1) / kTileRows);
-    kern<<<blocks, kBwdThreads, C::SMEM_ALLOC, stream>>>(a);
-    e = cudaGetLastError();
+    e = launch_dependent(kern, dim3(blocks), kBwdThreads, C::SMEM_ALLOC, stream, a);
     if (e != cudaSuccess) return e;
   }
   if ((steps & kBwdConvert) && a.dq_acc) {
     const size_t total = static_cast<size_t>(a.bh_count) * a.Nq * D / 8;
-    bwd_dq_convert_kernel<D, BF16><<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dependent(bwd_dq_convert_kernel<D, BF16>, dim3(static_cast<unsigned>((total + 255) / 256)), 256, 0,
+                                     stream, a);
     if (e != cudaSuccess) return e;
   }
   if (steps & kBwdDq) return launch_bwd_dq(a, stream);

@@ -90,6 +90,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_MISC + 4);
   const WaitCtx wc{abort_flag, a.err_word, a.timeout_ns};
 
+  // A dependent launch after this kernel (the backward's preprocess) may start once every CTA is
+  // running; it waits for this kernel to finish before it reads anything.
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
   const int head = bh % a.heads, batch = bh / a.heads;

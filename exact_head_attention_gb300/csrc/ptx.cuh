@@ -355,6 +355,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+// ------------------------------------------------------- dependent launch
+//
+// Programmatic dependent launch (sm_90 and later).  A kernel launched with programmatic stream
+// serialisation may start before the previous kernel on its stream has finished; griddep_wait blocks
+// until that kernel has completed and its memory operations are visible, so a dependent kernel calls it
+// before it touches anything an earlier kernel may still write.  griddep_launch_dependents lets the next
+// such kernel start once every CTA of this one has called it (or exited).  Both are no-ops for a kernel
+// launched without the attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------- descriptors
 //
 // Shared-memory matrix descriptor (tcgen05): start address >> 4 in bits
