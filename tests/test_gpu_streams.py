@@ -177,3 +177,69 @@ def test_pipelined_steps_over_three_streams():
         _step(w, d, b, torch.cuda.current_stream())
         torch.cuda.synchronize()
         _assert_same({n: t.to(DEV) for n, t in host_out[i].items()}, _snapshot(b), f"step {i}")
+
+
+def _atomic_bwd(w, d, b, stream):
+    s = exattn.bwd_raw(d["q"], d["k"], d["v"], b["o"], d["do"], b["lse"], b["dq"], b["dk"], b["dv"], w.causal,
+                       w.scale, b["ws"], stream=stream)
+    assert s == 0, exattn.last_error()
+
+
+def _close_dq(got, want, what):
+    err = (got.double() - want.double()).norm() / want.double().norm().clamp_min(1e-30)
+    assert err < 1e-4, f"{what}: dQ rel-L2 {float(err):.2e}"
+
+
+@pytest.mark.parametrize("shape", [(1, 4, 1024, 1024, 128, "bf16", True), (2, 2, 700, 500, 64, "fp16", False)],
+                         ids=str)
+def test_back_to_back_backwards_share_one_workspace(shape):
+    """The backward's three kernels are dependent launches: the next call's preprocess zeroes the shared
+    workspace only after the previous call's conversion has read it.  Two backward calls queued back to
+    back on one stream with one workspace must give what each gives alone (dK, dV bitwise; dQ within
+    fp32 summation order)."""
+    stream = torch.cuda.current_stream()
+    probs = [_inputs(shape, 80 + i) for i in range(2)]
+    bufs = [_buffers(d) for _, d, _ in probs]
+    alone = []
+    for (w, d, _), b in zip(probs, bufs):
+        assert exattn.fwd_raw(d["q"], d["k"], d["v"], b["o"], b["lse"], w.causal, w.scale, stream=stream) == 0
+        _atomic_bwd(w, d, b, stream)
+        torch.cuda.synchronize()
+        alone.append(_snapshot(b))
+    shared = bufs[0]["ws"]
+    for b in bufs:
+        b["ws"] = shared
+        for n in ("dq", "dk", "dv"):
+            b[n].zero_()
+    for (w, d, _), b in zip(probs, bufs):
+        _atomic_bwd(w, d, b, stream)
+    torch.cuda.synchronize()
+    assert exattn.check_device_error() == 0
+    for i, b in enumerate(bufs):
+        assert torch.equal(b["dk"], alone[i]["dk"]) and torch.equal(b["dv"], alone[i]["dv"]), f"call {i}"
+        _close_dq(b["dq"], alone[i]["dq"], f"call {i}")
+
+
+def test_input_written_by_the_kernel_just_before_the_backward():
+    """dO written on the stream by a device copy right before the backward call: the preprocess and the
+    main kernel (dependent launches) must see the new values, not the old ones."""
+    shape = (1, 4, 1024, 1024, 128, "bf16", True)
+    stream = torch.cuda.current_stream()
+    w, d, _ = _inputs(shape, 90)
+    _, d2, _ = _inputs(shape, 91)
+    b = _buffers(d)
+    assert exattn.fwd_raw(d["q"], d["k"], d["v"], b["o"], b["lse"], w.causal, w.scale, stream=stream) == 0
+    ref = {"do": d2["do"]}
+    ref.update({n: d[n] for n in ("q", "k", "v")})
+    b_ref = _buffers(d)
+    b_ref["o"].copy_(b["o"])
+    b_ref["lse"].copy_(b["lse"])
+    _atomic_bwd(w, ref, b_ref, stream)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        d["do"].copy_(d2["do"].flip(-1))  # something else first
+        d["do"].copy_(d2["do"])           # the values the backward must read, written just before it
+        _atomic_bwd(w, d, b, stream)
+        torch.cuda.synchronize()
+        assert torch.equal(b["dk"], b_ref["dk"]) and torch.equal(b["dv"], b_ref["dv"])
+        _close_dq(b["dq"], b_ref["dq"], "dQ")
