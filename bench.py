@@ -301,8 +301,9 @@ def pipelined_e2e(steps: int, slots: list, h2d, compute, d2h, flush) -> tuple[fl
 
 
 E2E_NOTE = ("pipelined over steps on three CUDA streams (copy-in, compute, copy-out) with two device buffer sets; "
-            "no L2 flush (each step's inputs arrive by host-to-device copy); alone_ms_per_step: one step by itself "
-            "on one stream after an L2 flush")
+            "the timed region runs from the first step's copy-in to the last step's copy-out, so filling and "
+            "draining the pipeline are included; no L2 flush (each step's inputs arrive by host-to-device copy); "
+            "alone_ms_per_step: one step by itself on one stream after an L2 flush")
 
 
 # ------------------------------------------------------------------ main
@@ -704,7 +705,7 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=None)
-    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--kl-dq-mode", choices=("atomic", "deterministic"), default="atomic",
                     help="attention-KL workloads: the one-pass backward (atomic dQ) or the repeatable two-kernel one")
