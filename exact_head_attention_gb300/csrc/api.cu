@@ -188,14 +188,18 @@ int causal_offset(int causal, int Nq, int Nk) { return causal == ATTN_MASK_CAUSA
 // mask the first key block of a head is the heaviest (it sees every query tile), and a group's first
 // blocks start only when that group does; a group of at least 2 * SMs / nkb heads has enough lighter
 // blocks to run beside them.
-int head_group(bool causal, long long bh, int Nk, size_t acc_per_head, const DeviceState* ds) {
-  if (static_cast<size_t>(bh) * acc_per_head <= (causal ? ds->l2_bytes / 2 : ds->l2_bytes / 4)) return static_cast<int>(bh);
-  long long g = std::max<long long>(1, static_cast<long long>(ds->l2_bytes / 16 / acc_per_head));
+int head_group_for(bool causal, long long bh, int Nk, size_t acc_per_head, size_t l2_bytes, int sm_count) {
+  if (static_cast<size_t>(bh) * acc_per_head <= (causal ? l2_bytes / 2 : l2_bytes / 4)) return static_cast<int>(bh);
+  long long g = std::max<long long>(1, static_cast<long long>(l2_bytes / 16 / acc_per_head));
   if (causal) {
     const long long nkb = (Nk + kTileRows - 1) / kTileRows;
-    g = std::max(g, (2LL * ds->sm_count + nkb - 1) / nkb);
+    g = std::max(g, (2LL * sm_count + nkb - 1) / nkb);
   }
   return static_cast<int>(std::min(g, bh));
+}
+
+int head_group(bool causal, long long bh, int Nk, size_t acc_per_head, const DeviceState* ds) {
+  return head_group_for(causal, bh, Nk, acc_per_head, ds->l2_bytes, ds->sm_count);
 }
 
 attn_status finish(cudaError_t e, cudaStream_t stream) {
@@ -283,6 +287,21 @@ extern "C" size_t attn_bwd_workspace_size(int B, int H, int Nq, int d) {
 // (head_group) sees to that: a head's blocks run close together whenever the accumulator as a whole
 // would not stay in L2.  The reductions then measured faster than the query-tile kernel on every
 // shape tried, by 1.3x to 1.6x, so the rule takes them for every shape; the mask is not needed.
+extern "C" int attn_bwd_head_group(int B, int H, int Nq, int Nk, int d, int causal, int sm_count, size_t l2_bytes) {
+  if (check_common(B, H, Nq, Nk, d, causal, 1.0f, ATTN_BF16) != ATTN_OK) return -1;
+  if (sm_count <= 0 || l2_bytes == 0) {
+    int dev = 0, sms = 0, l2 = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+      return -1;
+    if (sm_count <= 0) sm_count = sms;
+    if (l2_bytes == 0) l2_bytes = static_cast<size_t>(l2);
+  }
+  const size_t acc_per_head = static_cast<size_t>(padded_rows(Nq)) * d * sizeof(float);
+  return head_group_for(causal != ATTN_MASK_NONE, static_cast<long long>(B) * H, Nk, acc_per_head, l2_bytes, sm_count);
+}
+
 extern "C" int attn_bwd_auto_dq_mode(int B, int H, int Nq, int Nk, int d, int /*causal*/) {
   if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return -1;
   return ATTN_DQ_ATOMIC;

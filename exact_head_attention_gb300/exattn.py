@@ -95,6 +95,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_kl_fwd_splitkv.restype = i
             lib.attn_kl_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i, i]
             lib.attn_kl_fwd_splitkv_workspace_size.restype = sz
+            lib.attn_bwd_head_group.argtypes = [i, i, i, i, i, i, i, sz]
+            lib.attn_bwd_head_group.restype = i
             lib.attn_bwd_auto_dq_mode.argtypes = [i, i, i, i, i, i]
             lib.attn_bwd_auto_dq_mode.restype = i
             lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
@@ -266,6 +268,15 @@ def bwd_strided_raw(q, k, v, o, do, lse, dq, dk, dv, causal, scale: float, works
     return load().attn_bwd_strided(*_view(q), *_view(k), *_view(v), *_view(o), *_view(do), _ptr(lse),
                                    *_view(dq), *_view(dk), *_view(dv), B, H, Nq, Nk, d, mask_code(causal),
                                    float(scale), _dtype_code(q), *_workspace(workspace), _stream(stream))
+
+
+def head_group(B: int, H: int, Nq: int, Nk: int, d: int, causal=False, sm_count: int = 0, l2_bytes: int = 0) -> int:
+    """Heads per launch group of the reducing backward (attn_bwd_head_group); sm_count / l2_bytes 0 take
+    the current device's values."""
+    g = int(load().attn_bwd_head_group(B, H, Nq, Nk, d, mask_code(causal), sm_count, l2_bytes))
+    if g < 0:
+        raise ValueError("invalid sizes")
+    return g
 
 
 def auto_dq_mode(B: int, H: int, Nq: int, Nk: int, d: int, causal=False) -> str:

@@ -336,6 +336,22 @@ typedef enum {
 } attn_dq_mode;
 
 /*
+ * Heads per launch group of the key/value-block kernels when dQ is reduced
+ * into the fp32 accumulator (ATTN_DQ_ATOMIC, and the one-pass KL backward).
+ * The blocks (one per head and 128-row key block) are numbered in groups of
+ * this many heads, heads fastest within a group, the last group also taking
+ * the B*H mod G heads left over.  G = B*H (plain heads-fastest order) while
+ * the accumulator, B*H*ceil(Nq/128)*128*d*4 bytes, is at most a quarter of
+ * l2_bytes with no mask, or half of it under a causal mask.  Otherwise G is
+ * the number of heads whose accumulator rows fit in l2_bytes/16 (at least
+ * 1); under a causal mask it is at least ceil(2*sm_count / ceil(Nk/128)); and
+ * it is at most B*H.  sm_count <= 0 or l2_bytes = 0 take the current
+ * device's values.  Returns -1 for sizes the backward rejects, or when a
+ * device value is needed and cannot be read.
+ */
+int attn_bwd_head_group(int B, int H, int Nq, int Nk, int d, int causal, int sm_count, size_t l2_bytes);
+
+/*
  * The mode ATTN_DQ_AUTO resolves to for a backward of this shape (causal: an
  * attn_mask value): ATTN_DQ_ATOMIC.  On GB300 the reductions measured 1.3x to
  * 1.6x faster than the query-tile kernel on every shape tried (20 shapes with

@@ -105,6 +105,8 @@ def test_atomic_matches_deterministic_in_both_launch_orders(shape):
     agrees within fp32 summation order; "auto" resolves to the reductions."""
     B, H, N, d, causal = shape
     assert exattn.auto_dq_mode(B, H, N, N, d, causal) == "atomic"
+    want_g = {(16, 16, 2048, 128, False): 8, (1, 4, 2048, 128, True): 4, (4, 16, 8192, 128, True): 5}[shape]
+    assert exattn.head_group(B, H, N, N, d, causal) == want_g  # this device's SM count and L2 size
     dev = torch.device("cuda")
     g = torch.Generator(device=dev)
     g.manual_seed(B * H + N)
