@@ -29,10 +29,14 @@
  * Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  * stream) and allocate no device memory.  Arguments are validated before any
  * launch; on an error status nothing is launched and no output is written.
- * Every device-side wait is bounded: if one expires the kernel records
- * ATTN_ERR_TIMEOUT in a per-device error word and exits; attn_check_device_error
- * (or EXATTN_CHECKED=1 in the environment, which synchronises after each call)
- * reports it.
+ * The backward's kernels are dependent launches (programmatic stream
+ * serialisation): each may start before the work ahead of it on the stream
+ * has finished, but waits for that work before it reads or writes anything
+ * the work could touch, so stream order holds as for ordinary launches.
+ * Every wait between warp roles (an mbarrier) is bounded: if one expires the
+ * kernel records ATTN_ERR_TIMEOUT in a per-device error word and exits;
+ * attn_check_device_error (or EXATTN_CHECKED=1 in the environment, which
+ * synchronises after each call) reports it.
  */
 #ifndef EXATTN_H
 #define EXATTN_H
