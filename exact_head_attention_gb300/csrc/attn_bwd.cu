@@ -79,9 +79,9 @@ struct BwdCfg {
   static constexpr uint32_t OFF_ROWV = OFF_STAGE + STAGE_BYTES;
   static constexpr uint32_t ROWV_BYTES = 2 * 128 * 4;
   static constexpr uint32_t OFF_BAR = OFF_ROWV + 2 * ROWV_BYTES;
-  // kv_full, ring_full[NR], ring_empty[NR], s_full, s_used, dp_full, pd_ready, ds_empty,
-  // dq_full, dq_empty, done, mma_done, rowv_full[2], rowv_empty[2], dss_ready, dstile_free, p_ready
-  static constexpr int NBAR = 1 + 2 * NR + 16;
+  // kv_full, ring_full[NR], ring_empty[NR], s_full, s_used, dp_full, pd_ready, p_ready,
+  // dq_full, dq_empty, done, mma_done, rowv_full[2], rowv_empty[2], dss_ready, dstile_free
+  static constexpr int NBAR = 1 + 2 * NR + 15;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   // The operand tiles need 1024-byte alignment; the dynamic shared memory base is checked at entry
@@ -104,8 +104,9 @@ struct BwdBars {
   __device__ uint32_t dss_ready() const { return at(13); } // dS^T in shared memory
   // d = 128: the copy engine has read warpgroup 1's dQ rows out of the dS^T tile
   __device__ uint32_t dstile_free() const { return at(14); }
-  __device__ uint32_t p_ready() const { return at(15); }   // P^T packed in TMEM X (dV may go)
-  __device__ uint32_t ds_empty() const { return at(4); }
+  __device__ uint32_t p_ready() const { return at(4); }    // P^T packed in TMEM Y (dV may go)
+  // the dQ MMA has read the dS^T tile: the same completion as dq_full, which one commit marks
+  __device__ uint32_t ds_empty() const { return dq_full(); }
   __device__ uint32_t dq_full() const { return at(5); }
   __device__ uint32_t dq_empty() const { return at(6); }
   __device__ uint32_t done() const { return at(7); }
@@ -174,7 +175,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     mbar_init(bars.p_ready(), 256);
     mbar_init(bars.dss_ready(), 256);
     mbar_init(bars.dstile_free(), 1);
-    mbar_init(bars.ds_empty(), 1);
     mbar_init(bars.dq_full(), 1);
     mbar_init(bars.dq_empty(), 256);
     mbar_init(bars.done(), 1);
@@ -334,8 +334,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
 #pragma unroll
           for (int k = 1; k < 128 / 16; ++k) mma_ss_lo<true>(tY, ds_mn + k * (2048 >> 4), k_mn + k * (2048 >> 4), idQ);
         }
-        mma_commit(bars.dq_full());
-        mma_commit(bars.ds_empty());
+        mma_commit(bars.dq_full());  // also frees the dS^T tile (ds_empty)
         if (it + 1 < n && !(ok = issue_dP(it + 1))) break;
       }
       if (ok) mma_commit(bars.done());

@@ -72,9 +72,9 @@ struct KlBwdCfg {
   static constexpr uint32_t OFF_ROWV = OFF_STAGE + STAGE_BYTES;
   static constexpr uint32_t ROWV_BYTES = 3 * 64 * 4;
   static constexpr uint32_t OFF_BAR = OFF_ROWV + 2 * ROWV_BYTES;
-  // kv_full, ring_full[NR], ring_empty[NR], s_full, s_used, pd_ready, dss_ready, ds_empty, dq_full,
-  // dq_empty, dstile_free, done, mma_done
-  static constexpr int NBAR = 1 + 2 * NR + 10;
+  // kv_full, ring_full[NR], ring_empty[NR], s_full, s_used, pd_ready, dss_ready, mma_done, dq_full,
+  // dq_empty, dstile_free, done
+  static constexpr int NBAR = 1 + 2 * NR + 9;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   static_assert(BYTES <= 232448, "shared memory budget");
@@ -91,12 +91,13 @@ struct KlBwdBars {
   __device__ uint32_t s_used() const { return at(1); }       // both read into registers
   __device__ uint32_t pd_ready() const { return at(2); }     // dS^T packed in TMEM (dK may go)
   __device__ uint32_t dss_ready() const { return at(3); }    // dS^T in shared memory (dQ may go)
-  __device__ uint32_t ds_empty() const { return at(4); }     // dQ MMA has read the dS^T tile
+  // the dQ MMA has read the dS^T tile: the same completion as dq_full, which one commit marks
+  __device__ uint32_t ds_empty() const { return dq_full(); }
   __device__ uint32_t dq_full() const { return at(5); }
   __device__ uint32_t dq_empty() const { return at(6); }
   __device__ uint32_t dstile_free() const { return at(7); }  // d = 128: WG1's staged dQ rows read
   __device__ uint32_t done() const { return at(8); }
-  __device__ uint32_t mma_done() const { return at(9); }
+  __device__ uint32_t mma_done() const { return at(4); }
 };
 
 // TMEM column (from the allocation's base) where warpgroup h stores its packed dS^T half on tile
@@ -194,7 +195,6 @@ __global__ void __launch_bounds__(kKlBwdThreads, 1) kl_bwd_fused_kernel(const __
     mbar_init(bars.s_used(), 256);
     mbar_init(bars.pd_ready(), 256);
     mbar_init(bars.dss_ready(), 256);
-    mbar_init(bars.ds_empty(), 1);
     mbar_init(bars.dq_full(), 1);
     mbar_init(bars.dq_empty(), 256);
     mbar_init(bars.dstile_free(), 1);
@@ -304,8 +304,7 @@ __global__ void __launch_bounds__(kKlBwdThreads, 1) kl_bwd_fused_kernel(const __
 #pragma unroll
           for (int k = 1; k < 128 / 16; ++k) mma_ss_lo<true>(tY, ds_mn + k * (2048 >> 4), kt_mn + k * (2048 >> 4), idQ);
         }
-        mma_commit(bars.dq_full());
-        mma_commit(bars.ds_empty());
+        mma_commit(bars.dq_full());  // also frees the dS^T tile (ds_empty)
       }
       if (ok) mma_commit(bars.done());
       mma_commit(bars.mma_done());
