@@ -783,9 +783,12 @@ def main() -> None:
     sampler = ClockSampler(getattr(props, "uuid", None) and f"GPU-{props.uuid}")
     for _ in range(args.warmup):  # keep the GPU loaded while the sampler starts
         launch_step()
-    # The timed region: whole steps, an event before and after each (the backward's three launches are
-    # dependent launches that overlap one another's edges, which events between them would prevent).
+    # The timed region, two passes of K steps each.  Pass 1: whole steps, an event before and after each
+    # (the backward's three launches are dependent launches that overlap one another's edges, which
+    # events between them would prevent); it gives ms_per_step.  Pass 2: the same steps with an event
+    # after every kernel; it gives the per-kernel times, and so the roofline's kernel duration.
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -795,6 +798,10 @@ def main() -> None:
         step_ev[i][0].record(stream)
         launch_step()
         step_ev[i][1].record(stream)
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record(stream)
+        launch(evs[i])
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if dist:
@@ -803,15 +810,6 @@ def main() -> None:
         raise RuntimeError("device error word set during the timed region")
     ms_per_step = statistics.mean(a.elapsed_time(b) for a, b in step_ev)
     ms_per_step = max_over_ranks(ms_per_step, dist, dev)
-    # Per-kernel times, right after: the same steps with an event after every kernel.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
-        evs[i][0].record(stream)
-        launch(evs[i])
-    torch.cuda.synchronize()
-    if exattn.check_device_error() != 0:
-        raise RuntimeError("device error word set during the per-kernel pass")
     per = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)] for i in range(args.steps)]
     kern_ms = {name: statistics.mean(p[j] for p in per)
                for j, name in enumerate(("fwd", "bwd_preprocess", "bwd_kv_blocks", "bwd_dq_convert"))}
@@ -859,9 +857,9 @@ def main() -> None:
         "data": "synthetic: seeded normal Q,K (sigma %.2g), V, dO (sigma 1)" % w.sigma_qk,
         "config": config_dict(w, {"parallelism": "replicas" if world > 1 else "single GPU",
                                   "l2": "256 MiB flush write between timed steps, outside the CUDA events",
-                                  "timing": "ms_per_step: CUDA events around each whole step (forward call, "
-                                            "backward call); kernels_ms: a second pass of the same steps with "
-                                            "an event after every kernel"}),
+                                  "timing": "timed region = two passes of the steps: ms_per_step from CUDA "
+                                            "events around each whole step (forward call, backward call); "
+                                            "kernels_ms from the second pass, with an event after every kernel"}),
         "pct_of_peak": 100.0 * (flops / (ms_per_step * 1e-3) / 1e12) / pk["bf16_tflops"],
         "peak_tflops": pk["bf16_tflops"], "peak_source": pk["source"],
         "kernels_ms": kern_ms,
@@ -882,7 +880,7 @@ def main() -> None:
         "e2e": ({"value": job_throughput(flops, world, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                  "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "alone_ms_per_step": alone_ms,
                  "timing": E2E_NOTE} if args.e2e_steps else None),
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 2 * 4 * args.steps,  # both passes of the timed region
         "clocks": sampler.summary(t_wall0, t_wall1),
         "wall_s_timed_region": t_wall1 - t_wall0,
     }
