@@ -281,12 +281,7 @@ extern "C" size_t attn_bwd_workspace_size(int B, int H, int Nq, int d) {
   return align256(rows * d * sizeof(float)) + 2 * align256(rows * sizeof(float));
 }
 
-// ATTN_DQ_AUTO.  The StreamKL summary (backward, kernel fusion) adds dQ atomically while the buffer fits
-// in L2 and uses separate kernels when contention grows.  What decides on GB300 is whether the key
-// blocks that add into the same head's rows find them still in L2, and the launch order
-// (head_group) sees to that: a head's blocks run close together whenever the accumulator as a whole
-// would not stay in L2.  The reductions then measured faster than the query-tile kernel on every
-// shape tried, by 1.3x to 1.6x, so the rule takes them for every shape; the mask is not needed.
+// The launch grouping head_group picks, for callers and tests (sm_count / l2_bytes 0: this device's).
 extern "C" int attn_bwd_head_group(int B, int H, int Nq, int Nk, int d, int causal, int sm_count, size_t l2_bytes) {
   if (check_common(B, H, Nq, Nk, d, causal, 1.0f, ATTN_BF16) != ATTN_OK) return -1;
   if (sm_count <= 0 || l2_bytes == 0) {
@@ -302,6 +297,12 @@ extern "C" int attn_bwd_head_group(int B, int H, int Nq, int Nk, int d, int caus
   return head_group_for(causal != ATTN_MASK_NONE, static_cast<long long>(B) * H, Nk, acc_per_head, l2_bytes, sm_count);
 }
 
+// ATTN_DQ_AUTO.  The StreamKL summary (backward, kernel fusion) adds dQ atomically while the buffer fits
+// in L2 and uses separate kernels when contention grows.  What decides on GB300 is whether the key
+// blocks that add into the same head's rows find them still in L2, and the launch order
+// (head_group) sees to that: a head's blocks run close together whenever the accumulator as a whole
+// would not stay in L2.  The reductions then measured faster than the query-tile kernel on every
+// shape tried, by 1.3x to 1.6x, so the rule takes them for every shape; the mask is not needed.
 extern "C" int attn_bwd_auto_dq_mode(int B, int H, int Nq, int Nk, int d, int /*causal*/) {
   if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return -1;
   return ATTN_DQ_ATOMIC;
