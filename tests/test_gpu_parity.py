@@ -131,6 +131,23 @@ def test_many_heads_causal_accumulator_beyond_l2_sampled():
     _check_invariants(w, x, got, w.name)
 
 
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "nomask"])
+def test_more_heads_than_a_grid_y_dimension(causal):
+    """B*H = 66000 heads of 8 rows: more than the 65535 a grid's y dimension allows, so the key/value
+    blocks' one-dimensional numbering (and its head groups: the 2 GiB accumulator is far past L2) is what
+    reaches every head; the first, a middle and the last heads against the oracle, every head finite."""
+    w = workloads.custom(1100, 60, 8, 8, 64, "bf16", causal, index=34)
+    x = workloads.make_inputs(w)
+    got = run_gpu(w, x)
+    heads = [(0, 0), (550, 31), (1099, 59)]
+    ref = oracle_heads(w, x, heads)
+    sel = lambda a: np.stack([a[b, h] for b, h in heads])  # noqa: E731
+    check_fwd(w, sel(got["o"]), sel(got["lse"]), ref["o"], ref["lse"], w.name)
+    check_grads({k: sel(got[k]) for k in ("dq", "dk", "dv")}, ref, w.name)
+    for k in ("o", "dq", "dk", "dv"):
+        assert np.isfinite(got[k]).all(), k
+
+
 @pytest.mark.parametrize("shape", [(1, 1, 200003, 200003, 64, "bf16", True),
                                    (1, 1, 100001, 131075, 128, "bf16", "bottom_right")],
                          ids=["q200003_d64_causal", "q100001_k131075_d128_bottom_right"])
