@@ -232,6 +232,7 @@ attn_status fwd_impl(const void* Q, const RowStrides& qs, const void* K, const R
     return driver_fail("cuTensorMapEncodeTiled", r);
   a.lse = LSE;
   a.err_word = ds->err_word;
+  a.sm_count = ds->sm_count;
   a.bh_count = B * H;
   a.heads = H;
   a.Nq = Nq;

@@ -32,6 +32,12 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "softmax.cuh"
@@ -76,8 +82,124 @@ struct FwdBars {
   __device__ uint32_t mma_done() const { return base + 8 * (7 + 4 * ns); }
 };
 
-template <int D, bool CAUSAL, bool BF16>
-__global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdArgs a) {
+// ------------------------------------------------------------ persistent schedule
+//
+// Under a causal mask a 256-row query block's work grows with its position, from one key tile to the
+// whole row.  With one CTA per block the hardware hands blocks to SMs heaviest first, which leaves
+// about a tenth of the SMs' time idle at the end of the 8k workload (the blocks are few and coarse
+// against the SM count).  The persistent launch instead runs one CTA per SM over a list of blocks that
+// the host packs: longest first onto the least loaded CTA, then moves and swaps that lower the most
+// loaded CTA's total.  A block's cost is the key tiles its two query tiles visit plus a fixed part for
+// its start and its epilogue.
+constexpr int kPersistMaxCtas = 160;
+constexpr int kPersistMaxUnits = 2048;
+constexpr int kUnitFixedCost = 2;    // in key-tile visits
+constexpr int kPersistBlockCost = 2;  // extra per block on a list: the CTA-wide hand-over between blocks
+
+struct FwdSchedule {
+  int ctas;
+  uint16_t begin[kPersistMaxCtas + 1];  // CTA i runs unit[begin[i] .. begin[i + 1])
+  uint32_t unit[kPersistMaxUnits];      // bh * nqb + qb
+};
+
+// The packed schedule for this launch, or nullptr when a plain launch is as good (one wave or less) or
+// the blocks do not fit the schedule's capacity.  Schedules are cached per shape.
+const FwdSchedule* persistent_schedule(const FwdArgs& a, int nqb) {
+  const long long units = static_cast<long long>(a.bh_count) * nqb;
+  const int ctas = std::min(a.sm_count, kPersistMaxCtas);
+  if (ctas <= 0 || units <= ctas || units > kPersistMaxUnits) return nullptr;
+  using Key = std::tuple<int, int, int, int, int, int>;
+  static std::mutex mu;
+  static std::map<Key, FwdSchedule> cache;
+  const Key key{a.bh_count, nqb, a.Nq, a.Nk, a.causal_off, ctas};
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second.ctas > 0 ? &it->second : nullptr;
+  if (cache.size() >= 64) cache.clear();
+
+  const int nkv = (a.Nk + kTileRows - 1) / kTileRows;
+  auto tiles = [&](int qb, int t) {
+    const int last_key = qb * kFwdSubTiles * kTileRows + t * kTileRows + kTileRows - 1 + a.causal_off;
+    return last_key < 0 ? 0 : std::min(nkv, last_key / kTileRows + 1);
+  };
+  std::vector<int> qcost(nqb);
+  for (int qb = 0; qb < nqb; ++qb) qcost[qb] = tiles(qb, 0) + tiles(qb, 1) + kUnitFixedCost;
+  std::vector<uint32_t> order(static_cast<size_t>(units));
+  for (uint32_t u = 0; u < order.size(); ++u) order[u] = u;
+  auto cost = [&](uint32_t u) { return qcost[u % nqb]; };
+  std::stable_sort(order.begin(), order.end(), [&](uint32_t x, uint32_t y) { return cost(x) > cost(y); });
+  std::vector<std::vector<uint32_t>> bins(ctas);
+  std::vector<long long> load(ctas, 0);
+  for (uint32_t u : order) {  // longest first onto the least loaded CTA
+    const int b = static_cast<int>(std::min_element(load.begin(), load.end()) - load.begin());
+    bins[b].push_back(u);
+    load[b] += cost(u);
+  }
+  const long long lpt_max = *std::max_element(load.begin(), load.end());  // about what a plain launch gets
+  // Improve: move a block off the most loaded CTA, or swap it for a lighter one, while that lowers
+  // the larger of the two totals below the current maximum.
+  for (int round = 0; round < 4 * ctas; ++round) {
+    const int hi = static_cast<int>(std::max_element(load.begin(), load.end()) - load.begin());
+    bool improved = false;
+    for (int lo = 0; lo < ctas && !improved; ++lo) {
+      if (lo == hi) continue;
+      for (size_t i = 0; i < bins[hi].size() && !improved; ++i) {
+        const int ca = cost(bins[hi][i]);
+        if (std::max(load[hi] - ca, load[lo] + ca) < load[hi]) {
+          bins[lo].push_back(bins[hi][i]);
+          bins[hi].erase(bins[hi].begin() + static_cast<long>(i));
+          load[hi] -= ca;
+          load[lo] += ca;
+          improved = true;
+          break;
+        }
+        for (size_t j = 0; j < bins[lo].size(); ++j) {
+          const int cb = cost(bins[lo][j]);
+          if (cb >= ca) continue;
+          if (std::max(load[hi] - ca + cb, load[lo] - cb + ca) < load[hi]) {
+            std::swap(bins[hi][i], bins[lo][j]);
+            load[hi] += cb - ca;
+            load[lo] += ca - cb;
+            improved = true;
+            break;
+          }
+        }
+      }
+    }
+    if (!improved) break;
+  }
+  FwdSchedule& sch = cache[key];
+  // A block on a list costs a little more than a block of its own (the hand-over between blocks: two
+  // CTA-wide barriers, the ring drained, the barriers re-armed), and a list mixes heads and positions, so
+  // concurrent blocks share fewer K/V tiles in L2 than the plain launch's order.  Lists are used only
+  // where, with that extra cost, they still shorten the most loaded SM by 3 % or more.  Measured: the 8k
+  // workload's forward 160 -> 154 us packed; 32k ones, already balanced within 2 %, 4-8 % slower packed;
+  // 1k blocks (a few key tiles each) 4 % slower packed.
+  long long packed_max = 0;
+  for (int b = 0; b < ctas; ++b)
+    packed_max = std::max(packed_max, load[b] + kPersistBlockCost * static_cast<long long>(bins[b].size()));
+  if (100 * packed_max > 97 * lpt_max) {
+    sch.ctas = 0;
+    return nullptr;
+  }
+  sch.ctas = ctas;
+  int pos = 0;
+  for (int b = 0; b < ctas; ++b) {
+    std::sort(bins[b].begin(), bins[b].end(), [&](uint32_t x, uint32_t y) { return cost(x) > cost(y); });
+    sch.begin[b] = static_cast<uint16_t>(pos);
+    for (uint32_t u : bins[b]) sch.unit[pos++] = u;
+  }
+  sch.begin[ctas] = static_cast<uint16_t>(pos);
+  return &sch;
+}
+
+// The forward of query blocks units[0 .. nunits) of 256 rows each; unit = bh * nqb + qb.  A plain launch
+// gives each CTA one block; a persistent launch gives each CTA (one per SM) a list that the host packed
+// so that the CTAs' causal work is even.  Between two blocks every role has finished the first (its
+// loads consumed, its MMAs drained, its O stored), and the barriers are re-armed.
+template <int D, bool CAUSAL, bool BF16, bool MULTI>
+__device__ __forceinline__ void fwd_body(const FwdArgs& a, const uint32_t* units, int nunits_arg) {
+  const int nunits = MULTI ? nunits_arg : 1;  // a plain launch compiles without the block loop's machinery
   using C = FwdCfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -94,22 +216,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   // running; it waits for this kernel to finish before it reads anything.
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int head = bh % a.heads, batch = bh / a.heads;
-  const int qb = gridDim.y - 1 - blockIdx.y;  // heaviest (causal) query blocks are scheduled first
-  const int q0 = qb * (kFwdSubTiles * kTileRows);
+  const int nqb = (a.Nq + kFwdSubTiles * kTileRows - 1) / (kFwdSubTiles * kTileRows);
   const int nkv = (a.Nk + kTileRows - 1) / kTileRows;
   const int coff = CAUSAL ? a.causal_off : 0;
-  // key tiles visited by query tile t (causal: through the tile holding the last key its last row sees)
-  auto tiles_of = [&](int t) {
-    if (!CAUSAL) return nkv;
-    const int last_key = q0 + t * kTileRows + kTileRows - 1 + coff;
-    return last_key < 0 ? 0 : min(nkv, last_key / kTileRows + 1);
-  };
-  const int ntile0 = tiles_of(0), ntile1 = tiles_of(1);  // ntile1 >= ntile0
 
-  if (threadIdx.x == 0) {
-    *abort_flag = 0u;
+  auto init_bars = [&] {
     mbar_init(bars.q_full(), 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bars.k_full(s), 1);
@@ -124,6 +235,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     }
     mbar_init(bars.mma_done(), 1);
     fence_mbar_init();
+  };
+  if (threadIdx.x == 0) {
+    *abort_flag = 0u;
+    init_bars();
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -134,171 +249,244 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Start of block ui: after the first, all threads meet (named barrier 3), and unless a wait gave up
+  // in an earlier block (then every thread leaves the loop together) thread 0 re-arms the barriers.
+  auto next_unit = [&](int ui) -> bool {
+    if (!MULTI || ui == 0) return true;
+    tc_fence_before();
+    named_bar_sync(3, kFwdThreads);
+    const bool go = *abort_flag == 0u;
+    if (go && threadIdx.x == 0) {
+      mbar_inval(bars.q_full());
+      for (int s = 0; s < NS; ++s) {
+        mbar_inval(bars.k_full(s));
+        mbar_inval(bars.k_empty(s));
+        mbar_inval(bars.v_full(s));
+        mbar_inval(bars.v_empty(s));
+      }
+      for (int t = 0; t < 2; ++t) {
+        mbar_inval(bars.s_full(t));
+        mbar_inval(bars.p_full(t));
+        mbar_inval(bars.o_full(t));
+      }
+      mbar_inval(bars.mma_done());
+      init_bars();
+    }
+    named_bar_sync(3, kFwdThreads);
+    tc_fence_after();
+    return go;
+  };
+  // the block's coordinates and the key tiles its query tiles visit (causal: through the tile holding
+  // the last key the tile's last row sees)
+  struct Unit {
+    int bh, head, batch, q0, ntile0, ntile1;  // ntile1 >= ntile0
+  };
+  auto unit_of = [&](int ui) {
+    Unit u;
+    int qb;
+    if constexpr (MULTI) {
+      u.bh = static_cast<int>(units[ui]) / nqb;
+      qb = static_cast<int>(units[ui]) % nqb;
+    } else {  // a plain launch: (B*H, blocks) grid, heaviest causal blocks first
+      u.bh = blockIdx.x;
+      qb = gridDim.y - 1 - blockIdx.y;
+    }
+    u.head = u.bh % a.heads;
+    u.batch = u.bh / a.heads;
+    u.q0 = qb * (kFwdSubTiles * kTileRows);
+    auto tiles_of = [&](int t) {
+      if (!CAUSAL) return nkv;
+      const int last_key = u.q0 + t * kTileRows + kTileRows - 1 + coff;
+      return last_key < 0 ? 0 : min(nkv, last_key / kTileRows + 1);
+    };
+    u.ntile0 = tiles_of(0);
+    u.ntile1 = tiles_of(1);
+    return u;
+  };
+
   if (warp >= 8) {
     // ------------------------------------------------------------ control warpgroup
     // warp 8: TMA producer, warp 9: MMA issuer, warps 10-11: idle.
     regs_decrease<kRegsControl>();
-    if (warp == 8 && lane == 0 && ntile1 > 0) {
-      // ---- producer
-      prefetch_tmap(&a.tm_q);
-      prefetch_tmap(&a.tm_k);
-      prefetch_tmap(&a.tm_v);
-      mbar_arrive_expect_tx(bars.q_full(), 2 * C::TILE);
-      for (int t = 0; t < 2; ++t)
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(sQ + t * C::TILE + c * kChunkBytes, &a.tm_q, c * 64, q0 + t * kTileRows, head, batch, bars.q_full());
-      int issued_k = 0, issued_v = 0;
-      for (int j = 0; j < ntile1; ++j) {
-        const int s = j % NS;
-        const uint32_t ph = (j / NS) & 1;
-        if (!mbar_wait(bars.k_empty(s), ph ^ 1, wc)) break;
-        mbar_arrive_expect_tx(bars.k_full(s), C::TILE);
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(sK + s * C::TILE + c * kChunkBytes, &a.tm_k, c * 64, j * kTileRows, head, batch, bars.k_full(s));
-        ++issued_k;
-        if (!mbar_wait(bars.v_empty(s), ph ^ 1, wc)) break;
-        mbar_arrive_expect_tx(bars.v_full(s), C::TILE);
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(sV + s * C::TILE + c * kChunkBytes, &a.tm_v, c * 64, j * kTileRows, head, batch, bars.v_full(s));
-        ++issued_v;
-      }
-      // On abort, every load this thread issued must land before the CTA exits.
-      if (*abort_flag) {
-        for (int j = max(0, issued_k - NS); j < issued_k; ++j) mbar_drain(bars.k_full(j % NS), (j / NS) & 1, a.timeout_ns);
-        for (int j = max(0, issued_v - NS); j < issued_v; ++j) mbar_drain(bars.v_full(j % NS), (j / NS) & 1, a.timeout_ns);
-        mbar_drain(bars.q_full(), 0, a.timeout_ns);
-      }
-    } else if (warp == 9 && lane == 0 && ntile1 > 0) {
-      // ---- MMA issuer
-      constexpr uint32_t idS = idesc_f16(128, 128, BF16, false, false);
-      constexpr uint32_t idPV = idesc_f16(128, D, BF16, false, true);
-      bool ok = mbar_wait(bars.q_full(), 0, wc);
-      // Descriptor low words of the operand bases; a K step adds a constant (the issue loop of a
-      // single thread must keep up with one MMA per 64 tensor-core cycles).
-      constexpr uint32_t kTileLo = C::TILE >> 4;
-      const uint32_t q_lo = sdesc_lo(sQ, 16), k_lo = sdesc_lo(sK, 16), v_lo = sdesc_lo(sV, kChunkBytes);
+    for (int ui = 0; ui < nunits; ++ui) {
+      if (!next_unit(ui)) break;
+      const Unit u = unit_of(ui);
+      const int bh = u.bh, head = u.head, batch = u.batch, q0 = u.q0, ntile0 = u.ntile0, ntile1 = u.ntile1;
+      (void)bh;
+      if (warp == 8 && lane == 0 && ntile1 > 0) {
+        // ---- producer
+        prefetch_tmap(&a.tm_q);
+        prefetch_tmap(&a.tm_k);
+        prefetch_tmap(&a.tm_v);
+        mbar_arrive_expect_tx(bars.q_full(), 2 * C::TILE);
+        for (int t = 0; t < 2; ++t)
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_4d(sQ + t * C::TILE + c * kChunkBytes, &a.tm_q, c * 64, q0 + t * kTileRows, head, batch, bars.q_full());
+        int issued_k = 0, issued_v = 0;
+        for (int j = 0; j < ntile1; ++j) {
+          const int s = j % NS;
+          const uint32_t ph = (j / NS) & 1;
+          if (!mbar_wait(bars.k_empty(s), ph ^ 1, wc)) break;
+          mbar_arrive_expect_tx(bars.k_full(s), C::TILE);
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_4d(sK + s * C::TILE + c * kChunkBytes, &a.tm_k, c * 64, j * kTileRows, head, batch, bars.k_full(s));
+          ++issued_k;
+          if (!mbar_wait(bars.v_empty(s), ph ^ 1, wc)) break;
+          mbar_arrive_expect_tx(bars.v_full(s), C::TILE);
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_4d(sV + s * C::TILE + c * kChunkBytes, &a.tm_v, c * 64, j * kTileRows, head, batch, bars.v_full(s));
+          ++issued_v;
+        }
+        // On abort, every load this thread issued must land before the CTA exits.
+        if (*abort_flag) {
+          for (int j = max(0, issued_k - NS); j < issued_k; ++j) mbar_drain(bars.k_full(j % NS), (j / NS) & 1, a.timeout_ns);
+          for (int j = max(0, issued_v - NS); j < issued_v; ++j) mbar_drain(bars.v_full(j % NS), (j / NS) & 1, a.timeout_ns);
+          mbar_drain(bars.q_full(), 0, a.timeout_ns);
+        } else if (MULTI && nunits > 1) {
+          // Before the next block re-arms the barriers, the commits that free the ring slots (the last
+          // ones are never waited for otherwise) must all have arrived.
+          for (int j = ntile1; j < ntile1 + NS; ++j) {
+            if (!mbar_wait(bars.k_empty(j % NS), ((j / NS) & 1) ^ 1, wc)) break;
+            if (!mbar_wait(bars.v_empty(j % NS), ((j / NS) & 1) ^ 1, wc)) break;
+          }
+        }
+      } else if (warp == 9 && lane == 0 && ntile1 > 0) {
+        // ---- MMA issuer
+        constexpr uint32_t idS = idesc_f16(128, 128, BF16, false, false);
+        constexpr uint32_t idPV = idesc_f16(128, D, BF16, false, true);
+        bool ok = mbar_wait(bars.q_full(), 0, wc);
+        // Descriptor low words of the operand bases; a K step adds a constant (the issue loop of a
+        // single thread must keep up with one MMA per 64 tensor-core cycles).
+        constexpr uint32_t kTileLo = C::TILE >> 4;
+        const uint32_t q_lo = sdesc_lo(sQ, 16), k_lo = sdesc_lo(sK, 16), v_lo = sdesc_lo(sV, kChunkBytes);
 
-      auto issue_S = [&](int t, int j) -> bool {
-        const int s = j % NS;
-        if (!mbar_wait(bars.k_full(s), (j / NS) & 1, wc)) return false;
-        tc_fence_after();
-        const uint32_t d = tmem + t * 128, a_lo = q_lo + t * kTileLo, b_lo = k_lo + s * kTileLo;
-        mma_ss_lo<false>(d, a_lo, b_lo, idS);
-#pragma unroll
-        for (int k = 1; k < D / 16; ++k) {
-          const uint32_t off = ((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4;
-          mma_ss_lo<true>(d, a_lo + off, b_lo + off, idS);
-        }
-        mma_commit(bars.s_full(t));
-        return true;
-      };
-      auto issue_PV = [&](int t, int j) -> bool {
-        const int s = j % NS;
-        if (!mbar_wait(bars.v_full(s), (j / NS) & 1, wc)) return false;
-        if (!mbar_wait(bars.p_full(t), j & 1, wc)) return false;
-        tc_fence_after();
-        const uint32_t d = tmem + 256 + t * 128, a = tmem + t * 128, b_lo = v_lo + s * kTileLo;
-        mma_ts_lo_rt(d, a, b_lo, idPV, j > 0 ? 1u : 0u);
-#pragma unroll
-        for (int k = 1; k < kTileRows / 16; ++k) mma_ts_lo<true>(d, a + k * 8, b_lo + k * (2048 >> 4), idPV);
-        return true;
-      };
+        auto issue_S = [&](int t, int j) -> bool {
+          const int s = j % NS;
+          if (!mbar_wait(bars.k_full(s), (j / NS) & 1, wc)) return false;
+          tc_fence_after();
+          const uint32_t d = tmem + t * 128, a_lo = q_lo + t * kTileLo, b_lo = k_lo + s * kTileLo;
+          mma_ss_lo<false>(d, a_lo, b_lo, idS);
+  #pragma unroll
+          for (int k = 1; k < D / 16; ++k) {
+            const uint32_t off = ((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4;
+            mma_ss_lo<true>(d, a_lo + off, b_lo + off, idS);
+          }
+          mma_commit(bars.s_full(t));
+          return true;
+        };
+        auto issue_PV = [&](int t, int j) -> bool {
+          const int s = j % NS;
+          if (!mbar_wait(bars.v_full(s), (j / NS) & 1, wc)) return false;
+          if (!mbar_wait(bars.p_full(t), j & 1, wc)) return false;
+          tc_fence_after();
+          const uint32_t d = tmem + 256 + t * 128, a = tmem + t * 128, b_lo = v_lo + s * kTileLo;
+          mma_ts_lo_rt(d, a, b_lo, idPV, j > 0 ? 1u : 0u);
+  #pragma unroll
+          for (int k = 1; k < kTileRows / 16; ++k) mma_ts_lo<true>(d, a + k * 8, b_lo + k * (2048 >> 4), idPV);
+          return true;
+        };
 
-      if (ok && ntile0 > 0) ok = issue_S(0, 0);
-      if (ok) ok = issue_S(1, 0);
-      if (ok) mma_commit(bars.k_empty(0));
-      for (int j = 0; ok && j < ntile1; ++j) {
-        if (j < ntile0) {
-          if (!(ok = issue_PV(0, j))) break;
-          if (j == ntile0 - 1) mma_commit(bars.o_full(0));
-          if (j + 1 < ntile0 && !(ok = issue_S(0, j + 1))) break;
+        if (ok && ntile0 > 0) ok = issue_S(0, 0);
+        if (ok) ok = issue_S(1, 0);
+        if (ok) mma_commit(bars.k_empty(0));
+        for (int j = 0; ok && j < ntile1; ++j) {
+          if (j < ntile0) {
+            if (!(ok = issue_PV(0, j))) break;
+            if (j == ntile0 - 1) mma_commit(bars.o_full(0));
+            if (j + 1 < ntile0 && !(ok = issue_S(0, j + 1))) break;
+          }
+          if (!(ok = issue_PV(1, j))) break;
+          mma_commit(bars.v_empty(j % NS));
+          if (j == ntile1 - 1) mma_commit(bars.o_full(1));
+          if (j + 1 < ntile1) {
+            if (!(ok = issue_S(1, j + 1))) break;
+            mma_commit(bars.k_empty((j + 1) % NS));
+          }
         }
-        if (!(ok = issue_PV(1, j))) break;
-        mma_commit(bars.v_empty(j % NS));
-        if (j == ntile1 - 1) mma_commit(bars.o_full(1));
-        if (j + 1 < ntile1) {
-          if (!(ok = issue_S(1, j + 1))) break;
-          mma_commit(bars.k_empty((j + 1) % NS));
-        }
+        // Every MMA issued above completes before TMEM can be released.
+        mma_commit(bars.mma_done());
+        mbar_drain(bars.mma_done(), 0, a.timeout_ns);
       }
-      // Every MMA issued above completes before TMEM can be released.
-      mma_commit(bars.mma_done());
-      mbar_drain(bars.mma_done(), 0, a.timeout_ns);
     }
   } else {
     // ------------------------------------------------------------ softmax
     regs_increase<kRegsSoftmax>();
-    const int t = warp >> 2;                  // query tile of this warpgroup
-    const int quarter = warp & 3;             // TMEM lane quarter this warp may access
-    const int r = quarter * 32 + lane;        // row inside the tile = TMEM lane
-    const int row = q0 + t * kTileRows + r;   // query index inside the head
-    const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + t * 128 + lane_bits;
-    const uint32_t tO = tmem + 256 + t * 128 + lane_bits;
-    const float c_log2 = a.scale * 1.4426950408889634f;  // scale * log2(e)
-    const int n = t ? ntile1 : ntile0;
-    float m = -INFINITY;  // running max of the scaled scores, base-2 units
-    float l = 0.f;        // running sum of exp2(score - m)
-    bool ok = true;
+    for (int ui = 0; ui < nunits; ++ui) {
+      if (!next_unit(ui)) break;
+      const Unit u = unit_of(ui);
+      const int bh = u.bh, head = u.head, batch = u.batch, q0 = u.q0, ntile0 = u.ntile0, ntile1 = u.ntile1;
+      const int t = warp >> 2;                  // query tile of this warpgroup
+      const int quarter = warp & 3;             // TMEM lane quarter this warp may access
+      const int r = quarter * 32 + lane;        // row inside the tile = TMEM lane
+      const int row = q0 + t * kTileRows + r;   // query index inside the head
+      const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
+      const uint32_t tS = tmem + t * 128 + lane_bits;
+      const uint32_t tO = tmem + 256 + t * 128 + lane_bits;
+      const float c_log2 = a.scale * 1.4426950408889634f;  // scale * log2(e)
+      const int n = t ? ntile1 : ntile0;
+      float m = -INFINITY;  // running max of the scaled scores, base-2 units
+      float l = 0.f;        // running sum of exp2(score - m)
+      bool ok = true;
 
-    for (int j = 0; j < n; ++j) {
-      if (!(ok = mbar_wait_warp(bars.s_full(t), j & 1, wc))) break;
-      tc_fence_after();
-      // Columns at or past `lim` are masked (ragged last key tile, causal diagonal tile).
-      const bool need_mask =
-          ((j + 1) * kTileRows > a.Nk) || (CAUSAL && j * kTileRows + kTileRows - 1 > q0 + t * kTileRows + coff);
-      const int lim = need_mask ? (CAUSAL ? min(a.Nk, row + coff + 1) : a.Nk) - j * kTileRows : kTileRows;
-      if (need_mask)
-        softmax_tile<D, true, BF16>(tS, tO, lim, c_log2, j == 0, m, l, [] {});
-      else
-        softmax_tile<D, false, BF16>(tS, tO, lim, c_log2, j == 0, m, l, [] {});
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bars.p_full(t));
-    }
-
-    // ------------------------------------------------------------ epilogue
-    // A row that saw no key (l = 0) gets O = 0 and LSE = -inf.  A tile with no key tiles at all
-    // never had its O accumulated; it stages zeros once the Q copy into its staging tile has landed.
-    // (With no key tile anywhere in the block nothing was loaded and there is nothing to wait for.)
-    if (ok && (n > 0 || ntile1 > 0)) ok = mbar_wait_warp(n > 0 ? bars.o_full(t) : bars.q_full(), 0, wc);
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-      if (row < a.Nq)
-        a.lse[static_cast<size_t>(bh) * a.Nq + row] = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-      const uint32_t stage = sQ + t * C::TILE;  // Q_t is dead: all of its MMAs completed before o_full
-#pragma unroll
-      for (int ch = 0; ch < C::NCH; ++ch) {
-        uint32_t o[2][32];
-        if (n > 0) {
-          tmem_ld32(tO + ch * 64, o[0]);
-          tmem_ld32(tO + ch * 64 + 32, o[1]);
-          tmem_wait_ld();
-          reg_fence32(o[0]);
-          reg_fence32(o[1]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[0][i] = o[1][i] = 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int h = u >> 2, b = (u & 3) * 8;
-          const uint32_t w0 = pack2<BF16>(__uint_as_float(o[h][b + 0]) * inv_l, __uint_as_float(o[h][b + 1]) * inv_l);
-          const uint32_t w1 = pack2<BF16>(__uint_as_float(o[h][b + 2]) * inv_l, __uint_as_float(o[h][b + 3]) * inv_l);
-          const uint32_t w2 = pack2<BF16>(__uint_as_float(o[h][b + 4]) * inv_l, __uint_as_float(o[h][b + 5]) * inv_l);
-          const uint32_t w3 = pack2<BF16>(__uint_as_float(o[h][b + 6]) * inv_l, __uint_as_float(o[h][b + 7]) * inv_l);
-          st_shared_v4(stage + ch * kChunkBytes + sw128_offset(r, u), w0, w1, w2, w3);
-        }
+      for (int j = 0; j < n; ++j) {
+        if (!(ok = mbar_wait_warp(bars.s_full(t), j & 1, wc))) break;
+        tc_fence_after();
+        // Columns at or past `lim` are masked (ragged last key tile, causal diagonal tile).
+        const bool need_mask =
+            ((j + 1) * kTileRows > a.Nk) || (CAUSAL && j * kTileRows + kTileRows - 1 > q0 + t * kTileRows + coff);
+        const int lim = need_mask ? (CAUSAL ? min(a.Nk, row + coff + 1) : a.Nk) - j * kTileRows : kTileRows;
+        if (need_mask)
+          softmax_tile<D, true, BF16>(tS, tO, lim, c_log2, j == 0, m, l, [] {});
+        else
+          softmax_tile<D, false, BF16>(tS, tO, lim, c_log2, j == 0, m, l, [] {});
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bars.p_full(t));
       }
-      fence_proxy_async_smem();
-    }
-    named_bar_sync(1 + t, 128);
-    if (ok && r == 0 && q0 + t * kTileRows < a.Nq && !*abort_flag) {
-      for (int ch = 0; ch < C::NCH; ++ch)
-        tma_store_4d(&a.tm_o, sQ + t * C::TILE + ch * kChunkBytes, ch * 64, q0 + t * kTileRows, head, batch);
-      tma_store_commit();
-      tma_store_wait_all();
+
+      // ------------------------------------------------------------ epilogue
+      // A row that saw no key (l = 0) gets O = 0 and LSE = -inf.  A tile with no key tiles at all
+      // never had its O accumulated; it stages zeros once the Q copy into its staging tile has landed.
+      // (With no key tile anywhere in the block nothing was loaded and there is nothing to wait for.)
+      if (ok && (n > 0 || ntile1 > 0)) ok = mbar_wait_warp(n > 0 ? bars.o_full(t) : bars.q_full(), 0, wc);
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+        if (row < a.Nq)
+          a.lse[static_cast<size_t>(bh) * a.Nq + row] = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+        const uint32_t stage = sQ + t * C::TILE;  // Q_t is dead: all of its MMAs completed before o_full
+  #pragma unroll
+        for (int ch = 0; ch < C::NCH; ++ch) {
+          uint32_t o[2][32];
+          if (n > 0) {
+            tmem_ld32(tO + ch * 64, o[0]);
+            tmem_ld32(tO + ch * 64 + 32, o[1]);
+            tmem_wait_ld();
+            reg_fence32(o[0]);
+            reg_fence32(o[1]);
+          } else {
+  #pragma unroll
+            for (int i = 0; i < 32; ++i) o[0][i] = o[1][i] = 0u;
+          }
+  #pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int h = u >> 2, b = (u & 3) * 8;
+            const uint32_t w0 = pack2<BF16>(__uint_as_float(o[h][b + 0]) * inv_l, __uint_as_float(o[h][b + 1]) * inv_l);
+            const uint32_t w1 = pack2<BF16>(__uint_as_float(o[h][b + 2]) * inv_l, __uint_as_float(o[h][b + 3]) * inv_l);
+            const uint32_t w2 = pack2<BF16>(__uint_as_float(o[h][b + 4]) * inv_l, __uint_as_float(o[h][b + 5]) * inv_l);
+            const uint32_t w3 = pack2<BF16>(__uint_as_float(o[h][b + 6]) * inv_l, __uint_as_float(o[h][b + 7]) * inv_l);
+            st_shared_v4(stage + ch * kChunkBytes + sw128_offset(r, u), w0, w1, w2, w3);
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      named_bar_sync(1 + t, 128);
+      if (ok && r == 0 && q0 + t * kTileRows < a.Nq && !*abort_flag) {
+        for (int ch = 0; ch < C::NCH; ++ch)
+          tma_store_4d(&a.tm_o, sQ + t * C::TILE + ch * kChunkBytes, ch * 64, q0 + t * kTileRows, head, batch);
+        tma_store_commit();
+        tma_store_wait_all();
+      }
     }
   }
 
@@ -311,13 +499,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   }
 }
 
+// One 256-row query block per CTA; the grid is (B*H, blocks) with the heaviest causal blocks first.
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdArgs a) {
+  fwd_body<D, CAUSAL, BF16, false>(a, nullptr, 1);
+}
+
+// Persistent: CTA i takes the blocks sch.unit[sch.begin[i] .. sch.begin[i + 1]).
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel_persistent(const __grid_constant__ FwdArgs a,
+                                                                       const __grid_constant__ FwdSchedule sch) {
+  const int b = sch.begin[blockIdx.x], e = sch.begin[blockIdx.x + 1];
+  fwd_body<D, CAUSAL, BF16, true>(a, sch.unit + b, e - b);
+}
+
 template <int D, bool CAUSAL, bool BF16>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
+  const int nqb = (a.Nq + kFwdSubTiles * kTileRows - 1) / (kFwdSubTiles * kTileRows);
+  const FwdSchedule* sch = CAUSAL ? persistent_schedule(a, nqb) : nullptr;
+  if (sch) {
+    auto kern = fwd_kernel_persistent<D, CAUSAL, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    kern<<<sch->ctas, kFwdThreads, C::SMEM_ALLOC, stream>>>(a, *sch);
+    return cudaGetLastError();
+  }
   auto kern = fwd_kernel<D, CAUSAL, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  const int nqb = (a.Nq + kFwdSubTiles * kTileRows - 1) / (kFwdSubTiles * kTileRows);
   dim3 grid(a.bh_count, nqb, 1);
   kern<<<grid, kFwdThreads, C::SMEM_ALLOC, stream>>>(a);
   return cudaGetLastError();

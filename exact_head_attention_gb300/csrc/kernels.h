@@ -24,6 +24,7 @@ struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 4-D maps {d, N, H, B}, box {64, 128, 1, 1}, 128-byte swizzle
   float* lse;                          // [B*H][Nq]
   uint32_t* err_word;
+  int sm_count;                        // of the device (the persistent causal launch runs one CTA per SM)
   int bh_count, heads, Nq, Nk, d;
   bool causal, bf16;
   int causal_off;

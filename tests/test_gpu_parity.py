@@ -178,6 +178,31 @@ def test_outputs_written_everywhere():
         assert torch.isfinite(t).all()
 
 
+@pytest.mark.parametrize("shape", [(1, 12, 8192, 8192, 128, "bf16", True), (1, 12, 8192, 8192, 64, "fp16", True)],
+                         ids=["8k_causal_d128", "8k_causal_d64"])
+def test_every_query_block_written_by_the_packed_forward(shape):
+    """Causal shapes whose forward runs one CTA per SM over host-packed lists of query blocks (12 heads of
+    32 blocks: too coarse for an even spread over the SMs in launch order): O and LSE pre-filled with NaN
+    must be overwritten everywhere (every block is on exactly one list), and a second call must give the
+    same bits."""
+    from exact_head_attention_gb300 import exattn
+    w = workloads.custom(*shape, index=35)
+    x = workloads.make_inputs(w)
+    dev = torch.device("cuda")
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    outs = []
+    for _ in range(2):
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full((w.B, w.H, w.Nq), float("nan"), device=dev)
+        assert exattn.fwd_raw(q, k, v, o, lse, w.causal, w.scale) == 0
+        outs.append((o, lse))
+    torch.cuda.synchronize()
+    assert exattn.check_device_error() == 0
+    for o, lse in outs:
+        assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
 def test_guard_bytes_untouched():
     """Writes stay inside the outputs: sentinel bytes around each output are unchanged."""
     from exact_head_attention_gb300 import exattn
