@@ -326,7 +326,8 @@ def kernel_source_sha() -> str:
     the device headers they include, and from kernels.h the argument structs they take and the integer
     constants (the other workloads' structs there do not change these kernels)."""
     h = hashlib.sha256()
-    for f in ("attn_fwd.cu", "attn_bwd.cu", "ptx.cuh", "kernels.h", "softmax.cuh", "kv_order.cuh"):
+    for f in ("attn_fwd.cu", "attn_bwd.cu", "ptx.cuh", "kernels.h", "softmax.cuh", "kv_order.cuh", "fwd_schedule.h",
+              "fwd_schedule.cu"):
         src = open(os.path.join(ROOT, "exact_head_attention_gb300", "csrc", f)).read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
         src = re.sub(r"//[^\n]*", "", src)

@@ -13,6 +13,7 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/exattn.h"
+#include "fwd_schedule.h"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -280,6 +281,27 @@ extern "C" size_t attn_bwd_workspace_size(int B, int H, int Nq, int d) {
   if (B <= 0 || H <= 0 || Nq <= 0 || (d != 64 && d != 128)) return 0;
   const size_t rows = static_cast<size_t>(B) * H * padded_rows(Nq);
   return align256(rows * d * sizeof(float)) + 2 * align256(rows * sizeof(float));
+}
+
+// The forward's packed lists of query blocks (persistent_schedule), for callers and tests.
+extern "C" int attn_fwd_schedule(int B, int H, int Nq, int Nk, int d, int causal, int sm_count, uint32_t* blocks,
+                                 int blocks_cap, int* begin, int begin_cap) {
+  if (check_common(B, H, Nq, Nk, d, causal, 1.0f, ATTN_BF16) != ATTN_OK) return -1;
+  if (sm_count <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return -1;
+  }
+  if (causal == ATTN_MASK_NONE) return 0;
+  const int nqb = (Nq + kFwdSubTiles * kTileRows - 1) / (kFwdSubTiles * kTileRows);
+  const FwdSchedule* sch = persistent_schedule(B * H, nqb, Nq, Nk, causal_offset(causal, Nq, Nk), sm_count);
+  if (!sch) return 0;
+  const int n = sch->begin[sch->ctas];
+  if (!blocks || !begin || blocks_cap < n || begin_cap < sch->ctas + 1) return -1;
+  for (int i = 0; i < n; ++i) blocks[i] = sch->unit[i];
+  for (int c = 0; c <= sch->ctas; ++c) begin[c] = sch->begin[c];
+  return sch->ctas;
 }
 
 // The launch grouping head_group picks, for callers and tests (sm_count / l2_bytes 0: this device's).

@@ -32,12 +32,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include <algorithm>
-#include <map>
-#include <mutex>
-#include <tuple>
-#include <vector>
-
+#include "fwd_schedule.h"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "softmax.cuh"
@@ -81,117 +76,6 @@ struct FwdBars {
   __device__ uint32_t o_full(int t) const { return base + 8 * (5 + 4 * ns + t); }
   __device__ uint32_t mma_done() const { return base + 8 * (7 + 4 * ns); }
 };
-
-// ------------------------------------------------------------ persistent schedule
-//
-// Under a causal mask a 256-row query block's work grows with its position, from one key tile to the
-// whole row.  With one CTA per block the hardware hands blocks to SMs heaviest first, which leaves
-// about a tenth of the SMs' time idle at the end of the 8k workload (the blocks are few and coarse
-// against the SM count).  The persistent launch instead runs one CTA per SM over a list of blocks that
-// the host packs: longest first onto the least loaded CTA, then moves and swaps that lower the most
-// loaded CTA's total.  A block's cost is the key tiles its two query tiles visit plus a fixed part for
-// its start and its epilogue.
-constexpr int kPersistMaxCtas = 160;
-constexpr int kPersistMaxUnits = 2048;
-constexpr int kUnitFixedCost = 2;    // in key-tile visits
-constexpr int kPersistBlockCost = 2;  // extra per block on a list: the CTA-wide hand-over between blocks
-
-struct FwdSchedule {
-  int ctas;
-  uint16_t begin[kPersistMaxCtas + 1];  // CTA i runs unit[begin[i] .. begin[i + 1])
-  uint32_t unit[kPersistMaxUnits];      // bh * nqb + qb
-};
-
-// The packed schedule for this launch, or nullptr when a plain launch is as good (one wave or less) or
-// the blocks do not fit the schedule's capacity.  Schedules are cached per shape.
-const FwdSchedule* persistent_schedule(const FwdArgs& a, int nqb) {
-  const long long units = static_cast<long long>(a.bh_count) * nqb;
-  const int ctas = std::min(a.sm_count, kPersistMaxCtas);
-  if (ctas <= 0 || units <= ctas || units > kPersistMaxUnits) return nullptr;
-  using Key = std::tuple<int, int, int, int, int, int>;
-  static std::mutex mu;
-  static std::map<Key, FwdSchedule> cache;
-  const Key key{a.bh_count, nqb, a.Nq, a.Nk, a.causal_off, ctas};
-  std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find(key);
-  if (it != cache.end()) return it->second.ctas > 0 ? &it->second : nullptr;
-  if (cache.size() >= 64) cache.clear();
-
-  const int nkv = (a.Nk + kTileRows - 1) / kTileRows;
-  auto tiles = [&](int qb, int t) {
-    const int last_key = qb * kFwdSubTiles * kTileRows + t * kTileRows + kTileRows - 1 + a.causal_off;
-    return last_key < 0 ? 0 : std::min(nkv, last_key / kTileRows + 1);
-  };
-  std::vector<int> qcost(nqb);
-  for (int qb = 0; qb < nqb; ++qb) qcost[qb] = tiles(qb, 0) + tiles(qb, 1) + kUnitFixedCost;
-  std::vector<uint32_t> order(static_cast<size_t>(units));
-  for (uint32_t u = 0; u < order.size(); ++u) order[u] = u;
-  auto cost = [&](uint32_t u) { return qcost[u % nqb]; };
-  std::stable_sort(order.begin(), order.end(), [&](uint32_t x, uint32_t y) { return cost(x) > cost(y); });
-  std::vector<std::vector<uint32_t>> bins(ctas);
-  std::vector<long long> load(ctas, 0);
-  for (uint32_t u : order) {  // longest first onto the least loaded CTA
-    const int b = static_cast<int>(std::min_element(load.begin(), load.end()) - load.begin());
-    bins[b].push_back(u);
-    load[b] += cost(u);
-  }
-  const long long lpt_max = *std::max_element(load.begin(), load.end());  // about what a plain launch gets
-  // Improve: move a block off the most loaded CTA, or swap it for a lighter one, while that lowers
-  // the larger of the two totals below the current maximum.
-  for (int round = 0; round < 4 * ctas; ++round) {
-    const int hi = static_cast<int>(std::max_element(load.begin(), load.end()) - load.begin());
-    bool improved = false;
-    for (int lo = 0; lo < ctas && !improved; ++lo) {
-      if (lo == hi) continue;
-      for (size_t i = 0; i < bins[hi].size() && !improved; ++i) {
-        const int ca = cost(bins[hi][i]);
-        if (std::max(load[hi] - ca, load[lo] + ca) < load[hi]) {
-          bins[lo].push_back(bins[hi][i]);
-          bins[hi].erase(bins[hi].begin() + static_cast<long>(i));
-          load[hi] -= ca;
-          load[lo] += ca;
-          improved = true;
-          break;
-        }
-        for (size_t j = 0; j < bins[lo].size(); ++j) {
-          const int cb = cost(bins[lo][j]);
-          if (cb >= ca) continue;
-          if (std::max(load[hi] - ca + cb, load[lo] - cb + ca) < load[hi]) {
-            std::swap(bins[hi][i], bins[lo][j]);
-            load[hi] += cb - ca;
-            load[lo] += ca - cb;
-            improved = true;
-            break;
-          }
-        }
-      }
-    }
-    if (!improved) break;
-  }
-  FwdSchedule& sch = cache[key];
-  // A block on a list costs a little more than a block of its own (the hand-over between blocks: two
-  // CTA-wide barriers, the ring drained, the barriers re-armed), and a list mixes heads and positions, so
-  // concurrent blocks share fewer K/V tiles in L2 than the plain launch's order.  Lists are used only
-  // where, with that extra cost, they still shorten the most loaded SM by 3 % or more.  Measured: the 8k
-  // workload's forward 160 -> 154 us packed; 32k ones, already balanced within 2 %, 4-8 % slower packed;
-  // 1k blocks (a few key tiles each) 4 % slower packed.
-  long long packed_max = 0;
-  for (int b = 0; b < ctas; ++b)
-    packed_max = std::max(packed_max, load[b] + kPersistBlockCost * static_cast<long long>(bins[b].size()));
-  if (100 * packed_max > 97 * lpt_max) {
-    sch.ctas = 0;
-    return nullptr;
-  }
-  sch.ctas = ctas;
-  int pos = 0;
-  for (int b = 0; b < ctas; ++b) {
-    std::sort(bins[b].begin(), bins[b].end(), [&](uint32_t x, uint32_t y) { return cost(x) > cost(y); });
-    sch.begin[b] = static_cast<uint16_t>(pos);
-    for (uint32_t u : bins[b]) sch.unit[pos++] = u;
-  }
-  sch.begin[ctas] = static_cast<uint16_t>(pos);
-  return &sch;
-}
 
 // The forward of query blocks units[0 .. nunits) of 256 rows each; unit = bh * nqb + qb.  A plain launch
 // gives each CTA one block; a persistent launch gives each CTA (one per SM) a list that the host packed
@@ -517,7 +401,7 @@ template <int D, bool CAUSAL, bool BF16>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
   const int nqb = (a.Nq + kFwdSubTiles * kTileRows - 1) / (kFwdSubTiles * kTileRows);
-  const FwdSchedule* sch = CAUSAL ? persistent_schedule(a, nqb) : nullptr;
+  const FwdSchedule* sch = CAUSAL ? persistent_schedule(a.bh_count, nqb, a.Nq, a.Nk, a.causal_off, a.sm_count) : nullptr;
   if (sch) {
     auto kern = fwd_kernel_persistent<D, CAUSAL, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);

@@ -95,6 +95,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.attn_kl_fwd_splitkv.restype = i
             lib.attn_kl_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i, i]
             lib.attn_kl_fwd_splitkv_workspace_size.restype = sz
+            lib.attn_fwd_schedule.argtypes = [i, i, i, i, i, i, i, vp, i, vp, i]
+            lib.attn_fwd_schedule.restype = i
             lib.attn_bwd_head_group.argtypes = [i, i, i, i, i, i, i, sz]
             lib.attn_bwd_head_group.restype = i
             lib.attn_bwd_auto_dq_mode.argtypes = [i, i, i, i, i, i]
@@ -268,6 +270,20 @@ def bwd_strided_raw(q, k, v, o, do, lse, dq, dk, dv, causal, scale: float, works
     return load().attn_bwd_strided(*_view(q), *_view(k), *_view(v), *_view(o), *_view(do), _ptr(lse),
                                    *_view(dq), *_view(dk), *_view(dv), B, H, Nq, Nk, d, mask_code(causal),
                                    float(scale), _dtype_code(q), *_workspace(workspace), _stream(stream))
+
+
+def fwd_schedule(B: int, H: int, Nq: int, Nk: int, d: int, causal=False, sm_count: int = 0):
+    """The forward's packed lists of query blocks (attn_fwd_schedule): a list of per-CTA lists of block
+    ids (bh * ceil(Nq/256) + qb), or None when the plain launch is used."""
+    cap = 2048
+    blocks = (ctypes.c_uint32 * cap)()
+    begin = (ctypes.c_int * 256)()
+    n = int(load().attn_fwd_schedule(B, H, Nq, Nk, d, mask_code(causal), sm_count, blocks, cap, begin, 256))
+    if n < 0:
+        raise ValueError("invalid sizes")
+    if n == 0:
+        return None
+    return [list(blocks[begin[c]:begin[c + 1]]) for c in range(n)]
 
 
 def head_group(B: int, H: int, Nq: int, Nk: int, d: int, causal=False, sm_count: int = 0, l2_bytes: int = 0) -> int:

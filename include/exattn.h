@@ -340,6 +340,24 @@ typedef enum {
 } attn_dq_mode;
 
 /*
+ * How attn_fwd spreads a causal forward over the SMs.  The forward's work is
+ * in 256-row query blocks, block = bh * ceil(Nq/256) + qb, and under a causal
+ * mask a block's work grows with its position qb.  Where launching one CTA per
+ * block (heaviest first) would leave SMs idle at the end, attn_fwd instead
+ * runs one CTA per SM over lists of blocks that the host packs so that the
+ * CTAs' work is even.  Returns the number of lists (CTAs), with the lists in
+ * blocks[begin[i] .. begin[i+1]) for i < that number, or 0 when the plain
+ * launch is used (no mask, one wave or less, more than 2048 blocks, or a
+ * packing that would not shorten the busiest SM by 3 % after the hand-over
+ * cost between a CTA's blocks).  blocks_cap and begin_cap are the capacities
+ * of the two caller-owned host arrays.  sm_count <= 0 takes the current
+ * device's.  Returns -1 for sizes attn_fwd rejects, arrays too small, or a
+ * device count that is needed and cannot be read.
+ */
+int attn_fwd_schedule(int B, int H, int Nq, int Nk, int d, int causal, int sm_count, uint32_t* blocks,
+                      int blocks_cap, int* begin, int begin_cap);
+
+/*
  * Heads per launch group of the key/value-block kernels when dQ is reduced
  * into the fp32 accumulator (ATTN_DQ_ATOMIC, and the one-pass KL backward).
  * The blocks (one per head and 128-row key block) are numbered in groups of
