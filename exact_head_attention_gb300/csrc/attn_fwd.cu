@@ -29,6 +29,11 @@
 // entirely and only tiles the diagonal crosses (or the ragged last tile) are
 // masked.  A query tile that sees no key at all (bottom-right, Nq > Nk) writes
 // O = 0 and LSE = -inf without touching the tensor pipe.
+//
+// Launches: one CTA per 256-row block (grid (B*H, blocks), heaviest causal
+// blocks first), or, for causal grids too coarse to balance that way, one CTA
+// per SM over host-packed lists of blocks (fwd_schedule.h), walked by the same
+// body with the barriers re-armed between blocks.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
