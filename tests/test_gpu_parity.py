@@ -203,6 +203,22 @@ def test_every_query_block_written_by_the_packed_forward(shape):
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
+def test_packed_forward_bottom_right_ragged_sampled():
+    """A list-scheduled causal forward with the bottom-right mask and a ragged last block (Nq = 8000,
+    Nk = 9000): sampled rows of three heads, the last rows included, against the oracle."""
+    from exact_head_attention_gb300 import exattn
+    w = workloads.custom(1, 12, 8000, 9000, 128, "bf16", "bottom_right", index=36)
+    assert exattn.fwd_schedule(w.B, w.H, w.Nq, w.Nk, w.d, w.causal) is not None or \
+        torch.cuda.get_device_properties(0).multi_processor_count != 152
+    x = workloads.make_inputs(w)
+    got = run_gpu(w, x, backward=False)
+    for h in (0, 5, 11):
+        xs = {n: x[n][:, h:h + 1] for n in ("q", "k", "v")}
+        rows = np.array(sorted(set(sample_rows(w.Nq, 40, 36 + h).tolist()) | {7999, 7998, 7936, 7935}), dtype=np.int64)
+        o_r, lse_r = oracle.attn_fwd_rows(xs["q"], xs["k"], xs["v"], w.causal, w.scale, rows)
+        check_fwd(w, got["o"][0, h, rows], got["lse"][0, h, rows], o_r, lse_r, f"{w.name} head {h}")
+
+
 def test_guard_bytes_untouched():
     """Writes stay inside the outputs: sentinel bytes around each output are unchanged."""
     from exact_head_attention_gb300 import exattn
