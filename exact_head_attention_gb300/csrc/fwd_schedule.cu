@@ -105,7 +105,11 @@ const FwdSchedule* persistent_schedule(int bh, int nqb, int Nq, int Nk, int caus
     it = cache.emplace(key, FwdSchedule{}).first;
     pack(bh, nqb, Nk, causal_off, ctas, &it->second);
   }
-  return it->second.ctas > 0 ? &it->second : nullptr;
+  if (it->second.ctas == 0) return nullptr;
+  // A copy per thread: another thread may clear the cache as soon as the lock is released.
+  thread_local FwdSchedule copy;
+  copy = it->second;
+  return &copy;
 }
 
 }  // namespace exattn

@@ -23,7 +23,8 @@ struct FwdSchedule {
 
 // The packed lists for a causal forward of bh heads of nqb 256-row blocks (causal_off as in FwdArgs),
 // or nullptr when the launch order is used: one wave or less, more blocks than a list holds, or a
-// packing that does not beat the launch order clearly.  Cached per shape; the pointer stays valid.
+// packing that does not beat the launch order clearly.  Cached per shape; the pointer is to this
+// thread's copy and stays valid until the thread's next call.
 const FwdSchedule* persistent_schedule(int bh, int nqb, int Nq, int Nk, int causal_off, int sm_count);
 
 }  // namespace exattn
