@@ -42,6 +42,7 @@
 #define EXATTN_H
 
 #include <stddef.h>
+#include <stdint.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -260,7 +261,11 @@ attn_status attn_kl_bwd_ex(const void* Q1, const void* K1, const void* Q2, const
  * Bytes of device workspace attn_bwd needs for this shape: an fp32 dQ
  * accumulator [B,H,ceil(Nq/128)*128,d] plus two fp32 row vectors of the same
  * padded length (D = rowsum(dO o O) and the base-2 LSE).  Returns 0 for
- * invalid sizes.
+ * invalid sizes.  The accumulator is the buffer that the thread blocks of
+ * SparkAttention Figure 9 (and the column-block backward of "Fast Transformer
+ * training with long sequences") add their dQ contributions into; D is that
+ * figure's dPsum term.  The pages do not size it: this helper exists because
+ * the caller owns all device memory.
  */
 size_t attn_bwd_workspace_size(int B, int H, int Nq, int d);
 
@@ -473,7 +478,9 @@ attn_status attn_bwd_noalloc(const void* Q, const void* K, const void* V, const 
                              int B, int H, int Nq, int Nk, int d, int causal, float scale,
                              attn_dtype dtype, void* stream);
 
-/* Static description of a status code. */
+/* Static description of a status code (a diagnostic of this library; the
+ * pages have no counterpart).  Never NULL: unknown codes give
+ * "unknown status". */
 const char* attn_status_string(attn_status status);
 
 /*
