@@ -11,9 +11,10 @@ FLOPs per step follow the metric's convention: forward 4*B*H*Nq*Nk*d, backward
 
 Timing: W untimed warm-up steps, then K timed steps; between timed steps a
 256 MiB buffer is written (L2 flush) outside the timed events; every launch is
-bracketed by CUDA events on the launching stream; ms_per_step is the mean of
-the per-step device times, max over ranks.  With N > 1 (torchrun) every rank
-runs an independent replica of the workload (no collective on the data path).
+bracketed by CUDA events on the launching stream; ms_per_step is the median
+of the per-step device times, max over ranks (the mean is reported beside
+it).  With N > 1 (torchrun) every rank runs an independent replica of the
+workload (no collective on the data path).
 
 --impl reference times the CPU oracle (the plain fp64 definition) on the host
 cores instead, on bounded samples of the same workload.
@@ -42,6 +43,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -50,6 +52,7 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd+bwd TFLOPS (causal-adjusted) and % of GB300 BF16 tensor peak"
 FALLBACK_BF16_TFLOPS = 1900.0
+SPEC_BF16_TFLOPS = 2500.0  # GB300 dense bf16 tensor rate as specified (no sparsity), for context beside the measured peak
 FLUSH_BYTES = 256 << 20
 
 
@@ -109,12 +112,14 @@ class ClockSampler:
 
     def __init__(self, uuid: str | None):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # samples go to a private temporary file (EXATTN_CLOCKS_CSV names another place to keep them)
+        self.path = os.environ.get("EXATTN_CLOCKS_CSV") or os.path.join(
+            tempfile.gettempdir(), f"exattn_clocks_{os.getpid()}.csv")
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
         if uuid:
             cmd.insert(1, f"--id={uuid}")
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
@@ -203,13 +208,13 @@ def run_reference(args, w) -> None:
     for _ in range(args.warmup):
         _oracle_step(x, w, n)
     times = [_oracle_step(x, w, n) for _ in range(args.steps)]
-    mean = statistics.mean(times)
-    value = _sample_flops(w, n) / mean / 1e12
+    med = statistics.median(times)
+    value = _sample_flops(w, n) / med / 1e12
     sample = (f"per step: fp64 oracle forward+backward of head (b=0,h=0), first {n} queries and keys "
               f"(of {w.Nq}), 1 thread")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": med * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(w, {"sample_n": n}),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
@@ -297,7 +302,7 @@ def pipelined_e2e(steps: int, slots: list, h2d, compute, d2h, flush) -> tuple[fl
         b.record(s_cmp)
         b.synchronize()
         alone.append(a.elapsed_time(b))
-    return pipe_ms, statistics.mean(alone)
+    return pipe_ms, statistics.median(alone)
 
 
 E2E_NOTE = ("pipelined over steps on three CUDA streams (copy-in, compute, copy-out) with two device buffer sets; "
@@ -379,12 +384,12 @@ def run_decode(args, w, rank: int, world: int) -> None:
         for _ in range(args.warmup):
             _oracle_decode_heads(x, w, nheads)
         times = [_oracle_decode_heads(x, w, nheads) for _ in range(args.steps)]
-        mean = statistics.mean(times)
-        value = decode_bytes(w) * nheads / (w.B * w.H) / mean / 1e9
+        med = statistics.median(times)
+        value = decode_bytes(w) * nheads / (w.B * w.H) / med / 1e9
         sample = f"per step: fp64 oracle forward of the first {nheads} of {w.B * w.H} heads, 1 thread"
         print(json.dumps({
             "impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": med * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_dict(w, {"sample_heads": nheads}),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
@@ -450,7 +455,7 @@ def run_decode(args, w, rank: int, world: int) -> None:
         dist.barrier()
     if exattn.check_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
-    ms_per_step = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), dist, dev)
+    ms_per_step = max_over_ranks(statistics.median(a.elapsed_time(b) for a, b in evs), dist, dev)
 
     # end to end: pinned host Q, K, V -> device -> split-KV forward -> host O, LSE
     hq, hk, hv = (x[n].pin_memory() for n in ("q", "k", "v"))
@@ -551,12 +556,12 @@ def run_kl(args, w, rank: int, world: int) -> None:
         n = _kl_pick_n(x, w, max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup))))
         for _ in range(args.warmup):
             _oracle_kl_step(x, w, n)
-        mean = statistics.mean(_oracle_kl_step(x, w, n) for _ in range(args.steps))
-        value = _kl_sample_flops(w, n) / mean / 1e12
+        med = statistics.median(_oracle_kl_step(x, w, n) for _ in range(args.steps))
+        value = _kl_sample_flops(w, n) / med / 1e12
         sample = f"per step: fp64 oracle KL forward + student backward of head (0,0), first {n} queries and keys, 1 thread"
         print(json.dumps({
             "impl": "reference", "metric": KL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": med * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_dict(w, {"sample_n": n}),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
@@ -628,8 +633,8 @@ def run_kl(args, w, rank: int, world: int) -> None:
         dist.barrier()
     if exattn.check_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
-    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
     ms_per_step = max_over_ranks(fwd_ms + bwd_ms, dist, dev)
 
     # end to end: pinned host Q1, K1, Q2, K2, g -> device -> forward + backward -> host KL, dQ2, dK2
@@ -809,11 +814,13 @@ def main() -> None:
         dist.barrier()
     if exattn.check_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
-    ms_per_step = statistics.mean(a.elapsed_time(b) for a, b in step_ev)
-    ms_per_step = max_over_ranks(ms_per_step, dist, dev)
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    ms_per_step = max_over_ranks(statistics.median(step_ms), dist, dev)
+    ms_per_step_mean = max_over_ranks(statistics.mean(step_ms), dist, dev)
     per = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)] for i in range(args.steps)]
-    kern_ms = {name: statistics.mean(p[j] for p in per)
-               for j, name in enumerate(("fwd", "bwd_preprocess", "bwd_kv_blocks", "bwd_dq_convert"))}
+    kern_names = ("fwd", "bwd_preprocess", "bwd_kv_blocks", "bwd_dq_convert")
+    kern_ms = {name: statistics.median(p[j] for p in per) for j, name in enumerate(kern_names)}
+    kern_ms_mean = {name: statistics.mean(p[j] for p in per) for j, name in enumerate(kern_names)}
 
     # end to end through the C ABI: pinned host inputs -> device -> fwd + bwd -> host outputs
     hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "do"))
@@ -850,7 +857,8 @@ def main() -> None:
     value = job_throughput(flops, world, ms_per_step)
     pk = peaks()
     dominant = "bwd_kv_blocks"
-    achieved = bwd_f / (kern_ms[dominant] * 1e-3) / 1e12
+    # the roofline's kernel duration is its mean over the timed launches (the step figures are medians)
+    achieved = bwd_f / (kern_ms_mean[dominant] * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -861,9 +869,12 @@ def main() -> None:
                                   "timing": "timed region = two passes of the steps: ms_per_step from CUDA "
                                             "events around each whole step (forward call, backward call); "
                                             "kernels_ms from the second pass, with an event after every kernel"}),
+        "ms_per_step_mean": ms_per_step_mean,
         "pct_of_peak": 100.0 * (flops / (ms_per_step * 1e-3) / 1e12) / pk["bf16_tflops"],
         "peak_tflops": pk["bf16_tflops"], "peak_source": pk["source"],
-        "kernels_ms": kern_ms,
+        "pct_of_spec": 100.0 * (flops / (ms_per_step * 1e-3) / 1e12) / SPEC_BF16_TFLOPS,
+        "spec_tflops": SPEC_BF16_TFLOPS,
+        "kernels_ms": kern_ms, "kernels_ms_mean": kern_ms_mean,
         "fwd_tflops": fwd_f / (kern_ms["fwd"] * 1e-3) / 1e12,
         "bwd_tflops": bwd_f / (sum(kern_ms[n] for n in ("bwd_preprocess", "bwd_kv_blocks", "bwd_dq_convert")) * 1e-3) / 1e12,
         # each rate as a fraction of the measured bf16 tensor peak
