@@ -23,9 +23,14 @@ namespace {
 constexpr size_t kScratchBytes = ATTN_BWD_NOALLOC_MAX_WORKSPACE_BYTES;
 constexpr int kMaxDevices = 64;
 
-// The scratch array.  Every GPU on which this library's code is loaded reserves
-// it until the process exits.  In host code `g_bwd_scratch` only names a
-// host-side stand-in: its device address comes from cudaGetSymbolAddress.
+// The scratch array.  A GPU reserves it when this file's module is loaded there
+// (with CUDA's default lazy module loading: at the first attn_bwd_noalloc call
+// on that device; with eager loading: when the library's code is loaded) and
+// keeps it until the process exits.  In host code `g_bwd_scratch` only names a
+// host-side stand-in: its device address comes from cudaGetSymbolAddress.  The
+// address is looked up once per device and kept, so a device must not be
+// reset (cudaDeviceReset) while the library is in use: a new context may place
+// the array elsewhere.
 static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
 
 std::mutex g_scratch_mutex;
@@ -51,8 +56,19 @@ extern "C" attn_status attn_bwd_noalloc(const void* Q, const void* K, const void
   }
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return ATTN_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) {
+    char msg[160];
+    std::snprintf(msg, sizeof(msg), "attn_bwd_noalloc: cudaGetDevice: %s", cudaGetErrorName(e));
+    set_last_error(msg);
+    return ATTN_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    char msg[160];
+    std::snprintf(msg, sizeof(msg), "attn_bwd_noalloc: device index %d is beyond the %d devices this library tracks",
+                  dev, kMaxDevices);
+    set_last_error(msg);
+    return ATTN_ERR_UNSUPPORTED;
+  }
   void* scratch = nullptr;
   {
     // One-time set-up per device, with that device current: look up the array's device address.

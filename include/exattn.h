@@ -27,8 +27,12 @@
  * are rounded to nearest even into the input dtype.
  *
  * Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
- * stream) and allocate no device memory.  Arguments are validated before any
- * launch; on an error status nothing is launched and no output is written.
+ * stream) and allocate no device memory.  The library keeps per-device state
+ * (the device address of its error word, the device's SM count and L2 size)
+ * from the first call on a device to process exit: do not reset a device
+ * (cudaDeviceReset) while the library is in use on it.  Arguments are
+ * validated before any launch; on an error status nothing is launched and no
+ * output is written.
  * The backward's kernels are dependent launches (programmatic stream
  * serialisation): each may start before the work ahead of it on the stream
  * has finished, but waits for that work before it reads or writes anything
@@ -459,13 +463,19 @@ attn_status attn_selftest_wait_timeout(int timeout_ms, void* stream);
  *
  * Same arguments, layouts and results as attn_bwd, minus the workspace: the
  * scratch comes from one fixed array of ATTN_BWD_NOALLOC_MAX_WORKSPACE_BYTES
- * built into the library, which every GPU that loads the library reserves
- * until the process exits.  Nothing is allocated by this call.
+ * built into the library.  A GPU reserves the array when the library's module
+ * that holds it is loaded there -- with CUDA's default lazy module loading at
+ * the first attn_bwd_noalloc call on that device, with eager loading
+ * (CUDA_MODULE_LOADING=EAGER) when the library's code is loaded -- and keeps
+ * it until the process exits.  Nothing is allocated by this call.
  *   - Shapes whose attn_bwd_workspace_size exceeds the maximum are rejected
  *     with ATTN_ERR_WORKSPACE (attn_last_error gives the sizes); nothing runs.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture begins.
+ *     before any stream capture begins.  The address is kept for the life
+ *     of the process, so do not reset the device (cudaDeviceReset) between
+ *     calls: the library's per-device state, this address included, would
+ *     then name memory of a context that no longer exists.
  *   - All calls share the one array, which keeps the last call's contents;
  *     each call clears what must start at zero.  Calls whose executions
  *     overlap on the GPU (different streams, or different host threads on

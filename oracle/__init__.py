@@ -74,16 +74,19 @@ def _load():
             lib.oracle_attn_fwd_rows.argtypes = [dp, dp, dp, I, I, L, L, I, I, D, L, lp, dp, dp]
             lib.oracle_attn_dq_rows.argtypes = [dp, dp, dp, dp, I, I, L, L, I, I, D, L, lp, dp, dp]
             lib.oracle_attn_dkdv_cols.argtypes = [dp, dp, dp, dp, I, I, L, L, I, I, D, L, lp, dp, dp]
+            lib.oracle_attn_dkdv_cols_part.argtypes = [dp, dp, dp, dp, I, I, L, L, I, I, D, L, lp, L, L, dp, dp]
             lib.oracle_attn_probs.argtypes = [dp, dp, L, L, I, I, D, dp, dp]
             lib.oracle_kl_fwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, I, I, L, L, I, I, D]
             lib.oracle_kl_bwd.argtypes = [dp, dp, dp, dp, dp, I, dp, dp, I, I, L, L, I, I, D]
             lib.oracle_kl_fwd_rows.argtypes = [dp, dp, dp, dp, I, I, L, L, I, I, D, L, lp, dp, dp, dp]
             lib.oracle_kl_dq_rows.argtypes = [dp, dp, dp, dp, dp, I, I, I, L, L, I, I, D, L, lp, dp]
             lib.oracle_kl_dk_cols.argtypes = [dp, dp, dp, dp, dp, I, I, I, L, L, I, I, D, L, lp, dp]
+            lib.oracle_kl_dk_cols_part.argtypes = [dp, dp, dp, dp, dp, I, I, I, L, L, I, I, D, L, lp, L, L, dp]
             for f in (lib.oracle_attn_fwd, lib.oracle_attn_bwd, lib.oracle_attn_fwd_rows,
-                      lib.oracle_attn_dq_rows, lib.oracle_attn_dkdv_cols, lib.oracle_attn_probs,
+                      lib.oracle_attn_dq_rows, lib.oracle_attn_dkdv_cols, lib.oracle_attn_dkdv_cols_part,
+                      lib.oracle_attn_probs,
                       lib.oracle_kl_fwd, lib.oracle_kl_bwd, lib.oracle_kl_fwd_rows, lib.oracle_kl_dq_rows,
-                      lib.oracle_kl_dk_cols):
+                      lib.oracle_kl_dk_cols, lib.oracle_kl_dk_cols_part):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -179,17 +182,22 @@ def attn_dq_rows(q, k, v, do, causal, scale: float, rows):
     return dq, D
 
 
-def attn_dkdv_cols(q, k, v, do, causal, scale: float, cols):
-    """dK and dV for chosen key rows; cols[i] = (b*H + h)*Nk + k."""
+def attn_dkdv_cols(q, k, v, do, causal, scale: float, cols, q_range=None):
+    """dK and dV for chosen key rows; cols[i] = (b*H + h)*Nk + k.
+
+    q_range = (q_lo, q_hi) keeps only the contributions of query rows q_lo <= q < q_hi (dK and dV are sums
+    over query rows; the parts of a partition of the rows add up to the whole)."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, Nq, Nk, d = _shape(q, k)
     cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
     dk = np.zeros((len(cols), d))
     dv = np.zeros((len(cols), d))
-    rc = _load().oracle_attn_dkdv_cols(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, H, Nq, Nk, d,
-                                       _mask(causal), float(scale), len(cols), _lptr(cols), _ptr(dk), _ptr(dv))
+    lo, hi = (0, Nq) if q_range is None else (int(q_range[0]), int(q_range[1]))
+    rc = _load().oracle_attn_dkdv_cols_part(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, H, Nq, Nk, d,
+                                            _mask(causal), float(scale), len(cols), _lptr(cols), lo, hi,
+                                            _ptr(dk), _ptr(dv))
     if rc != 0:
-        raise MemoryError("oracle_attn_dkdv_cols failed")
+        raise MemoryError("oracle_attn_dkdv_cols_part failed")
     return dk, dv
 
 
@@ -269,14 +277,18 @@ def kl_dq_rows(q1, k1, q2, k2, g, setting, causal, scale: float, rows):
     return dq
 
 
-def kl_dk_cols(q1, k1, q2, k2, g, setting, causal, scale: float, cols):
-    """dK of the trained distribution for chosen key rows; cols[i] = (b*H + h)*Nk + k."""
+def kl_dk_cols(q1, k1, q2, k2, g, setting, causal, scale: float, cols, q_range=None):
+    """dK of the trained distribution for chosen key rows; cols[i] = (b*H + h)*Nk + k.
+
+    q_range = (q_lo, q_hi) keeps only the contributions of query rows q_lo <= q < q_hi."""
     q1, k1, q2, k2, g = _f64(q1), _f64(k1), _f64(q2), _f64(k2), _f64(g)
     B, H, Nq, Nk, d = _kl_shape(q1, k1, q2, k2)
     cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
     dk = np.zeros((len(cols), d))
-    rc = _load().oracle_kl_dk_cols(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(g), _setting(setting), B, H, Nq,
-                                   Nk, d, _mask(causal), float(scale), len(cols), _lptr(cols), _ptr(dk))
+    lo, hi = (0, Nq) if q_range is None else (int(q_range[0]), int(q_range[1]))
+    rc = _load().oracle_kl_dk_cols_part(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(g), _setting(setting), B, H,
+                                        Nq, Nk, d, _mask(causal), float(scale), len(cols), _lptr(cols), lo, hi,
+                                        _ptr(dk))
     if rc != 0:
-        raise MemoryError("oracle_kl_dk_cols failed")
+        raise MemoryError("oracle_kl_dk_cols_part failed")
     return dk

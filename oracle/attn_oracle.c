@@ -248,14 +248,21 @@ int oracle_attn_dq_rows(const double* Q, const double* K, const double* V, const
 }
 
 /*
- * dK and dV restricted to chosen key columns (cols[i] = bh * Nk + k);
- * dK_cols, dV_cols [ncols][d].  Every query row that sees a chosen key is
- * evaluated in full (its whole score row), exactly as in oracle_attn_bwd.
+ * The part of dK and dV of chosen key columns (cols[i] = bh * Nk + k) that
+ * comes from the query rows q in [q_lo, q_hi): dK_k and dV_k are sums over
+ * query rows, dK_k = scale sum_q dS_qk Q_q and dV_k = sum_q P_qk dO_q, and
+ * this is that sum over the given rows only (the rows of any partition of
+ * [0, Nq) add up to the whole).  dK_cols, dV_cols [ncols][d].  Every query
+ * row taken is evaluated in full (its whole score row), exactly as in
+ * oracle_attn_bwd.
  */
-int oracle_attn_dkdv_cols(const double* Q, const double* K, const double* V, const double* dO,
-                          int B, int H, long Nq, long Nk, int d, int causal, double scale,
-                          long ncols, const long* cols, double* dK_cols, double* dV_cols) {
+int oracle_attn_dkdv_cols_part(const double* Q, const double* K, const double* V, const double* dO,
+                               int B, int H, long Nq, long Nk, int d, int causal, double scale,
+                               long ncols, const long* cols, long q_lo, long q_hi,
+                               double* dK_cols, double* dV_cols) {
   const long off = mask_offset(causal, Nq, Nk);
+  if (q_lo < 0) q_lo = 0;
+  if (q_hi > Nq) q_hi = Nq;
   double* P = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
   double* dP = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
   if (!P || !dP) {
@@ -275,7 +282,9 @@ int oracle_attn_dkdv_cols(const double* Q, const double* K, const double* V, con
     const double* Kh = K + (size_t)bh * Nk * d;
     const double* Vh = V + (size_t)bh * Nk * d;
     const double* dOh = dO + (size_t)bh * Nq * d;
-    for (long q = (causal && kmin - off > 0) ? kmin - off : 0; q < Nq; ++q) {
+    long q0 = (causal && kmin - off > 0) ? kmin - off : 0;
+    if (q0 < q_lo) q0 = q_lo;
+    for (long q = q0; q < q_hi; ++q) {
       double lse;
       row_probs(Qh, Kh, Nk, d, q, causal, off, scale, P, &lse);
       double D = row_dp(dOh, Vh, Nk, d, q, P, dP);
@@ -296,6 +305,14 @@ int oracle_attn_dkdv_cols(const double* Q, const double* K, const double* V, con
   free(P);
   free(dP);
   return 0;
+}
+
+/* dK and dV of chosen key columns (cols[i] = bh * Nk + k) over all query rows. */
+int oracle_attn_dkdv_cols(const double* Q, const double* K, const double* V, const double* dO,
+                          int B, int H, long Nq, long Nk, int d, int causal, double scale,
+                          long ncols, const long* cols, double* dK_cols, double* dV_cols) {
+  return oracle_attn_dkdv_cols_part(Q, K, V, dO, B, H, Nq, Nk, d, causal, scale, ncols, cols, 0, Nq, dK_cols,
+                                    dV_cols);
 }
 
 /* The full probability matrix of one head, P [Nq][Nk] (small shapes; used by invariant checks). */
@@ -488,12 +505,19 @@ int oracle_kl_dq_rows(const double* Q1, const double* K1, const double* Q2, cons
   return 0;
 }
 
-/* dK of the trained distribution for chosen key rows (cols[i] = bh * Nk + k); dK_cols [ncols][d]. */
-int oracle_kl_dk_cols(const double* Q1, const double* K1, const double* Q2, const double* K2, const double* G,
-                      int setting, int B, int H, long Nq, long Nk, int d, int causal, double scale, long ncols,
-                      const long* cols, double* dK_cols) {
+/*
+ * The part of dK of the trained distribution, for chosen key rows (cols[i] =
+ * bh * Nk + k), that comes from the query rows q in [q_lo, q_hi): dK_k =
+ * scale sum_q dS_qk Q_q summed over the given rows only (the rows of any
+ * partition of [0, Nq) add up to the whole).  dK_cols [ncols][d].
+ */
+int oracle_kl_dk_cols_part(const double* Q1, const double* K1, const double* Q2, const double* K2, const double* G,
+                           int setting, int B, int H, long Nq, long Nk, int d, int causal, double scale, long ncols,
+                           const long* cols, long q_lo, long q_hi, double* dK_cols) {
   if (setting != 1 && setting != 2) return -2;
   const long off = mask_offset(causal, Nq, Nk);
+  if (q_lo < 0) q_lo = 0;
+  if (q_hi > Nq) q_hi = Nq;
   double* P1 = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
   double* P2 = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
   double* dS = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
@@ -511,7 +535,9 @@ int oracle_kl_dk_cols(const double* Q1, const double* K1, const double* Q2, cons
     if (kmin < 0) continue;
     const size_t qo = (size_t)bh * Nq * d, ko = (size_t)bh * Nk * d;
     const double* Qt = (setting == 1 ? Q2 : Q1) + qo;
-    for (long q = (causal && kmin - off > 0) ? kmin - off : 0; q < Nq; ++q) {
+    long q0 = (causal && kmin - off > 0) ? kmin - off : 0;
+    if (q0 < q_lo) q0 = q_lo;
+    for (long q = q0; q < q_hi; ++q) {
       kl_row_ds(Q1 + qo, K1 + ko, Q2 + qo, K2 + ko, Nk, d, q, causal, off, scale, G[(size_t)bh * Nq + q], setting,
                 P1, P2, dS);
       for (long i = 0; i < ncols; ++i) {
@@ -526,4 +552,12 @@ int oracle_kl_dk_cols(const double* Q1, const double* K1, const double* Q2, cons
   free(P2);
   free(dS);
   return 0;
+}
+
+/* dK of the trained distribution for chosen key rows (cols[i] = bh * Nk + k) over all query rows. */
+int oracle_kl_dk_cols(const double* Q1, const double* K1, const double* Q2, const double* K2, const double* G,
+                      int setting, int B, int H, long Nq, long Nk, int d, int causal, double scale, long ncols,
+                      const long* cols, double* dK_cols) {
+  return oracle_kl_dk_cols_part(Q1, K1, Q2, K2, G, setting, B, H, Nq, Nk, d, causal, scale, ncols, cols, 0, Nq,
+                                dK_cols);
 }

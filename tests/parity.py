@@ -8,6 +8,9 @@ Tolerances (fixed by the method's numeric contract):
 """
 from __future__ import annotations
 
+import concurrent.futures
+import os
+
 import numpy as np
 import torch
 
@@ -95,3 +98,41 @@ def sample_rows(N: int, n: int, seed: int) -> np.ndarray:
     rows = set(r for r in fixed if 0 <= r < N)
     rows.update(rng.integers(0, N, size=max(0, n - len(rows))).tolist())
     return np.array(sorted(rows), dtype=np.int64)
+
+
+def heavy_cols(Nk: int) -> np.ndarray:
+    """Key rows of the first key blocks and one in the middle.  Under a causal mask the first keys are seen by
+    every query row, so their dK/dV sum over all query tiles: the longest accumulations in the backward."""
+    return np.array(sorted({c for c in (0, 1, 127, 128, Nk // 2) if 0 <= c < Nk}), dtype=np.int64)
+
+
+def query_parts(Nq: int, Nk: int, causal, parts: int):
+    """Split the query rows [0, Nq) into `parts` ranges of about equal oracle work (a row costs its visible
+    keys)."""
+    q = np.arange(Nq, dtype=np.int64)
+    off = Nk - Nq if causal == "bottom_right" else 0
+    cost = np.clip(q + off + 1, 0, Nk) if causal else np.full(Nq, Nk)
+    cum = np.cumsum(cost + 1)
+    cuts = np.searchsorted(cum, cum[-1] * np.arange(1, parts) / parts).tolist()
+    edges = sorted({0, Nq, *[min(max(c, 0), Nq) for c in cuts]})
+    return list(zip(edges[:-1], edges[1:]))
+
+
+def oracle_cols_threaded(fn, Nq: int, Nk: int, causal, workers: int | None = None):
+    """Sum fn(q_range) over a partition of the query rows, the parts on a thread pool.
+
+    fn is a column-sampled oracle call (dK/dV of chosen key rows restricted to query rows in q_range); the
+    oracle's C code runs without holding the GIL, so the parts run on separate cores.  The parts of a
+    partition add up to the whole sum over query rows (pinned on CPU)."""
+    workers = workers or max(1, min(16, len(os.sched_getaffinity(0))))
+    parts = query_parts(Nq, Nk, causal, workers)
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
+        results = list(ex.map(fn, parts))
+    if isinstance(results[0], tuple):
+        return tuple(sum(r[i] for r in results) for i in range(len(results[0])))
+    return sum(results)
+
+
+def f64_head(t, b: int, h: int) -> np.ndarray:
+    """One head of a [B, H, N, d] (or [B, H, N]) tensor as a contiguous fp64 array with B = H = 1 (exact)."""
+    return np.ascontiguousarray(t[b:b + 1, h:h + 1].double().cpu().numpy())

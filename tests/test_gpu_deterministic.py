@@ -11,7 +11,7 @@ import torch
 import oracle
 from exact_head_attention_gb300 import exattn, workloads
 
-from parity import check_grads, rel_l2, sample_rows
+from parity import check_grads, f64_head, heavy_cols, oracle_cols_threaded, rel_l2, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -79,9 +79,14 @@ def test_deterministic_long_workloads_sampled(name):
         sel = lambda t: t[b:b + 1, h:h + 1]  # noqa: E731
         dq_r, _ = oracle.attn_dq_rows(sel(x["q"]), sel(x["k"]), sel(x["v"]), sel(x["do"]), w.causal, w.scale, rows)
         check_grads({"dq": dq[b, h, rows]}, {"dq": dq_r}, f"{name} head {bh} dQ rows")
-        cols = np.array([w.Nk - 1, w.Nk - 100, w.Nk - 300], dtype=np.int64)
-        dk_c, dv_c = oracle.attn_dkdv_cols(sel(x["q"]), sel(x["k"]), sel(x["v"]), sel(x["do"]), w.causal, w.scale,
-                                           cols)
+        # the last key rows and those of the first key blocks (every query tile adds into them when causal)
+        cols = np.array(sorted({w.Nk - 1, w.Nk - 100, w.Nk - 300, *heavy_cols(w.Nk).tolist()}), dtype=np.int64)
+        xs = {n: f64_head(x[n], b, h) for n in ("q", "k", "v", "do")}
+
+        def part(r):
+            return oracle.attn_dkdv_cols(xs["q"], xs["k"], xs["v"], xs["do"], w.causal, w.scale, cols, q_range=r)
+
+        dk_c, dv_c = oracle_cols_threaded(part, w.Nq, w.Nk, w.causal)
         check_grads({"dk": dk[b, h, cols], "dv": dv[b, h, cols]}, {"dk": dk_c, "dv": dv_c}, f"{name} head {bh}")
 
 

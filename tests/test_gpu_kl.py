@@ -16,7 +16,7 @@ import torch
 import oracle
 from exact_head_attention_gb300 import exattn, workloads
 
-from parity import rel_l2, sample_rows
+from parity import f64_head, heavy_cols, oracle_cols_threaded, rel_l2, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -128,13 +128,20 @@ def test_kl_workload_full_size_sampled(mode, shape):
         rows = sample_rows(w.Nq, 48, 11 + h)
         ref = oracle.kl_fwd_rows(*args, w.causal, w.scale, rows)
         _check_fwd(kl[b, h, rows], l1[b, h, rows], l2[b, h, rows], ref, f"{w.name} head {h}")
-        cols = np.array([w.Nk - 1, w.Nk - 77, w.Nk - 300], dtype=np.int64)
+        # the last key rows and those of the first key tiles (every query tile adds into them when causal)
+        cols = np.array(sorted({w.Nk - 1, w.Nk - 77, w.Nk - 300, *heavy_cols(w.Nk).tolist()}), dtype=np.int64)
+        a64 = tuple(f64_head(x[n], b, h) for n in ("q1", "k1", "q2", "k2"))
+        g64 = f64_head(x["g"], b, h)
         for train, setting in (("student", 1), ("teacher", 2)):
             dq, dk = (t.float().cpu().numpy() for t in grads[train])
             rq = oracle.kl_dq_rows(*args, sel(x["g"]), setting, w.causal, w.scale, rows[:24])
             assert rel_l2(dq[b, h, rows[:24]], rq) <= GRAD_TOL, f"{train} dQ rows head {h}"
-            rk = oracle.kl_dk_cols(*args, sel(x["g"]), setting, w.causal, w.scale, cols)
-            assert rel_l2(dk[b, h, cols], rk) <= GRAD_TOL, f"{train} dK rows head {h}"
+
+            def part(r, setting=setting):
+                return oracle.kl_dk_cols(*a64, g64, setting, w.causal, w.scale, cols, q_range=r)
+
+            rk = oracle_cols_threaded(part, w.Nq, w.Nk, w.causal)
+            assert rel_l2(dk[b, h, cols], rk) <= GRAD_TOL, f"{train} dK rows {cols.tolist()} head {h}"
 
 
 @pytest.mark.parametrize("shape,splits", [

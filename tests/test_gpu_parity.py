@@ -3,8 +3,9 @@
 Small and ragged shapes are compared element by element over every output;
 the mid-size workloads on a subset of heads with the full oracle; the
 long-sequence workloads at full size on sampled query rows (O, LSE, dQ) and
-key rows (dK, dV) that the oracle evaluates one by one, plus gradient
-invariants that hold at any size.
+key rows (dK, dV) that the oracle evaluates one by one -- the last key rows
+and the rows of the first key blocks, which every query tile adds into under
+a causal mask -- plus gradient invariants that hold at any size.
 """
 import numpy as np
 import pytest
@@ -13,7 +14,8 @@ import torch
 import oracle
 from exact_head_attention_gb300 import workloads
 
-from parity import (check_fwd, check_grads, oracle_heads, pick_heads, rel_l2, run_gpu, sample_rows)
+from parity import (check_fwd, check_grads, f64_head, heavy_cols, oracle_cols_threaded, oracle_heads, pick_heads,
+                    rel_l2, run_gpu, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -88,9 +90,26 @@ def _check_invariants(w, x, got, what):
     assert (err <= 2e-2).all(), f"{what}: sum_k dV_k != sum_q dO_q ({err.max():.2e})"
 
 
-def _sampled_check(w, x, got, n_rows, heads, seed):
+def _heavy_cols_check(w, x, got, b, h):
+    """dK and dV of head (b, h) on the rows of its first key blocks and one in the middle.  Under a causal mask
+    the first keys are seen by every query row, so these rows accumulate over all query tiles (the key block
+    that does the most work); the oracle evaluates every query row for them, split over threads."""
+    cols = heavy_cols(w.Nk)
+    xs = {n: f64_head(x[n], b, h) for n in ("q", "k", "v", "do")}
+
+    def part(r):
+        return oracle.attn_dkdv_cols(xs["q"], xs["k"], xs["v"], xs["do"], w.causal, w.scale, cols, q_range=r)
+
+    dk_c, dv_c = oracle_cols_threaded(part, w.Nq, w.Nk, w.causal)
+    check_grads({"dk": got["dk"][b, h, cols], "dv": got["dv"][b, h, cols]}, {"dk": dk_c, "dv": dv_c},
+                f"{w.name} head ({b},{h}) dK/dV rows {cols.tolist()}")
+
+
+def _sampled_check(w, x, got, n_rows, heads, seed, heavy=True):
     N = w.Nq
     for (b, h) in heads:
+        if heavy:
+            _heavy_cols_check(w, x, got, b, h)
         bh = b * w.H + h
         rows = sample_rows(N, n_rows, seed + bh)
         flat = bh * N + rows
@@ -157,7 +176,8 @@ def test_very_long_sequences_sampled(shape):
     w = workloads.custom(*shape, index=31)
     x = workloads.make_inputs(w)
     got = run_gpu(w, x)
-    _sampled_check(w, x, got, 24, [(0, 0)], seed=w.index)
+    # the first key rows here would need every one of 100k-200k query rows evaluated in full: the tail only
+    _sampled_check(w, x, got, 24, [(0, 0)], seed=w.index, heavy=False)
 
 
 def test_outputs_written_everywhere():
@@ -187,6 +207,7 @@ def test_every_query_block_written_by_the_packed_forward(shape):
     same bits."""
     from exact_head_attention_gb300 import exattn
     w = workloads.custom(*shape, index=35)
+    _require_packed(w)
     x = workloads.make_inputs(w)
     dev = torch.device("cuda")
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
@@ -203,13 +224,21 @@ def test_every_query_block_written_by_the_packed_forward(shape):
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
+def _require_packed(w):
+    """Skip unless this device runs the shape's forward from packed lists (the plan depends on the SM count)."""
+    from exact_head_attention_gb300 import exattn
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    lists = exattn.fwd_schedule(w.B, w.H, w.Nq, w.Nk, w.d, w.causal, sm_count=sms)
+    if lists is None:
+        pytest.skip(f"the forward of this shape runs in launch order on {sms} SMs")
+    return lists
+
+
 def test_packed_forward_bottom_right_ragged_sampled():
     """A list-scheduled causal forward with the bottom-right mask and a ragged last block (Nq = 8000,
     Nk = 9000): sampled rows of three heads, the last rows included, against the oracle."""
-    from exact_head_attention_gb300 import exattn
     w = workloads.custom(1, 12, 8000, 9000, 128, "bf16", "bottom_right", index=36)
-    assert exattn.fwd_schedule(w.B, w.H, w.Nq, w.Nk, w.d, w.causal) is not None or \
-        torch.cuda.get_device_properties(0).multi_processor_count != 152
+    _require_packed(w)
     x = workloads.make_inputs(w)
     got = run_gpu(w, x, backward=False)
     for h in (0, 5, 11):
@@ -217,6 +246,36 @@ def test_packed_forward_bottom_right_ragged_sampled():
         rows = np.array(sorted(set(sample_rows(w.Nq, 40, 36 + h).tolist()) | {7999, 7998, 7936, 7935}), dtype=np.int64)
         o_r, lse_r = oracle.attn_fwd_rows(xs["q"], xs["k"], xs["v"], w.causal, w.scale, rows)
         check_fwd(w, got["o"][0, h, rows], got["lse"][0, h, rows], o_r, lse_r, f"{w.name} head {h}")
+
+
+def test_packed_forward_blocks_without_keys():
+    """Bottom-right mask with more queries than keys (Nq = 9000, Nk = 8000): rows q < 1000 see no key, so the
+    first three 256-row blocks of every head have no key tile, and the packed lists put them behind blocks
+    that do.  Such a block skips the loads and products and writes O = 0, LSE = -inf; the block after it on
+    the same list must still run normally.  O and LSE are pre-filled with NaN; every head's key-less rows
+    are checked exactly and sampled rows (the boundary at q = 1000 included) against the oracle."""
+    from exact_head_attention_gb300 import exattn
+    w = workloads.custom(1, 12, 9000, 8000, 128, "bf16", "bottom_right", index=37)
+    lists = _require_packed(w)
+    nqb = -(-w.Nq // 256)
+    assert any(any(b % nqb < 3 for b in lst[1:]) for lst in lists), "no key-less block follows another block"
+    x = workloads.make_inputs(w)
+    dev = torch.device("cuda")
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((w.B, w.H, w.Nq), float("nan"), device=dev)
+    assert exattn.fwd_raw(q, k, v, o, lse, w.causal, w.scale) == 0
+    torch.cuda.synchronize()
+    assert exattn.check_device_error() == 0
+    o, lse = o.float().cpu().numpy(), lse.cpu().numpy()
+    assert (o[:, :, :1000] == 0).all() and np.isneginf(lse[:, :, :1000]).all()
+    assert np.isfinite(o).all() and np.isfinite(lse[:, :, 1000:]).all()
+    for h in (0, 6, 11):
+        xs = {n: x[n][:, h:h + 1] for n in ("q", "k", "v")}
+        rows = np.array(sorted(set(sample_rows(w.Nq, 32, 37 + h).tolist()) | {998, 999, 1000, 1001, 1023, 1024}),
+                        dtype=np.int64)
+        o_r, lse_r = oracle.attn_fwd_rows(xs["q"], xs["k"], xs["v"], w.causal, w.scale, rows)
+        check_fwd(w, o[0, h, rows], lse[0, h, rows], o_r, lse_r, f"{w.name} head {h}")
 
 
 def test_guard_bytes_untouched():

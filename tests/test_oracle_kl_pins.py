@@ -165,3 +165,23 @@ def test_kl_sampled_functions_match_full(setting, causal, Nq, Nk):
     bk, ki = cols // Nk, cols % Nk
     np.testing.assert_allclose(oracle.kl_dk_cols(q1, k1, q2, k2, g, setting, causal, 0.3, cols),
                                dk.reshape(-1, Nk, d)[bk, ki], atol=1e-13)
+
+
+@pytest.mark.parametrize("setting", [1, 2])
+@pytest.mark.parametrize("causal,Nq,Nk", [(0, 21, 33), (1, 40, 40), (2, 50, 30)])
+def test_kl_dk_column_parts_add_up_to_the_full_backward(setting, causal, Nq, Nk):
+    """dK is a sum over query rows: the parts over a partition of [0, Nq) add up to oracle.kl_bwd's dK, and a
+    part equals the full backward with g zeroed outside its rows (dK is linear in g)."""
+    B, H, d = 2, 2, 8
+    q1, k1, q2, k2, g = _inputs(B, H, Nq, Nk, d, seed=9)
+    _, dk = oracle.kl_bwd(q1, k1, q2, k2, g, setting, causal, 0.3)
+    cols = np.array([0, 1, Nk // 2, Nk - 1, Nk + 2, 3 * Nk + Nk - 1])
+    bk, ki = cols // Nk, cols % Nk
+    edges = [0, 3, 3, Nq // 2, Nq]
+    parts = [oracle.kl_dk_cols(q1, k1, q2, k2, g, setting, causal, 0.3, cols, q_range=(a, b))
+             for a, b in zip(edges[:-1], edges[1:])]
+    np.testing.assert_allclose(sum(parts), dk.reshape(-1, Nk, d)[bk, ki], atol=1e-13)
+    g_part = np.zeros_like(g)
+    g_part[:, :, 3:Nq // 2] = g[:, :, 3:Nq // 2]
+    _, dk_p = oracle.kl_bwd(q1, k1, q2, k2, g_part, setting, causal, 0.3)
+    np.testing.assert_allclose(parts[2], dk_p.reshape(-1, Nk, d)[bk, ki], atol=1e-13)

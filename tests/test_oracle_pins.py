@@ -342,3 +342,51 @@ def test_bottom_right_sampled_rows_and_cols_match_full(Nq, Nk):
     dk_c, dv_c = oracle.attn_dkdv_cols(q, k, v, do, 2, 0.3, cols)
     np.testing.assert_allclose(dk_c, dk.reshape(-1, Nk, d)[bk, ki], atol=1e-13)
     np.testing.assert_allclose(dv_c, dv.reshape(-1, Nk, d)[bk, ki], atol=1e-13)
+
+
+# ------------------------------- query-row parts of the column-sampled gradients
+
+@pytest.mark.parametrize("causal,Nq,Nk", [(0, 37, 29), (1, 40, 40), (2, 30, 50), (2, 50, 30)])
+def test_dkdv_column_parts_add_up_to_the_full_backward(causal, Nq, Nk):
+    """dK_k and dV_k are sums over query rows: the parts over the rows of a partition of [0, Nq) (empty parts,
+    parts without visible keys included) add up to oracle_attn_bwd's full gradients, and a part equals the
+    full backward of the same rows with dO zeroed elsewhere."""
+    B, H, d = 2, 2, 8
+    q, k, v, do = _qkv(B, H, Nq, Nk, d, seed=31)
+    _, dk, dv, _ = oracle.attn_bwd(q, k, v, do, causal, 0.3)
+    cols = np.array([0, 1, Nk // 2, Nk - 1, Nk + 3, 3 * Nk + Nk - 1])
+    bk, ki = cols // Nk, cols % Nk
+    edges = [0, 0, 5, 6, Nq // 2, Nq - 1, Nq]
+    parts = [oracle.attn_dkdv_cols(q, k, v, do, causal, 0.3, cols, q_range=(a, b))
+             for a, b in zip(edges[:-1], edges[1:])]
+    np.testing.assert_allclose(sum(p[0] for p in parts), dk.reshape(-1, Nk, d)[bk, ki], atol=1e-13)
+    np.testing.assert_allclose(sum(p[1] for p in parts), dv.reshape(-1, Nk, d)[bk, ki], atol=1e-13)
+    # rows [6, Nq/2) alone (parts[3]): dK and dV are linear in dO given P (D too), so zeroing dO outside the
+    # rows gives the same part
+    do_part = np.zeros_like(do)
+    do_part[:, :, 6:Nq // 2] = do[:, :, 6:Nq // 2]
+    _, dk_p, dv_p, _ = oracle.attn_bwd(q, k, v, do_part, causal, 0.3)
+    np.testing.assert_allclose(parts[3][0], dk_p.reshape(-1, Nk, d)[bk, ki], atol=1e-13)
+    np.testing.assert_allclose(parts[3][1], dv_p.reshape(-1, Nk, d)[bk, ki], atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True, "bottom_right"])
+def test_threaded_heavy_columns_equal_the_serial_oracle(causal):
+    """The GPU tests' threaded evaluation of the first key rows (parts over query rows on a thread pool,
+    summed) equals one serial oracle call."""
+    import sys
+    sys.path.insert(0, os.path.dirname(__file__))
+    from parity import heavy_cols, oracle_cols_threaded, query_parts
+
+    Nq, Nk, d = 700, 900, 16
+    q, k, v, do = _qkv(1, 1, Nq, Nk, d, seed=32)
+    mask = {False: 0, True: 1, "bottom_right": 2}[causal]
+    cols = heavy_cols(Nk)
+    want = oracle.attn_dkdv_cols(q, k, v, do, mask, 0.25, cols)
+    got = oracle_cols_threaded(lambda r: oracle.attn_dkdv_cols(q, k, v, do, mask, 0.25, cols, q_range=r),
+                               Nq, Nk, causal, workers=5)
+    for a, b in zip(got, want):
+        np.testing.assert_allclose(a, b, atol=1e-12)
+    parts = query_parts(Nq, Nk, causal, 5)
+    assert parts[0][0] == 0 and parts[-1][1] == Nq and all(a < b for a, b in parts)
+    assert all(parts[i][1] == parts[i + 1][0] for i in range(len(parts) - 1))

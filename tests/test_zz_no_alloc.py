@@ -6,10 +6,13 @@ call or its failure.  attn_bwd_noalloc serves them by taking its scratch from a
 fixed array built into the library; the caller passes only inputs and outputs.
 
 These tests call it through the C ABI and compare it with attn_bwd (the entry
-point that takes a caller-supplied workspace), with the same tolerance as the
-parity tests, on two calls in a row (the array keeps the previous call's
-contents, so the second call checks that whatever must start at zero is
-cleared).  The file is named to be collected last: a run that stops at its
+point that takes a caller-supplied workspace) on two calls in a row (the array
+keeps the previous call's contents, so the second call checks that whatever
+must start at zero is cleared).  dK and dV are the same bits on every run of
+the backward, so they must equal attn_bwd's bit for bit; dQ's fp32 reductions
+run in no fixed order, so it must agree within 1e-3 relative L2 (the bound the
+repeatability test of the regular backward uses), far inside the 2e-2 parity
+tolerance against the oracle.  The file is named to be collected last: a run that stops at its
 first failure has already run every other test.  It also passes on its own.
 """
 import ctypes
@@ -49,7 +52,7 @@ def test_noalloc_rejects_shapes_beyond_the_builtin_scratch():
 def test_noalloc_matches_attn_bwd_on_two_calls(shape):
     import torch
 
-    from parity import GRAD_TOL, rel_l2
+    from parity import rel_l2
 
     lib = _lib()
     B, H, Nq, Nk, d, dt, causal = shape
@@ -72,5 +75,6 @@ def test_noalloc_matches_attn_bwd_on_two_calls(shape):
         assert exattn.check_device_error() == 0
         for name, got, want in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
             assert torch.isfinite(got).all(), (call, name)
-            err = rel_l2(got.float().cpu().numpy(), want.double().cpu().numpy())
-            assert err <= GRAD_TOL, (call, name, err)
+        assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2]), call
+        err = rel_l2(dq.float().cpu().numpy(), ref[0].double().cpu().numpy())
+        assert err <= 1e-3, (call, "dq", err)
