@@ -35,10 +35,11 @@ def _cuda_home():
     return os.path.dirname(os.path.dirname(nvcc)) if nvcc else "/usr/local/cuda"
 
 
-def _compile(out, extra):
+def _compile(out, cflags, ldflags=()):
+    """Compile and link the C program; libraries follow the source (the linker drops those named before)."""
     lib_dir = _lib_dir()
-    cmd = ["gcc", "-std=c99", *STRICT, f"-I{INCLUDE}", *extra, SRC, "-o", out,
-           f"-L{lib_dir}", "-lexattn", f"-Wl,-rpath,{lib_dir}"]
+    cmd = ["gcc", "-std=c99", *STRICT, f"-I{INCLUDE}", *cflags, SRC, "-o", out,
+           f"-L{lib_dir}", "-lexattn", f"-Wl,-rpath,{lib_dir}", *ldflags]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
 
@@ -73,7 +74,7 @@ def test_c_program_forward_backward_matches_oracle(tmp_path, shape):
     x = workloads.make_inputs(w)
     cuda = _cuda_home()
     exe = str(tmp_path / "consumer_gpu")
-    _compile(exe, ["-DWITH_CUDART", f"-I{cuda}/include", f"-L{cuda}/lib64", "-lcudart", f"-Wl,-rpath,{cuda}/lib64"])
+    _compile(exe, ["-DWITH_CUDART", f"-I{cuda}/include"], [f"-L{cuda}/lib64", "-lcudart", f"-Wl,-rpath,{cuda}/lib64"])
 
     inp, out = tmp_path / "in.bin", tmp_path / "out.bin"
     hdr = np.array([B, H, Nq, Nk, d, 1 if causal else 0, 0 if dt == "bf16" else 1], dtype=np.int32)
