@@ -352,7 +352,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
     const float c_log2 = a.scale * 1.4426950408889634f;
     const uint32_t ds_row = sDS + h * kChunkBytes;
+    // Once a wait has failed (its time limit expired, or another warp raised the abort flag) a compute
+    // warp does not leave the tile loop: it skips its remaining waits and runs on, so that every warp
+    // of its warpgroup meets the warpgroup's named barriers equally often and in the same order.  (A
+    // warp that left early would arrive at the epilogue's barrier of the same number while the others
+    // wait inside the loop, and the barrier would release both groups in the wrong rounds.)  What the
+    // warp computes after a failure is never stored: the epilogue checks the abort flag.  `ok` stays
+    // warp-uniform.
     bool ok = true;
+    auto wait = [&](uint32_t bar, uint32_t parity) { ok = ok && mbar_wait_warp(bar, parity, wc); };
 
     // dQ_i from TMEM Y -> fp32 reductions into the accumulator; Y is released as soon as the
     // values are in registers.
@@ -363,8 +371,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     // ago); warpgroup 1 uses the dS^T tile, free from the end of the dQ_i MMA until the next dS^T store,
     // which waits for this reduction's read (see dstile_free).  The rows come out of TMEM 32 at a time;
     // with `pp`, this warpgroup's P^T of the next tile goes into the first 32 columns once they are read.
-    auto drain128 = [&](int it, bool with_p, const uint32_t (&pp)[32]) -> bool {
-      if (!mbar_wait_warp(bars.dq_full(), it & 1, wc)) return false;
+    auto drain128 = [&](int it, bool with_p, const uint32_t (&pp)[32]) {
+      wait(bars.dq_full(), it & 1);
       tc_fence_after();
       uint32_t v[32];
       tmem_ld32(tY + lane_bits + h * 64, v);
@@ -398,14 +406,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         bulk_reduce_add_f32(a.dq_acc + row0 * D, sbase + buf_off, C::STAGE_BYTES);
         tma_store_commit();
       }
-      return true;
     };
-    auto drain_dq = [&](int it) -> bool {
+    auto drain_dq = [&](int it) {
       if constexpr (D == 128) {
         const uint32_t none[32] = {};
-        if (!drain128(it, false, none)) return false;
+        drain128(it, false, none);
       } else {
-        if (!mbar_wait_warp(bars.dq_full(), it & 1, wc)) return false;
+        wait(bars.dq_full(), it & 1);
         tc_fence_after();
         // dQ_i: lane = query row; this warpgroup reduces d columns [32h, 32h + 32).  Its box [128
         // query][32 d] (128 bytes per row) goes into its half of the staging tile with the 128-byte
@@ -429,7 +436,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
           tma_store_commit();
         }
       }
-      return true;
     };
 
     const bool ragged_kv = k0 + kTileRows > a.Nk;  // block-uniform
@@ -439,7 +445,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       const float* rowv = reinterpret_cast<const float*>(gbase + C::OFF_ROWV + rs * C::ROWV_BYTES);
       const float* lse2 = rowv + h * 64;
       const float* dsum = rowv + 128 + h * 64;
-      if (!(ok = mbar_wait_warp(bars.s_full(), it & 1, wc))) break;
+      wait(bars.s_full(), it & 1);
       tc_fence_after();
       uint32_t s[2][32];
       tmem_ld32(tX + lane_bits + h * 64, s[0]);
@@ -449,7 +455,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       reg_fence32(s[1]);
       tc_fence_before();
       mbar_arrive(bars.s_used());
-      if (!(ok = mbar_wait_warp(bars.rowv_full(rs), (it >> 1) & 1, wc))) break;
+      wait(bars.rowv_full(rs), (it >> 1) & 1);
 
       // P^T = exp2(S^T * scale*log2e - LSE2); masked entries are exactly 0.  Only query tiles the
       // causal diagonal crosses and a ragged last key block need the mask: columns below `lo` are zeroed.
@@ -481,7 +487,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       // half of Y (dQ_{i-1} runs just before dP^T_i), at d = 64 straight away.  dV_i then queues behind
       // dP^T_i.  Staging dQ_{i-1} for the copy engine fits before dP^T_i lands.
       if (DQ && D == 128 && it > 0) {
-        if (!(ok = drain128(it - 1, true, pp))) break;
+        drain128(it - 1, true, pp);
       } else {
         tmem_st32(tY + lane_bits + p_base<D>() + h * p_stride<D>(), pp);
         tmem_wait_st();
@@ -489,7 +495,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         mbar_arrive(bars.p_ready());  // dV_i may go
       }
 
-      if (!(ok = mbar_wait_warp(bars.dp_full(), it & 1, wc))) break;
+      wait(bars.dp_full(), it & 1);
       tc_fence_after();
       tmem_ld32(tX + lane_bits + h * 64, s[0]);
       tmem_ld32(tX + lane_bits + h * 64 + 32, s[1]);
@@ -518,7 +524,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       tc_fence_before();
       mbar_arrive(bars.pd_ready());  // dK_i and S_{i+1} may go
       if constexpr (!DQ) continue;
-      if (it > 0 && !(ok = mbar_wait_warp(bars.ds_empty(), (it - 1) & 1, wc))) break;
+      if (it > 0) wait(bars.ds_empty(), (it - 1) & 1);
       if constexpr (D == 128) {
         // The dS^T tile held warpgroup 1's dQ_{i-1} rows; the copy engine must have read them.
         if (it > 0 && h == 1) {
@@ -526,7 +532,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
           named_bar_sync(2, 128);
           if (r == 0) mbar_arrive(bars.dstile_free());
         }
-        if (it > 0 && h == 0 && !(ok = mbar_wait_warp(bars.dstile_free(), (it - 1) & 1, wc))) break;
+        if (it > 0 && h == 0) wait(bars.dstile_free(), (it - 1) & 1);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u)
@@ -535,9 +541,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       mbar_arrive(bars.dss_ready());  // dQ_i may go
 
       // d = 64: the previous tile's dQ is staged and handed to the copy engine after this tile is handed over.
-      if (DQ && D == 64 && it > 0 && !(ok = drain_dq(it - 1))) break;
+      if (DQ && D == 64 && it > 0) drain_dq(it - 1);
     }
-    if (DQ && ok && n > 0) ok = drain_dq(n - 1);
+    if (DQ && n > 0) drain_dq(n - 1);
 
     // ------------------------------------------------------------ epilogue
     // warps 0-3 write dV (staged in the V tile), warps 4-7 write dK * scale (staged in the K tile).

@@ -331,15 +331,21 @@ __global__ void __launch_bounds__(kKlBwdThreads, 1) kl_bwd_fused_kernel(const __
       return v;
     };
     float4 rnext = fetch_rows(0);
+    // Once a wait has failed (its time limit expired, or another warp raised the abort flag) a compute
+    // warp does not leave the tile loop: it skips its remaining waits and runs on, so that every warp
+    // of its warpgroup meets the warpgroup's named barriers equally often and in the same order (a warp
+    // that left early would release a barrier of the same number for the wrong round).  What it computes
+    // after a failure is never stored: the epilogue checks the abort flag.  `ok` stays warp-uniform.
     bool ok = true;
+    auto wait = [&](uint32_t bar, uint32_t parity) { ok = ok && mbar_wait_warp(bar, parity, wc); };
 
     // d = 128, dQ_i^T (lane = d, column = query row): this warpgroup reduces query rows [64h, 64h + 64)
     // through a 32 KB row-major buffer (warpgroup 0: the staging tile; warpgroup 1: the dS^T tile, free
     // from the end of the dQ_i MMA until the next dS^T store, which waits for this read: dstile_free),
     // one flat copy-engine reduce-add per warpgroup.  The rows come out of TMEM 32 at a time; with
     // `ds`, this warpgroup's packed dS^T of the next tile goes into the first 32 columns once read.
-    auto drain128 = [&](int it, bool with_ds, const uint32_t (&ds)[32]) -> bool {
-      if (!mbar_wait_warp(bars.dq_full(), it & 1, wc)) return false;
+    auto drain128 = [&](int it, bool with_ds, const uint32_t (&ds)[32]) {
+      wait(bars.dq_full(), it & 1);
       tc_fence_after();
       uint32_t v[32];
       tmem_ld32(tY + lane_bits + h * 64, v);
@@ -373,12 +379,11 @@ __global__ void __launch_bounds__(kKlBwdThreads, 1) kl_bwd_fused_kernel(const __
         bulk_reduce_add_f32(a.dq_acc + row0 * D, sbase + buf_off, C::STAGE_BYTES);
         tma_store_commit();
       }
-      return true;
     };
     // d = 64, dQ_i (lane = query row): this warpgroup reduces d columns [32h, 32h + 32) as one
     // [128 query][32 d] box written with the accumulator map's 128-byte swizzle, one tensor reduce-add.
-    auto drain64 = [&](int it) -> bool {
-      if (!mbar_wait_warp(bars.dq_full(), it & 1, wc)) return false;
+    auto drain64 = [&](int it) {
+      wait(bars.dq_full(), it & 1);
       tc_fence_after();
       uint32_t v[32];
       tmem_ld32(tY + lane_bits + h * 32, v);
@@ -397,13 +402,12 @@ __global__ void __launch_bounds__(kKlBwdThreads, 1) kl_bwd_fused_kernel(const __
         tma_reduce_add_2d(&a.tm_dqacc, box, 32 * h, bh * a.Nq_pad + (i_start + it) * kTileRows);
         tma_store_commit();
       }
-      return true;
     };
 
     const bool ragged_kv = k0 + kTileRows > a.Nk;  // block-uniform
     for (int it = 0; it < n; ++it) {
       const int qb = (i_start + it) * kTileRows + h * 64;  // first query column of this half
-      if (!(ok = mbar_wait_warp(bars.s_full(), it & 1, wc))) break;
+      wait(bars.s_full(), it & 1);
       tc_fence_after();
       // This tile's row values into shared memory (the barrier before: every thread of the warpgroup
       // has finished reading the previous tile's), and the next tile's fetched meanwhile.
@@ -452,7 +456,7 @@ __global__ void __launch_bounds__(kKlBwdThreads, 1) kl_bwd_fused_kernel(const __
       // Y (dQ_{i-1} follows dK_{i-1}, so that has also read dS^T_{i-1}); at d = 64 into the buffer of
       // this tile's parity, which dK_{i-2} read before S_i was issued.
       if (D == 128 && it > 0) {
-        if (!(ok = drain128(it - 1, true, pk))) break;
+        drain128(it - 1, true, pk);
       } else {
         tmem_st32(tmem + lane_bits + ds_store_col<D>(it, h), pk);
         tmem_wait_st();
@@ -460,7 +464,7 @@ __global__ void __launch_bounds__(kKlBwdThreads, 1) kl_bwd_fused_kernel(const __
         mbar_arrive(bars.pd_ready());  // dK_i may go
       }
       // dS^T into the shared tile for dQ_i, once dQ_{i-1} has read it
-      if (it > 0 && !(ok = mbar_wait_warp(bars.ds_empty(), (it - 1) & 1, wc))) break;
+      if (it > 0) wait(bars.ds_empty(), (it - 1) & 1);
       if constexpr (D == 128) {
         // The dS^T tile held warpgroup 1's dQ_{i-1} rows; the copy engine must have read them.
         if (it > 0 && h == 1) {
@@ -468,21 +472,21 @@ __global__ void __launch_bounds__(kKlBwdThreads, 1) kl_bwd_fused_kernel(const __
           named_bar_sync(2, 128);
           if (r == 0) mbar_arrive(bars.dstile_free());
         }
-        if (it > 0 && h == 0 && !(ok = mbar_wait_warp(bars.dstile_free(), (it - 1) & 1, wc))) break;
+        if (it > 0 && h == 0) wait(bars.dstile_free(), (it - 1) & 1);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u)
         st_shared_v4(ds_row + sw128_offset(r, u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       fence_proxy_async_smem();
       mbar_arrive(bars.dss_ready());  // dQ_i may go
-      if (D == 64 && it > 0 && !(ok = drain64(it - 1))) break;
+      if (D == 64 && it > 0) drain64(it - 1);
     }
-    if (ok && n > 0) {
+    if (n > 0) {
       if constexpr (D == 128) {
         const uint32_t none[32] = {};
-        ok = drain128(n - 1, false, none);
+        drain128(n - 1, false, none);
       } else {
-        ok = drain64(n - 1);
+        drain64(n - 1);
       }
     }
 
