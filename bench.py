@@ -713,6 +713,9 @@ def main() -> None:
     ap.add_argument("--workload", default=None)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--dq-mode", choices=("atomic", "deterministic"), default="atomic",
+                    help="attention workloads: dQ by reductions into the fp32 accumulator (attn_bwd) or by the "
+                         "query-tile kernel (attn_bwd_ex, deterministic)")
     ap.add_argument("--kl-dq-mode", choices=("atomic", "deterministic"), default="atomic",
                     help="attention-KL workloads: the one-pass backward (atomic dQ) or the repeatable two-kernel one")
     args = ap.parse_args()
@@ -759,22 +762,37 @@ def main() -> None:
     ws = torch.empty(exattn.workspace_size(w.B, w.H, w.Nq, w.d), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
+    deterministic = args.dq_mode == "deterministic"
+
+    def backward_call(stream_=None):
+        if deterministic:
+            return exattn.bwd_ex_raw(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, "deterministic", ws, stream=stream_)
+        return exattn.bwd_raw(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, ws, stream=stream_)
+
     def launch_step():
         """One step as a caller runs it: the forward, then the whole backward in one call."""
-        st = (exattn.fwd_raw(q, k, v, o, lse, w.causal, w.scale),
-              exattn.bwd_raw(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, ws))
+        st = (exattn.fwd_raw(q, k, v, o, lse, w.causal, w.scale), backward_call())
         if any(st):
             raise RuntimeError(f"C-ABI status {st}: {exattn.last_error()}")
 
     def launch(ev=None):
-        """The same step with each backward launch called on its own and an event after every kernel."""
+        """The same step with each backward launch called on its own and an event after every kernel (the
+        deterministic mode: its whole backward between two events, reported as the key/value-block step)."""
         st = [exattn.fwd_raw(q, k, v, o, lse, w.causal, w.scale)]
         if ev:
             ev[1].record(stream)
-        for i, name in enumerate(exattn.BWD_STEPS):
-            st.append(exattn.bwd_raw(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, ws, step=name))
+        if deterministic:
             if ev:
-                ev[2 + i].record(stream)
+                ev[2].record(stream)
+            st.append(backward_call())
+            if ev:
+                ev[3].record(stream)
+                ev[4].record(stream)
+        else:
+            for i, name in enumerate(exattn.BWD_STEPS):
+                st.append(exattn.bwd_raw(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, ws, step=name))
+                if ev:
+                    ev[2 + i].record(stream)
         if any(st):
             raise RuntimeError(f"C-ABI status {st}: {exattn.last_error()}")
 
@@ -838,8 +856,8 @@ def main() -> None:
 
     def compute_(sl, s):
         s1 = exattn.fwd_raw(sl["q"], sl["k"], sl["v"], sl["o"], sl["lse"], w.causal, w.scale, stream=s)
-        s2 = exattn.bwd_raw(sl["q"], sl["k"], sl["v"], sl["o"], sl["do"], sl["lse"], sl["dq"], sl["dk"], sl["dv"],
-                            w.causal, w.scale, sl["ws"], stream=s)
+        s2 = exattn.bwd_ex_raw(sl["q"], sl["k"], sl["v"], sl["o"], sl["do"], sl["lse"], sl["dq"], sl["dk"], sl["dv"],
+                               w.causal, w.scale, args.dq_mode, sl["ws"], stream=s)
         if s1 or s2:
             raise RuntimeError(exattn.last_error())
 
@@ -866,6 +884,7 @@ def main() -> None:
         "data": "synthetic: seeded normal Q,K (sigma %.2g), V, dO (sigma 1)" % w.sigma_qk,
         "config": config_dict(w, {"parallelism": "replicas" if world > 1 else "single GPU",
                                   "l2": "256 MiB flush write between timed steps, outside the CUDA events",
+                                  "dq_mode": args.dq_mode,
                                   "timing": "timed region = two passes of the steps: ms_per_step from CUDA "
                                             "events around each whole step (forward call, backward call); "
                                             "kernels_ms from the second pass, with an event after every kernel"}),
@@ -884,15 +903,18 @@ def main() -> None:
                    / 1e12 / pk["bf16_tflops"],
             "fwd_bwd": flops / (ms_per_step * 1e-3) / 1e12 / pk["bf16_tflops"],
         },
-        "roofline": {"kernel": "bwd_main_kernel (attn_bwd_kv_blocks)", "bound": "tensor", "achieved": achieved,
+        "roofline": {"kernel": ("bwd_main_kernel + pair_dq_kernel (attn_bwd_ex, deterministic dQ)" if deterministic
+                               else "bwd_main_kernel (attn_bwd_kv_blocks)"), "bound": "tensor", "achieved": achieved,
                      "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-                     "traffic": traffic_from_profile(f"{dominant}:{w.name}"),
+                     "traffic": None if deterministic else traffic_from_profile(f"{dominant}:{w.name}"),
                      "peak_kind": f"bf16 dense burst ({pk['source']})"},
         "cpu_baseline": ({k_: v_ for k_, v_ in cpu.items() if k_ != "seconds"} if cpu else None),
         "e2e": ({"value": job_throughput(flops, world, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                  "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "alone_ms_per_step": alone_ms,
                  "timing": E2E_NOTE} if args.e2e_steps else None),
-        "gpu_launches": 2 * 4 * args.steps,  # both passes of the timed region
+        # both passes of the timed region: the forward, then preprocess + key/value blocks + conversion
+        # (atomic) or preprocess + key/value blocks + query tiles (deterministic)
+        "gpu_launches": 2 * 4 * args.steps,
         "clocks": sampler.summary(t_wall0, t_wall1),
         "wall_s_timed_region": t_wall1 - t_wall0,
     }

@@ -23,6 +23,10 @@
 //    kernel (attn_bwd_dq.cu) produces dQ instead.
 // 3. bwd_dq_convert_kernel: dQ = scale * dQacc rounded to the input dtype.
 //
+// L2: the dQ accumulator's reduce-adds carry an evict-last hint and the loads of K_j, V_j and the
+// stores of dK, dV an evict-first one, so that what this kernel touches once does not push the
+// accumulator's lines out of L2 between the key blocks that add into them.
+//
 // Main-kernel warp roles (320 threads):
 //   warps 0-3   compute, query columns [0, 64) of each tile (thread = key row),
 //               and query rows [0, 64) of the dQ drain
@@ -204,9 +208,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       prefetch_tmap(&a.tm_q);
       prefetch_tmap(&a.tm_do);
       mbar_arrive_expect_tx(bars.kv_full(), 2 * C::TILE);
+      // K_j and V_j are read by this block only: their lines should not push out the dQ accumulator's
+      // or the query tiles' (which the other key blocks of the head read too).
+      const uint64_t once = l2_evict_first();
       for (int c = 0; c < C::NCH; ++c) {
-        tma_load_4d(sK + c * kChunkBytes, &a.tm_k, c * 64, k0, head, batch, bars.kv_full());
-        tma_load_4d(sV + c * kChunkBytes, &a.tm_v, c * 64, k0, head, batch, bars.kv_full());
+        tma_load_4d_hint(sK + c * kChunkBytes, &a.tm_k, c * 64, k0, head, batch, bars.kv_full(), once);
+        tma_load_4d_hint(sV + c * kChunkBytes, &a.tm_v, c * 64, k0, head, batch, bars.kv_full(), once);
       }
     }
     griddep_wait();
@@ -357,8 +364,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     // of its warpgroup meets the warpgroup's named barriers equally often and in the same order.  (A
     // warp that left early would arrive at the epilogue's barrier of the same number while the others
     // wait inside the loop, and the barrier would release both groups in the wrong rounds.)  What the
-    // warp computes after a failure is never stored: the epilogue checks the abort flag.  `ok` stays
-    // warp-uniform.
+    // warp computes after a failure is garbage: the epilogue skips the dK/dV stores (it checks the abort
+    // flag), and the dQ still added into the accumulator is marked invalid by the error word.  `ok`
+    // stays warp-uniform.
     bool ok = true;
     auto wait = [&](uint32_t bar, uint32_t parity) { ok = ok && mbar_wait_warp(bar, parity, wc); };
 
@@ -403,7 +411,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       named_bar_sync(1 + h, 128);
       if (r == 0) {
         const size_t row0 = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows + h * 64;
-        bulk_reduce_add_f32(a.dq_acc + row0 * D, sbase + buf_off, C::STAGE_BYTES);
+        bulk_reduce_add_f32_hint(a.dq_acc + row0 * D, sbase + buf_off, C::STAGE_BYTES, l2_evict_last());
         tma_store_commit();
       }
     };
@@ -432,7 +440,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         fence_proxy_async_smem();
         named_bar_sync(1 + h, 128);
         if (r == 0) {
-          tma_reduce_add_2d(&a.tm_dqacc, box, 32 * h, bh * a.Nq_pad + (i_start + it) * kTileRows);
+          tma_reduce_add_2d_hint(&a.tm_dqacc, box, 32 * h, bh * a.Nq_pad + (i_start + it) * kTileRows, l2_evict_last());
           tma_store_commit();
         }
       }
@@ -581,7 +589,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     named_bar_sync(1 + h, 128);
     if (ok && r == 0 && !*abort_flag) {
       const CUtensorMap* map = h ? &a.tm_dk : &a.tm_dv;
-      for (int ch = 0; ch < C::NCH; ++ch) tma_store_4d(map, stage + ch * kChunkBytes, ch * 64, k0, head, batch);
+      const uint64_t once = l2_evict_first();  // dK and dV are not read again here
+      for (int ch = 0; ch < C::NCH; ++ch) tma_store_4d_hint(map, stage + ch * kChunkBytes, ch * 64, k0, head, batch, once);
       tma_store_commit();
     }
     if (r == 0) tma_store_wait_all();  // this thread's stores and dQ reductions have completed
