@@ -218,9 +218,11 @@ __global__ void __launch_bounds__(kKlBwdThreads, 1) kl_bwd_fused_kernel(const __
       prefetch_tmap(&a.tm_qa);
       prefetch_tmap(&a.tm_qb);
       mbar_arrive_expect_tx(bars.kv_full(), 2 * C::TILE);
+      // both key tiles are read by this block only (evict-first); the dQ reduce-adds are evict-last
+      const uint64_t once = l2_evict_first();
       for (int c = 0; c < C::NCH; ++c) {
-        tma_load_4d(sKa + c * kChunkBytes, &a.tm_ka, c * 64, k0, head, batch, bars.kv_full());
-        tma_load_4d(sKb + c * kChunkBytes, &a.tm_kb, c * 64, k0, head, batch, bars.kv_full());
+        tma_load_4d_hint(sKa + c * kChunkBytes, &a.tm_ka, c * 64, k0, head, batch, bars.kv_full(), once);
+        tma_load_4d_hint(sKb + c * kChunkBytes, &a.tm_kb, c * 64, k0, head, batch, bars.kv_full(), once);
       }
       int issued = 0;
       for (int L = 0; L < 2 * n; ++L) {
@@ -335,7 +337,8 @@ __global__ void __launch_bounds__(kKlBwdThreads, 1) kl_bwd_fused_kernel(const __
     // warp does not leave the tile loop: it skips its remaining waits and runs on, so that every warp
     // of its warpgroup meets the warpgroup's named barriers equally often and in the same order (a warp
     // that left early would release a barrier of the same number for the wrong round).  What it computes
-    // after a failure is never stored: the epilogue checks the abort flag.  `ok` stays warp-uniform.
+    // after a failure is garbage: the epilogue skips the dK store (it checks the abort flag), and the dQ
+    // still added into the accumulator is marked invalid by the error word.  `ok` stays warp-uniform.
     bool ok = true;
     auto wait = [&](uint32_t bar, uint32_t parity) { ok = ok && mbar_wait_warp(bar, parity, wc); };
 
@@ -376,7 +379,7 @@ __global__ void __launch_bounds__(kKlBwdThreads, 1) kl_bwd_fused_kernel(const __
       named_bar_sync(1 + h, 128);
       if (r == 0) {
         const size_t row0 = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows + h * 64;
-        bulk_reduce_add_f32(a.dq_acc + row0 * D, sbase + buf_off, C::STAGE_BYTES);
+        bulk_reduce_add_f32_hint(a.dq_acc + row0 * D, sbase + buf_off, C::STAGE_BYTES, l2_evict_last());
         tma_store_commit();
       }
     };
@@ -399,7 +402,7 @@ __global__ void __launch_bounds__(kKlBwdThreads, 1) kl_bwd_fused_kernel(const __
       fence_proxy_async_smem();
       named_bar_sync(1 + h, 128);
       if (r == 0) {
-        tma_reduce_add_2d(&a.tm_dqacc, box, 32 * h, bh * a.Nq_pad + (i_start + it) * kTileRows);
+        tma_reduce_add_2d_hint(&a.tm_dqacc, box, 32 * h, bh * a.Nq_pad + (i_start + it) * kTileRows, l2_evict_last());
         tma_store_commit();
       }
     };
@@ -521,7 +524,7 @@ __global__ void __launch_bounds__(kKlBwdThreads, 1) kl_bwd_fused_kernel(const __
     }
     named_bar_sync(1 + h, 128);
     if (ok && mine && r == 0 && !*abort_flag) {
-      tma_store_4d(&a.tm_dk, stage, h * 64, k0, head, batch);
+      tma_store_4d_hint(&a.tm_dk, stage, h * 64, k0, head, batch, l2_evict_first());  // not read again here
       tma_store_commit();
     }
     if (r == 0) tma_store_wait_all();  // this thread's stores and dQ reductions have completed
