@@ -165,13 +165,19 @@ attn_status attn_fwd_splitkv_strided(const void* Q, attn_strides q_strides, cons
  * that minimises (waves of blocks over sm_count SMs, one resident block each)
  * x (key tiles per block + one tile of fixed cost), kept at 1 unless a split
  * wins by more than 2 %.  sm_count <= 0 asks the current device.  Returns 0
- * for invalid sizes (or when no device answers for sm_count <= 0).
+ * for invalid sizes (or when no device answers for sm_count <= 0).  The
+ * StreamKL summary names the split-K variant for small N_Q without a rule for
+ * the number of slices; this one is the library's own.
  */
 int attn_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int d, int sm_count);
 
 /*
  * Workspace bytes of attn_fwd_splitkv for num_splits (0: the library's choice
- * on the current device, which may need none).  0 for invalid arguments.
+ * on the current device, which may need none): fp32 partial O
+ * [splits][B*H][Nq][d] and partial base-2 LSE [splits][B*H][Nq], each part
+ * 256-byte aligned.  0 for invalid arguments.  The partial results are the
+ * per-slice state of the StreamKL summary's split-K variant; the pages do not
+ * size them (the caller owns all device memory).
  */
 size_t attn_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
 
@@ -210,7 +216,10 @@ attn_status attn_kl_fwd_splitkv(const void* Q1, const void* K1, const void* Q2, 
                                 float scale, attn_dtype dtype, int num_splits, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
-/* Workspace bytes of attn_kl_fwd_splitkv for num_splits (0: the library's choice, which may need none). */
+/* Workspace bytes of attn_kl_fwd_splitkv for num_splits (0: the library's
+ * choice, which may need none): the five running scalars of the StreamKL
+ * summary's Methodology 1, per slice and query row, in fp32.  The pages do not
+ * size them (the caller owns all device memory). */
 size_t attn_kl_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
 
 /*
@@ -235,7 +244,9 @@ attn_status attn_kl_bwd(const void* Q1, const void* K1, const void* Q2, const vo
 /*
  * Bytes of device workspace attn_kl_bwd_ex needs in the one-pass mode: an fp32
  * dQ accumulator [B,H,ceil(Nq/128)*128,d] plus three fp32 row vectors of that
- * padded length.  Returns 0 for invalid sizes.
+ * padded length.  Returns 0 for invalid sizes.  The accumulator is the
+ * buffer of the StreamKL summary's fused backward ("atomics while the buffer
+ * fits in L2"); the pages do not size it (the caller owns all device memory).
  */
 size_t attn_kl_bwd_workspace_size(int B, int H, int Nq, int d);
 
@@ -361,7 +372,10 @@ typedef enum {
  * cost between a CTA's blocks).  blocks_cap and begin_cap are the capacities
  * of the two caller-owned host arrays.  sm_count <= 0 takes the current
  * device's.  Returns -1 for sizes attn_fwd rejects, arrays too small, or a
- * device count that is needed and cannot be read.
+ * device count that is needed and cannot be read.  The pages parallelise the
+ * forward over batch x heads x row blocks ("Fast Transformer training with
+ * long sequences", attention parallelism); packing the blocks onto the SMs is
+ * this library's own scheduling, with no counterpart there.
  */
 int attn_fwd_schedule(int B, int H, int Nq, int Nk, int d, int causal, int sm_count, uint32_t* blocks,
                       int blocks_cap, int* begin, int begin_cap);
@@ -378,7 +392,9 @@ int attn_fwd_schedule(int B, int H, int Nq, int Nk, int d, int causal, int sm_co
  * 1); under a causal mask it is at least ceil(2*sm_count / ceil(Nk/128)); and
  * it is at most B*H.  sm_count <= 0 or l2_bytes = 0 take the current
  * device's values.  Returns -1 for sizes the backward rejects, or when a
- * device value is needed and cannot be read.
+ * device value is needed and cannot be read.  The rule serves the StreamKL
+ * summary's condition for atomics (the buffer in use fits in L2); the launch
+ * order itself has no counterpart on the pages.
  */
 int attn_bwd_head_group(int B, int H, int Nq, int Nk, int d, int causal, int sm_count, size_t l2_bytes);
 
@@ -389,7 +405,9 @@ int attn_bwd_head_group(int B, int H, int Nq, int Nk, int d, int causal, int sm_
  * 16 MiB to 512 MiB of accumulator, causal and not, d = 64 and 128): the
  * query-tile kernel recomputes S and dP, and with the launch order of
  * ATTN_DQ_ATOMIC the reductions' working set stays in L2.  Returns -1 for
- * invalid sizes.  Needs no device.
+ * invalid sizes.  Needs no device.  This is the choice the StreamKL summary
+ * makes in its backward (atomics while the buffer fits in L2, separate
+ * kernels under contention), measured on GB300.
  */
 int attn_bwd_auto_dq_mode(int B, int H, int Nq, int Nk, int d, int causal);
 
@@ -496,14 +514,17 @@ const char* attn_status_string(attn_status status);
 /*
  * Describes, on the calling host thread, the most recent failure inside this
  * library (which CUDA call failed and its error string); "" if none.  The
- * pointer stays valid until the thread's next call into the library.
+ * pointer stays valid until the thread's next call into the library.  A
+ * diagnostic of this library; the pages have no counterpart.
  */
 const char* attn_last_error(void);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns ATTN_ERR_TIMEOUT if a kernel's bounded wait expired since the
- * last check, ATTN_ERR_CUDA if synchronisation failed, else ATTN_OK.
+ * last check, ATTN_ERR_CUDA if synchronisation failed, else ATTN_OK.  A
+ * diagnostic of this library's failure detection; the pages have no
+ * counterpart.
  */
 attn_status attn_check_device_error(void* stream);
 

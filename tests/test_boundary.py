@@ -227,3 +227,35 @@ def test_kl_splitkv_rejects_bad_arguments(lib):
     assert call(4, ws=None) == 6
     assert call(4, nbytes=need - 1) == 6
     assert call(4, ws=FAKE + 8) == 3
+
+
+def _declaration_comments():
+    """(function name, the comment block directly above its declaration) for every function in the header;
+    declarations grouped under one comment share it."""
+    text = open(os.path.join(ROOT, "include", "exattn.h")).read()
+    out, last_comment, pos = [], "", 0
+    for m in re.finditer(r"/\*.*?\*/|\b(attn_[a-z_0-9]+)\s*\(", text, flags=re.S):
+        if m.group(0).startswith("/*"):
+            last_comment = m.group(0)
+        elif text[pos:m.start()].count(";") or not out or out[-1][0] != m.group(1):
+            # a declaration (not a call inside a comment): the name starts a statement
+            line_start = text.rfind("\n", 0, m.start()) + 1
+            if re.match(r"\s*(attn_status|size_t|int|const char\*)\s", text[line_start:m.start()]):
+                out.append((m.group(1), last_comment))
+        pos = m.end()
+    return out
+
+
+def test_every_entry_point_is_documented_with_its_source():
+    """Each declaration carries a comment that cites the pages (by title) or says the pages have no
+    counterpart, or points to the documented entry point it varies."""
+    pages = ("SparkAttention", "StreamKL", "Fast Transformer training", "CANN")
+    decls = _declaration_comments()
+    names = {n for n, _ in decls}
+    assert {"attn_fwd", "attn_bwd", "attn_bwd_noalloc", "attn_status_string"} <= names
+    for name, comment in decls:
+        assert comment, f"{name}: no comment"
+        comment = re.sub(r"\s*\n\s*\*?\s*", " ", comment)  # one line, without the leading stars
+        cites = any(p in comment for p in pages) or "no counterpart" in comment
+        refers = any(other in comment for other in names if other != name)
+        assert cites or refers, f"{name}: its comment neither cites a page nor refers to a documented entry point"
