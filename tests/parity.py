@@ -2,7 +2,12 @@
 and compare with the fp64 CPU oracle on the same seeded inputs.
 
 Tolerances (fixed by the method's numeric contract):
-  forward O  max-abs  <= 1e-2 (bf16) / 2e-3 (fp16)
+  forward O  max-abs  <= 1e-2 (bf16) / 2e-3 (fp16), for the value before its
+             final rounding to the 16-bit output: |O - O_ref| may exceed the
+             bound by at most half a unit in the last place of the output
+             format at |O| (the correctly rounded exact result itself is that
+             far away: 1.6e-2 for bf16 at |O| >= 4, where the stated bound
+             alone could not be met by any 16-bit output)
   LSE        max-abs  <= 1e-3
   dQ, dK, dV relative L2 <= 2e-2
 """
@@ -46,6 +51,14 @@ def rel_l2(a, b) -> float:
     return float(np.linalg.norm(np.asarray(a, np.float64) - b) / max(np.linalg.norm(b), floor))
 
 
+def half_ulp(x, dtype: str) -> np.ndarray:
+    """Half a unit in the last place of the 16-bit format (bf16: 8 significant bits, fp16: 11) at |x|:
+    the largest error of rounding to nearest there (subnormal spacing below the smallest normal)."""
+    mant, emin = (7, -126) if dtype == "bf16" else (10, -14)
+    e = np.floor(np.log2(np.maximum(np.abs(np.asarray(x, np.float64)), 2.0 ** emin)))
+    return 0.5 * 2.0 ** (e - mant)
+
+
 def check_fwd(w, got_o, got_lse, ref_o, ref_lse, what=""):
     # Rows that see no key (bottom-right mask, Nq > Nk): exactly O = 0 and LSE = -inf.
     empty = np.isneginf(ref_lse)
@@ -53,10 +66,20 @@ def check_fwd(w, got_o, got_lse, ref_o, ref_lse, what=""):
         assert np.isneginf(got_lse[empty]).all(), f"{what}: LSE of rows without keys is not -inf"
         assert (got_o[empty] == 0).all(), f"{what}: O of rows without keys is not 0"
         got_o, got_lse, ref_o, ref_lse = got_o[~empty], got_lse[~empty], ref_o[~empty], ref_lse[~empty]
-    err_o = float(np.abs(got_o - ref_o).max()) if ref_o.size else 0.0
-    err_l = float(np.abs(got_lse - ref_lse).max()) if ref_lse.size else 0.0
     assert np.isfinite(got_o).all() and np.isfinite(got_lse).all(), f"{what}: non-finite output"
-    assert err_o <= O_TOL[w.dtype], f"{what}: O max-abs {err_o:.3e} > {O_TOL[w.dtype]}"
+    diff = np.abs(got_o.astype(np.float64) - ref_o)
+    err_o = float(diff.max()) if ref_o.size else 0.0
+    err_l = float(np.abs(got_lse - ref_lse).max()) if ref_lse.size else 0.0
+    # The bound applies to the value before its final rounding to the output dtype: allow half an ulp of the
+    # output format on top (taken at the larger of |O| and |O_ref|, so a value rounded across a binade
+    # boundary is measured in the wider spacing).
+    slack = half_ulp(np.maximum(np.abs(got_o), np.abs(ref_o)), w.dtype)
+    over = diff - (O_TOL[w.dtype] + slack)
+    if ref_o.size and over.max() > 0:
+        i = np.unravel_index(int(np.argmax(over)), diff.shape)
+        raise AssertionError(f"{what}: O error {diff[i]:.3e} at {i} (|O_ref| = {abs(ref_o[i]):.4f}) exceeds "
+                             f"{O_TOL[w.dtype]} + half an ulp ({slack[i]:.2e}); plain max-abs {err_o:.3e}, "
+                             f"{int((diff > O_TOL[w.dtype]).sum())} elements above {O_TOL[w.dtype]}")
     assert err_l <= LSE_TOL, f"{what}: LSE max-abs {err_l:.3e} > {LSE_TOL}"
     return err_o, err_l
 
@@ -136,3 +159,52 @@ def oracle_cols_threaded(fn, Nq: int, Nk: int, causal, workers: int | None = Non
 def f64_head(t, b: int, h: int) -> np.ndarray:
     """One head of a [B, H, N, d] (or [B, H, N]) tensor as a contiguous fp64 array with B = H = 1 (exact)."""
     return np.ascontiguousarray(t[b:b + 1, h:h + 1].double().cpu().numpy())
+
+
+def _workers(workers=None) -> int:
+    return workers or max(1, min(16, len(os.sched_getaffinity(0))))
+
+
+def oracle_every_head(w, x, backward=True, workers=None):
+    """The full oracle on every (b, h) head, one single-threaded oracle call per head on a thread pool (the
+    oracle's C code runs without the GIL).  Arrays [B, H, N, d] (LSE [B, H, Nq]), like the GPU outputs."""
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+
+    def one(bh):
+        b, h = bh
+        s = {n: f64_head(x[n], b, h) for n in (("q", "k", "v", "do") if backward else ("q", "k", "v"))}
+        o, lse = oracle.attn_fwd(s["q"], s["k"], s["v"], w.causal, w.scale)
+        r = {"o": o[0, 0], "lse": lse[0, 0]}
+        if backward:
+            dq, dk, dv, _ = oracle.attn_bwd(s["q"], s["k"], s["v"], s["do"], w.causal, w.scale)
+            r.update(dq=dq[0, 0], dk=dk[0, 0], dv=dv[0, 0])
+        return r
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=_workers(workers)) as ex:
+        res = list(ex.map(one, heads))
+    return {key: np.stack([r[key] for r in res]).reshape((w.B, w.H) + res[0][key].shape) for key in res[0]}
+
+
+def oracle_one_head_split(w, x, b, h, workers=None):
+    """Every output of one (long) head, its query rows split over a thread pool.  O, LSE and dQ are row-local
+    (the row-sampled oracle calls on contiguous row ranges); dK and dV are sums over query rows (the
+    column-sampled call over every key row, on query-row parts of about equal work, summed)."""
+    s = {n: f64_head(x[n], b, h) for n in ("q", "k", "v", "do")}
+    parts = query_parts(w.Nq, w.Nk, w.causal, _workers(workers))
+    all_cols = np.arange(w.Nk, dtype=np.int64)
+
+    def rows_part(r):
+        rows = np.arange(r[0], r[1], dtype=np.int64)
+        o, lse = oracle.attn_fwd_rows(s["q"], s["k"], s["v"], w.causal, w.scale, rows)
+        dq, _ = oracle.attn_dq_rows(s["q"], s["k"], s["v"], s["do"], w.causal, w.scale, rows)
+        return o, lse, dq
+
+    def cols_part(r):
+        return oracle.attn_dkdv_cols(s["q"], s["k"], s["v"], s["do"], w.causal, w.scale, all_cols, q_range=r)
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=_workers(workers)) as ex:
+        row_res = list(ex.map(rows_part, parts))
+        col_res = list(ex.map(cols_part, parts))
+    return {"o": np.concatenate([r[0] for r in row_res]), "lse": np.concatenate([r[1] for r in row_res]),
+            "dq": np.concatenate([r[2] for r in row_res]), "dk": sum(c[0] for c in col_res),
+            "dv": sum(c[1] for c in col_res)}

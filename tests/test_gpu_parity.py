@@ -1,11 +1,14 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
 
-Small and ragged shapes are compared element by element over every output;
-the mid-size workloads on a subset of heads with the full oracle; the
-long-sequence workloads at full size on sampled query rows (O, LSE, dQ) and
-key rows (dK, dV) that the oracle evaluates one by one -- the last key rows
-and the rows of the first key blocks, which every query tile adds into under
-a causal mask -- plus gradient invariants that hold at any size.
+Small and ragged shapes are compared element by element over every output.
+The standard, encoder-decoder and long-sequence (8k) workloads are compared
+element by element over every head (one oracle call per head on a thread
+pool), and the two very-long-context (32k) workloads over their first and
+last heads (query rows split over threads).  Every head of the long workloads
+is also checked at full size on sampled query rows (O, LSE, dQ) and key rows
+(dK, dV) that the oracle evaluates one by one -- the last key rows and the
+rows of the first key blocks, which every query tile adds into under a
+causal mask -- plus gradient invariants that hold at any size.
 """
 import numpy as np
 import pytest
@@ -14,8 +17,8 @@ import torch
 import oracle
 from exact_head_attention_gb300 import workloads
 
-from parity import (check_fwd, check_grads, f64_head, heavy_cols, oracle_cols_threaded, oracle_heads, pick_heads,
-                    rel_l2, run_gpu, sample_rows)
+from parity import (check_fwd, check_grads, f64_head, heavy_cols, oracle_cols_threaded, oracle_every_head,
+                    oracle_heads, oracle_one_head_split, rel_l2, run_gpu, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -64,16 +67,47 @@ def test_tiny_workload_full(name):
 
 
 @pytest.mark.parametrize("name", ["self1k_bf16", "self1k_causal_bf16", "dec_self512_fp16", "dec_cross512x1024_fp16"])
-def test_midsize_workloads_on_head_subset(name):
+def test_midsize_workloads_every_head(name):
+    """The standard self-attention and encoder-decoder workloads in full: every output of every head against
+    the oracle (one oracle call per head, on a thread pool)."""
     w = W[name]
     x = workloads.make_inputs(w)
     got = run_gpu(w, x)
-    heads = pick_heads(w, 2)
-    ref = oracle_heads(w, x, heads)
-    sel = lambda a: np.stack([a[b, h] for b, h in heads])  # noqa: E731
-    check_fwd(w, sel(got["o"]), sel(got["lse"]), ref["o"], ref["lse"], name)
-    check_grads({k: sel(got[k]) for k in ("dq", "dk", "dv")}, ref, name)
+    ref = oracle_every_head(w, x)
+    check_fwd(w, got["o"], got["lse"], ref["o"], ref["lse"], name)
+    check_grads(got, ref, name)
     _check_invariants(w, x, got, name)
+
+
+def test_long_sequence_workload_every_element():
+    """The long-sequence workload (B=1, H=12, N=8192, d=128, causal, sigma 1.5) in full: every element of O,
+    LSE, dQ, dK and dV of all twelve heads against the oracle (one oracle call per head, on a thread pool),
+    in the launch configuration the benchmark times."""
+    w = W["long8k_causal_bf16"]
+    x = workloads.make_inputs(w)
+    got = run_gpu(w, x)
+    ref = oracle_every_head(w, x)
+    check_fwd(w, got["o"], got["lse"], ref["o"], ref["lse"], w.name)
+    errs = check_grads(got, ref, w.name)
+    # per head as well: a head whose gradients were wrong could hide in the 12-head norm
+    for h in range(w.H):
+        check_grads({k: got[k][0, h] for k in ("dq", "dk", "dv")}, {k: ref[k][0, h] for k in ("dq", "dk", "dv")},
+                    f"{w.name} head {h}")
+    assert max(errs.values()) <= 2e-2
+
+
+@pytest.mark.parametrize("name", ["ctx32k_d128_causal_bf16", "ctx32k_d64_causal_bf16"])
+def test_very_long_context_two_heads_every_element(name):
+    """The very-long-context workloads (B=1, H=8, N=32768, causal, d=128 and d=64): every element of the first
+    and the last head against the oracle, its query rows split over a thread pool; the other heads are
+    checked on sampled rows and key rows and through invariants (test_long_workloads_full_size_sampled)."""
+    w = W[name]
+    x = workloads.make_inputs(w)
+    got = run_gpu(w, x)
+    for (b, h) in [(0, 0), (w.B - 1, w.H - 1)]:
+        ref = oracle_one_head_split(w, x, b, h)
+        check_fwd(w, got["o"][b, h], got["lse"][b, h], ref["o"], ref["lse"], f"{name} head ({b},{h})")
+        check_grads({k: got[k][b, h] for k in ("dq", "dk", "dv")}, ref, f"{name} head ({b},{h})")
 
 
 def _check_invariants(w, x, got, what):

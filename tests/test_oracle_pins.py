@@ -390,3 +390,24 @@ def test_threaded_heavy_columns_equal_the_serial_oracle(causal):
     parts = query_parts(Nq, Nk, causal, 5)
     assert parts[0][0] == 0 and parts[-1][1] == Nq and all(a < b for a, b in parts)
     assert all(parts[i][1] == parts[i + 1][0] for i in range(len(parts) - 1))
+
+
+def test_threaded_whole_head_helpers_equal_the_plain_oracle():
+    """The GPU tests' whole-head oracle runs -- one oracle call per head on a thread pool, and one long head
+    split into query-row parts -- equal the plain single-call oracle (rows without keys included)."""
+    import sys
+    sys.path.insert(0, os.path.dirname(__file__))
+    from exact_head_attention_gb300 import workloads
+    from parity import oracle_every_head, oracle_one_head_split
+
+    for causal in (False, True, "bottom_right"):
+        w = workloads.custom(2, 3, 300, 260, 32, "bf16", causal)
+        x = workloads.make_inputs(w)
+        o, lse = oracle.attn_fwd(x["q"], x["k"], x["v"], causal, w.scale)
+        dq, dk, dv, _ = oracle.attn_bwd(x["q"], x["k"], x["v"], x["do"], causal, w.scale)
+        ref = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+        every = oracle_every_head(w, x, workers=3)
+        one = oracle_one_head_split(w, x, 1, 2, workers=5)
+        for key, want in ref.items():
+            np.testing.assert_array_equal(every[key], want)
+            np.testing.assert_allclose(one[key], want[1, 2], atol=1e-12)
