@@ -11,7 +11,7 @@ import torch
 import oracle
 from exact_head_attention_gb300 import exattn, workloads
 
-from parity import check_grads, f64_head, heavy_cols, oracle_cols_threaded, rel_l2, sample_rows
+from parity import check_grads, f64_head, heavy_cols, oracle_cols_threaded, oracle_every_head, rel_l2, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -88,6 +88,18 @@ def test_deterministic_long_workloads_sampled(name):
 
         dk_c, dv_c = oracle_cols_threaded(part, w.Nq, w.Nk, w.causal)
         check_grads({"dk": dk[b, h, cols], "dv": dv[b, h, cols]}, {"dk": dk_c, "dv": dv_c}, f"{name} head {bh}")
+
+
+def test_deterministic_long_sequence_workload_every_element():
+    """The deterministic mode on the long-sequence workload (B=1, H=12, N=8192, d=128, causal): every element
+    of dQ, dK and dV of all twelve heads against the oracle (one oracle call per head on a thread pool)."""
+    w = W["long8k_causal_bf16"]
+    x = workloads.make_inputs(w)
+    dq, dk, dv = (t.float().cpu().numpy() for t in _grads(w, x, "deterministic"))
+    ref = oracle_every_head(w, x)
+    for h in range(w.H):
+        check_grads({"dq": dq[0, h], "dk": dk[0, h], "dv": dv[0, h]},
+                    {k: ref[k][0, h] for k in ("dq", "dk", "dv")}, f"deterministic {w.name} head {h}")
 
 
 def test_auto_mode_is_the_atomic_path():

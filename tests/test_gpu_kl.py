@@ -16,6 +16,9 @@ import torch
 import oracle
 from exact_head_attention_gb300 import exattn, workloads
 
+import concurrent.futures
+import os
+
 from parity import f64_head, heavy_cols, oracle_cols_threaded, rel_l2, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -142,6 +145,48 @@ def test_kl_workload_full_size_sampled(mode, shape):
 
             rk = oracle_cols_threaded(part, w.Nq, w.Nk, w.causal)
             assert rel_l2(dk[b, h, cols], rk) <= GRAD_TOL, f"{train} dK rows {cols.tolist()} head {h}"
+
+
+def _kl_oracle_every_head(w, x):
+    """The KL oracle (forward, both backward settings) on every head, one head per thread."""
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+
+    def one(bh):
+        b, h = bh
+        a = tuple(f64_head(x[n], b, h) for n in ("q1", "k1", "q2", "k2"))
+        g = f64_head(x["g"], b, h)
+        out = dict(zip(("kl", "l1", "l2"), (t[0, 0] for t in oracle.kl_fwd(*a, w.causal, w.scale))))
+        for setting in (1, 2):
+            dq, dk = oracle.kl_bwd(*a, g, setting, w.causal, w.scale)
+            out[f"dq{setting}"], out[f"dk{setting}"] = dq[0, 0], dk[0, 0]
+        return out
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(16, len(os.sched_getaffinity(0))))) as ex:
+        res = list(ex.map(one, heads))
+    return {k: np.stack([r[k] for r in res]).reshape((w.B, w.H) + res[0][k].shape) for k in res[0]}
+
+
+def test_kl_workload_every_element():
+    """The KL workload (B=1, H=12, N=8192, d=128, causal) in full: KL, LSE1, LSE2 and, in both dQ modes and
+    both settings, every element of dQ and dK of all twelve heads against the oracle (one head per
+    thread)."""
+    w = workloads.WORKLOADS["kl8k_causal_bf16"]
+    x = workloads.make_kl_inputs(w)
+    d = _dev(x)
+    kl, l1, l2 = exattn.kl_forward(d["q1"], d["k1"], d["q2"], d["k2"], w.causal, w.scale)
+    grads = {(m, t): exattn.kl_backward(d["q1"], d["k1"], d["q2"], d["k2"], kl, l1, l2, d["g"], t, w.causal,
+                                         w.scale, dq_mode=m)
+             for m in MODES for t in ("student", "teacher")}
+    torch.cuda.synchronize()
+    assert exattn.check_device_error() == 0
+    ref = _kl_oracle_every_head(w, x)
+    _check_fwd(kl.cpu().numpy(), l1.cpu().numpy(), l2.cpu().numpy(), (ref["kl"], ref["l1"], ref["l2"]), w.name)
+    for (m, t), (dq, dk) in grads.items():
+        setting = 1 if t == "student" else 2
+        dq, dk = dq.float().cpu().numpy(), dk.float().cpu().numpy()
+        for h in range(w.H):
+            assert rel_l2(dq[0, h], ref[f"dq{setting}"][0, h]) <= GRAD_TOL, f"{m} {t} dQ head {h}"
+            assert rel_l2(dk[0, h], ref[f"dk{setting}"][0, h]) <= GRAD_TOL, f"{m} {t} dK head {h}"
 
 
 @pytest.mark.parametrize("shape,splits", [
