@@ -293,7 +293,7 @@ extern "C" int attn_fwd_schedule(int B, int H, int Nq, int Nk, int d, int causal
         cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return -1;
   }
-  if (causal == ATTN_MASK_NONE) return 0;
+  if (causal == ATTN_MASK_NONE || fwd_uses_tile_kernel(d, true, Nk)) return 0;
   const int nqb = (Nq + kFwdSubTiles * kTileRows - 1) / (kFwdSubTiles * kTileRows);
   const FwdSchedule* sch = persistent_schedule(B * H, nqb, Nq, Nk, causal_offset(causal, Nq, Nk), sm_count);
   if (!sch) return 0;

@@ -12,6 +12,11 @@ namespace exattn {
 constexpr int kTileRows = 128;   // query rows per MMA tile (tcgen05 M) and key rows per K/V tile
 constexpr int kFwdSubTiles = 2;  // query tiles per forward CTA (256 rows)
 
+// The causal forward at d = 64 over at most this many keys runs one 128-row query tile per CTA, two CTAs
+// per SM (fwd_tile_kernel) instead of 256-row blocks.
+constexpr int kTileKernelMaxKeys = 2048;
+inline bool fwd_uses_tile_kernel(int d, bool causal, int Nk) { return d == 64 && causal && Nk <= kTileKernelMaxKeys; }
+
 // Element strides of a [B][H][N][d] view whose d elements are contiguous.
 struct RowStrides {
   long long b, h, n;

@@ -366,10 +366,11 @@ typedef enum {
  * block (heaviest first) would leave SMs idle at the end, attn_fwd instead
  * runs one CTA per SM over lists of blocks that the host packs so that the
  * CTAs' work is even.  Returns the number of lists (CTAs), with the lists in
- * blocks[begin[i] .. begin[i+1]) for i < that number, or 0 when the plain
- * launch is used (no mask, one wave or less, more than 2048 blocks, or a
- * packing that would not shorten the busiest SM by 3 % after the hand-over
- * cost between a CTA's blocks).  blocks_cap and begin_cap are the capacities
+ * blocks[begin[i] .. begin[i+1]) for i < that number, or 0 when no lists
+ * are used: no mask; d = 64 with Nk <= 2048, where attn_fwd runs one 128-row
+ * query tile per CTA, two CTAs per SM; one wave or less; more than 2048
+ * blocks; or a packing that would not shorten the busiest SM by 3 % after the
+ * hand-over cost between a CTA's blocks.  blocks_cap and begin_cap are the capacities
  * of the two caller-owned host arrays.  sm_count <= 0 takes the current
  * device's.  Returns -1 for sizes attn_fwd rejects, arrays too small, or a
  * device count that is needed and cannot be read.  The pages parallelise the

@@ -57,7 +57,9 @@ def test_coarse_causal_grids_are_packed(shape):
     (1, 4, 8192, 8192, 128, True),      # 128 blocks: one wave
     (1, 8, 32768, 32768, 128, True),    # 6-7 blocks per SM: the launch order is already even
     (2, 16, 8192, 8192, 128, True),
-    (8, 16, 1024, 1024, 64, True),      # blocks of a few key tiles: the hand-over would cost more
+    (8, 16, 1024, 1024, 64, True),      # d = 64 over at most 2048 keys: one query tile per CTA, two per SM
+    (1, 12, 2048, 2048, 64, True),
+    (2, 8, 512, 2048, 64, "bottom_right"),
     (4, 16, 16384, 16384, 128, True),   # 4096 blocks: more than a list holds
 ], ids=str)
 def test_other_grids_keep_the_launch_order(shape):
