@@ -312,6 +312,29 @@ def test_packed_forward_blocks_without_keys():
         check_fwd(w, o[0, h, rows], lse[0, h, rows], o_r, lse_r, f"{w.name} head {h}")
 
 
+@pytest.mark.parametrize("shape", [(2, 3, 700, 300, 64, "fp16", "bottom_right"), (1, 2, 1500, 2048, 64, "bf16", True),
+                                   (3, 1, 257, 129, 64, "bf16", "bottom_right")],
+                         ids=["nq700_nk300_bottom_right", "nq1500_nk2048", "nq257_nk129_bottom_right"])
+def test_one_tile_forward_every_output(shape):
+    """The causal forward at d = 64 over at most 2048 keys runs one query tile per CTA, two CTAs per SM:
+    every output against the oracle, with O and LSE pre-filled with NaN.  With the bottom-right mask and
+    more queries than keys, whole query tiles see no key (their CTAs load nothing and write O = 0,
+    LSE = -inf) while the CTA beside them on the SM runs a normal tile."""
+    from exact_head_attention_gb300 import exattn
+    w = workloads.custom(*shape, index=38)
+    assert exattn.fwd_schedule(w.B, w.H, w.Nq, w.Nk, w.d, w.causal, sm_count=152) is None
+    x = workloads.make_inputs(w)
+    dev = torch.device("cuda")
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((w.B, w.H, w.Nq), float("nan"), device=dev)
+    assert exattn.fwd_raw(q, k, v, o, lse, w.causal, w.scale) == 0
+    torch.cuda.synchronize()
+    assert exattn.check_device_error() == 0
+    ref_o, ref_lse = oracle.attn_fwd(x["q"], x["k"], x["v"], w.causal, w.scale)
+    check_fwd(w, o.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_lse, w.name)
+
+
 def test_guard_bytes_untouched():
     """Writes stay inside the outputs: sentinel bytes around each output are unchanged."""
     from exact_head_attention_gb300 import exattn
