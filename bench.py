@@ -328,11 +328,13 @@ def traffic_from_profile(kernel_key: str) -> float | None:
 def kernel_source_sha() -> str:
     """Hash of what the headline kernels compile from, with comments and blank lines removed (a comment
     edit leaves the compiled kernels, and so the profiled traffic, unchanged): their translation units,
-    the device headers they include (fwd_schedule.h: the persistent forward's argument), and from
+    the device headers they include (fwd_schedule.h: the persistent forward's argument; fwd_tile.cuh: the
+    one-tile forward), and from
     kernels.h the argument structs they take and the integer constants (the other workloads' structs
     there do not change these kernels).  Host-only code is left out."""
     h = hashlib.sha256()
-    for f in ("attn_fwd.cu", "attn_bwd.cu", "ptx.cuh", "kernels.h", "softmax.cuh", "kv_order.cuh", "fwd_schedule.h"):
+    for f in ("attn_fwd.cu", "attn_bwd.cu", "ptx.cuh", "kernels.h", "softmax.cuh", "kv_order.cuh", "fwd_schedule.h",
+              "fwd_tile.cuh"):
         src = open(os.path.join(ROOT, "exact_head_attention_gb300", "csrc", f)).read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
         src = re.sub(r"//[^\n]*", "", src)

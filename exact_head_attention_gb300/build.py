@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libexattn.so")
 SOURCES = ["api.cu", "attn_fwd.cu", "fwd_schedule.cu", "attn_bwd.cu", "attn_bwd_dq.cu", "attn_splitkv.cu", "attn_kl.cu", "attn_kl_bwd.cu", "noalloc.cu"]
-HEADERS = ["ptx.cuh", "kernels.h", "softmax.cuh", "ds_ops.cuh", "kv_order.cuh", "fwd_schedule.h"]
+HEADERS = ["ptx.cuh", "kernels.h", "softmax.cuh", "ds_ops.cuh", "kv_order.cuh", "fwd_schedule.h", "fwd_tile.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -541,16 +541,17 @@ namespace {
 constexpr int kMaxSplits = 256;
 
 // Slices per query tile that minimise (waves of CTAs) x (key tiles per CTA + one tile of fixed cost),
-// with one slice CTA resident per SM.  1 means the plain forward is the better launch, which is always
-// the case once the query tiles alone fill the SMs.
-int choose_splits(long long bh, int Nq, int Nk, int sm_count) {
+// with `per_sm` slice CTAs resident per SM.  1 means the plain forward is the better launch, which is
+// always the case once the query tiles alone fill the SMs.
+int choose_splits(long long bh, int Nq, int Nk, int sm_count, int per_sm) {
   const long long base = bh * ((Nq + kTileRows - 1) / kTileRows);
   const int nkv = (Nk + kTileRows - 1) / kTileRows;
   if (base >= sm_count) return 1;
+  const long long slots = static_cast<long long>(sm_count) * per_sm;
   int best = 1;
   double best_cost = 0.0;
   for (int s = 1; s <= std::min(nkv, kMaxSplits); ++s) {
-    const long long waves = (base * s + sm_count - 1) / sm_count;
+    const long long waves = (base * s + slots - 1) / slots;
     const double cost = static_cast<double>(waves) * ((nkv + s - 1) / s + 1);
     if (s == 1 || cost < best_cost * 0.98) {  // a split must win clearly: it adds a merge pass
       best = s;
@@ -559,6 +560,10 @@ int choose_splits(long long bh, int Nq, int Nk, int sm_count) {
   }
   return best;
 }
+
+// Slice CTAs of the split-KV attention forward resident per SM: two at d = 64 (the one-tile kernel of
+// fwd_tile.cuh), one at d = 128.
+int split_blocks_per_sm(int d) { return d == 64 ? 2 : 1; }
 
 int device_sm_count() {
   int dev = 0, sms = 0;
@@ -581,7 +586,7 @@ attn_status fwd_split_impl(const void* Q, const RowStrides& qs, const void* K, c
     return ATTN_ERR_INVALID_ARG;
   if (num_splits == 0) {
     int sms = device_sm_count();
-    num_splits = choose_splits(static_cast<long long>(B) * H, Nq, Nk, sms > 0 ? sms : 1);
+    num_splits = choose_splits(static_cast<long long>(B) * H, Nq, Nk, sms > 0 ? sms : 1, split_blocks_per_sm(d));
     if (num_splits == 1) return fwd_impl(Q, qs, K, ks, V, vs, O, os, LSE, B, H, Nq, Nk, d, causal, scale, dtype, stream);
   }
   if (!workspace || workspace_bytes < split_workspace(B, H, Nq, d, num_splits)) return ATTN_ERR_WORKSPACE;
@@ -626,7 +631,7 @@ extern "C" int attn_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int d, 
   if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return 0;
   if (sm_count <= 0) sm_count = device_sm_count();
   if (sm_count <= 0) return 0;
-  return choose_splits(static_cast<long long>(B) * H, Nq, Nk, sm_count);
+  return choose_splits(static_cast<long long>(B) * H, Nq, Nk, sm_count, split_blocks_per_sm(d));
 }
 
 extern "C" size_t attn_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
@@ -894,7 +899,8 @@ extern "C" size_t attn_kl_fwd_splitkv_workspace_size(int B, int H, int Nq, int N
   if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128) || num_splits < 0 || num_splits > kMaxSplits)
     return 0;
   if (num_splits == 0) {
-    num_splits = attn_fwd_splitkv_num_splits(B, H, Nq, Nk, d, 0);
+    const int sms = device_sm_count();
+    num_splits = choose_splits(static_cast<long long>(B) * H, Nq, Nk, sms > 0 ? sms : 1, 1);
     if (num_splits <= 1) return 0;
   }
   return kl_split_workspace(B, H, Nq, num_splits);
@@ -911,7 +917,7 @@ extern "C" attn_status attn_kl_fwd_splitkv(const void* Q1, const void* K1, const
     attn_status st = check_common(B, H, Nq, Nk, d, causal, scale, dtype);
     if (st != ATTN_OK) return st;
     const int sms = device_sm_count();
-    num_splits = choose_splits(static_cast<long long>(B) * H, Nq, Nk, sms > 0 ? sms : 1);
+    num_splits = choose_splits(static_cast<long long>(B) * H, Nq, Nk, sms > 0 ? sms : 1, 1);
     if (num_splits == 1)
       return attn_kl_fwd(Q1, K1, Q2, K2, KL, LSE1, LSE2, B, H, Nq, Nk, d, causal, scale, dtype, stream);
   }

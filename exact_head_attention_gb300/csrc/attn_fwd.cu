@@ -40,6 +40,7 @@
 #include <cuda_fp16.h>
 
 #include "fwd_schedule.h"
+#include "fwd_tile.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "softmax.cuh"
@@ -404,206 +405,39 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel_persistent(const __
   fwd_body<D, CAUSAL, BF16, true>(a, sch.unit + b, e - b);
 }
 
-// ---------------------------------------------------------------------------------------------------
-// One 128-row query tile per CTA, two CTAs per SM: the forward of short sequences at d = 64.
-//
-// Where a head has few key tiles, a 256-row block's start (its first loads come from DRAM) and drain
-// (the epilogue, and a query tile that finishes early waiting for its partner at the teardown) are a
-// large share of its time, and with one CTA per SM nothing hides them.  Here a CTA holds one query tile
-// in 256 TMEM columns (S, with P packed over it, then O) and 80 KB of shared memory, so two CTAs share
-// an SM: one's start and drain overlap the other's products, and the tiles pack onto the SMs in finer
-// units.  The per-tile chain (S, online softmax, P V) is the two-tile kernel's, and so are the results
-// (the same arithmetic in the same order).
-//
-// Warp roles (256 threads, two warpgroups): warps 0-3 softmax (thread = query row = TMEM lane), warp 4
-// TMA producer, warp 5 MMA issuer and TMEM owner, warps 6-7 idle (they complete the control warpgroup).
-// Two CTAs of 256 threads launch with 128 registers a thread; setmaxnreg moves 80 of the control
-// warpgroup's to the softmax warpgroup (208 / 48), which holds a whole score row.  Issue order S_0 | PV_0 S_1 | PV_1 S_2 ...: S_{j+1} overwrites P_j
-// after PV_j has read it (one thread's MMAs run in order), and when the softmax of tile j+1 starts,
-// PV_j has completed, so O may be rescaled then.
-constexpr int kTileThreads = 256;
-constexpr uint32_t kTileRegsSoftmax = 208, kTileRegsControl = 48;
-static_assert(kTileRegsSoftmax + kTileRegsControl == 2 * 128, "register split must match the launch (2 CTAs of 256)");
-
-template <int D>
-struct TileCfg {
-  static constexpr int NCH = D / 64;
-  static constexpr uint32_t TILE = kTileRows * D * 2;
-  static constexpr int NS = 2;  // K and V ring depth (3 measured no faster)
-  static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = OFF_Q + TILE;
-  static constexpr uint32_t OFF_V = OFF_K + NS * TILE;
-  static constexpr uint32_t OFF_BAR = OFF_V + NS * TILE;
-  static constexpr int NBAR = 1 + 4 * NS + 7;  // the two-tile kernel's barrier layout (FwdBars), tile 0 only
-  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t BYTES = OFF_MISC + 16;
-  // No alignment slack (two CTAs must fit an SM): the dynamic shared memory base is checked at entry.
-  static constexpr uint32_t SMEM_ALLOC = BYTES;
-  static_assert(2 * (SMEM_ALLOC + 1024) <= 228 * 1024, "two CTAs per SM (1 KB of each CTA's is reserved)");
-};
-
+// One 128-row query tile per CTA, two CTAs per SM (fwd_tile.cuh): the causal forward of short sequences
+// at d = 64.  Where a head has few key tiles, a 256-row block's start (its first loads come from DRAM)
+// and drain (the epilogue, and a query tile that finishes early waiting for its partner at the
+// teardown) are a large share of its time, and with one CTA per SM nothing hides them.  Grid
+// (B*H, ceil(Nq/128)), heaviest causal tiles first.
 template <int D, bool CAUSAL, bool BF16>
-__global__ void __launch_bounds__(kTileThreads, 2) fwd_tile_kernel(const __grid_constant__ FwdArgs a) {
-  using C = TileCfg<D>;
-  constexpr int NS = C::NS;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const uint32_t sbase = smem_u32(smem_raw);
-  if (!smem_base_aligned(sbase, a.err_word)) return;
-  uint8_t* gbase = smem_raw;
-  const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
-  const FwdBars bars{sbase + C::OFF_BAR, NS};
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_MISC + 4);
-  const WaitCtx wc{abort_flag, a.err_word, a.timeout_ns};
-
+__global__ void __launch_bounds__(tile::kThreads, 2) fwd_tile_kernel(const __grid_constant__ FwdArgs a) {
   griddep_launch_dependents();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
-  const int head = bh % a.heads, batch = bh / a.heads;
-  const int q0 = (gridDim.y - 1 - blockIdx.y) * kTileRows;  // heaviest causal tiles first
+  tile::Work w;
+  w.head = bh % a.heads;
+  w.batch = bh / a.heads;
+  w.q0 = (gridDim.y - 1 - blockIdx.y) * kTileRows;
+  w.j0 = 0;
   const int nkv = (a.Nk + kTileRows - 1) / kTileRows;
-  const int coff = CAUSAL ? a.causal_off : 0;
-  int n = nkv;  // key tiles this query tile sees (causal: through the tile of its last row's last key)
+  w.n = nkv;  // key tiles the query tile sees (causal: through the tile of its last row's last key)
   if (CAUSAL) {
-    const int last_key = q0 + kTileRows - 1 + coff;
-    n = last_key < 0 ? 0 : min(nkv, last_key / kTileRows + 1);
+    const int last_key = w.q0 + kTileRows - 1 + a.causal_off;
+    w.n = last_key < 0 ? 0 : min(nkv, last_key / kTileRows + 1);
   }
-
-  if (threadIdx.x == 0) {
-    *abort_flag = 0u;
-    mbar_init(bars.q_full(), 1);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(bars.k_full(s), 1);
-      mbar_init(bars.k_empty(s), 1);
-      mbar_init(bars.v_full(s), 1);
-      mbar_init(bars.v_empty(s), 1);
-    }
-    mbar_init(bars.s_full(0), 1);
-    mbar_init(bars.p_full(0), kTileRows);
-    mbar_init(bars.o_full(0), 1);
-    mbar_init(bars.mma_done(), 1);
-    fence_mbar_init();
-  }
-  if (warp == 5) {
-    tmem_alloc(smem_u32(tmem_slot), 256);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp >= 4) {
-    regs_decrease<kTileRegsControl>();
-    if (warp == 4 && lane == 0 && n > 0) {
-      // ---------------------------------------------------------- producer
-      prefetch_tmap(&a.tm_q);
-      prefetch_tmap(&a.tm_k);
-      prefetch_tmap(&a.tm_v);
-      mbar_arrive_expect_tx(bars.q_full(), C::TILE);
-      for (int c = 0; c < C::NCH; ++c)
-        tma_load_4d(sQ + c * kChunkBytes, &a.tm_q, c * 64, q0, head, batch, bars.q_full());
-      int issued_k = 0, issued_v = 0;
-      for (int j = 0; j < n; ++j) {
-        const int s = j % NS;
-        const uint32_t ph = (j / NS) & 1;
-        if (!mbar_wait(bars.k_empty(s), ph ^ 1, wc)) break;
-        mbar_arrive_expect_tx(bars.k_full(s), C::TILE);
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(sK + s * C::TILE + c * kChunkBytes, &a.tm_k, c * 64, j * kTileRows, head, batch, bars.k_full(s));
-        ++issued_k;
-        if (!mbar_wait(bars.v_empty(s), ph ^ 1, wc)) break;
-        mbar_arrive_expect_tx(bars.v_full(s), C::TILE);
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(sV + s * C::TILE + c * kChunkBytes, &a.tm_v, c * 64, j * kTileRows, head, batch, bars.v_full(s));
-        ++issued_v;
-      }
-      // On abort, every load this thread issued must land before the CTA exits.
-      if (*abort_flag) {
-        for (int j = max(0, issued_k - NS); j < issued_k; ++j) mbar_drain(bars.k_full(j % NS), (j / NS) & 1, a.timeout_ns);
-        for (int j = max(0, issued_v - NS); j < issued_v; ++j) mbar_drain(bars.v_full(j % NS), (j / NS) & 1, a.timeout_ns);
-        mbar_drain(bars.q_full(), 0, a.timeout_ns);
-      }
-    } else if (warp == 5 && lane == 0 && n > 0) {
-      // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idS = idesc_f16(128, 128, BF16, false, false);
-      constexpr uint32_t idPV = idesc_f16(128, D, BF16, false, true);
-      constexpr uint32_t kTileLo = C::TILE >> 4;
-      const uint32_t q_lo = sdesc_lo(sQ, 16), k_lo = sdesc_lo(sK, 16), v_lo = sdesc_lo(sV, kChunkBytes);
-      auto issue_S = [&](int j) -> bool {
-        const int s = j % NS;
-        if (!mbar_wait(bars.k_full(s), (j / NS) & 1, wc)) return false;
-        tc_fence_after();
-        const uint32_t b_lo = k_lo + s * kTileLo;
-        mma_ss_lo<false>(tmem, q_lo, b_lo, idS);
-#pragma unroll
-        for (int k = 1; k < D / 16; ++k) {
-          const uint32_t off = ((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4;
-          mma_ss_lo<true>(tmem, q_lo + off, b_lo + off, idS);
-        }
-        mma_commit(bars.s_full(0));
-        mma_commit(bars.k_empty(s));
-        return true;
-      };
-      auto issue_PV = [&](int j) -> bool {
-        const int s = j % NS;
-        if (!mbar_wait(bars.v_full(s), (j / NS) & 1, wc)) return false;
-        if (!mbar_wait(bars.p_full(0), j & 1, wc)) return false;
-        tc_fence_after();
-        const uint32_t d = tmem + 128, b_lo = v_lo + s * kTileLo;
-        mma_ts_lo_rt(d, tmem, b_lo, idPV, j > 0 ? 1u : 0u);
-#pragma unroll
-        for (int k = 1; k < kTileRows / 16; ++k) mma_ts_lo<true>(d, tmem + k * 8, b_lo + k * (2048 >> 4), idPV);
-        mma_commit(bars.v_empty(s));
-        return true;
-      };
-      bool ok = mbar_wait(bars.q_full(), 0, wc);
-      if (ok) ok = issue_S(0);
-      for (int j = 0; ok && j < n; ++j) {
-        if (!(ok = issue_PV(j))) break;
-        if (j == n - 1) mma_commit(bars.o_full(0));
-        if (j + 1 < n && !(ok = issue_S(j + 1))) break;
-      }
-      // Every MMA issued above completes before TMEM can be released.
-      mma_commit(bars.mma_done());
-      mbar_drain(bars.mma_done(), 0, a.timeout_ns);
-    }
-  } else {
-    // ------------------------------------------------------------ softmax
-    regs_increase<kTileRegsSoftmax>();
-    const int r = warp * 32 + lane;  // row inside the tile = TMEM lane
-    const int row = q0 + r;
-    const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_bits, tO = tmem + 128 + lane_bits;
-    const float c_log2 = a.scale * 1.4426950408889634f;
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      if (!(ok = mbar_wait_warp(bars.s_full(0), j & 1, wc))) break;
-      tc_fence_after();
-      const bool need_mask = ((j + 1) * kTileRows > a.Nk) || (CAUSAL && j * kTileRows + kTileRows - 1 > q0 + coff);
-      const int lim = need_mask ? (CAUSAL ? min(a.Nk, row + coff + 1) : a.Nk) - j * kTileRows : kTileRows;
-      if (need_mask)
-        softmax_tile<D, true, BF16>(tS, tO, lim, c_log2, j == 0, m, l, [] {});
-      else
-        softmax_tile<D, false, BF16>(tS, tO, lim, c_log2, j == 0, m, l, [] {});
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bars.p_full(0));
-    }
-
-    // ------------------------------------------------------------ epilogue
-    // A row that saw no key gets O = 0 and LSE = -inf; a tile with no key tile at all loaded nothing.
-    if (ok && n > 0) ok = mbar_wait_warp(bars.o_full(0), 0, wc);
+  // O / l rounded to the dtype, staged in the dead Q tile with the tensor map's swizzle, one TMA store;
+  // a row that saw no key (l = 0) gets O = 0 and LSE = -inf.
+  auto epilogue = [&](bool ok, float m, float l, int r, uint32_t tO, uint32_t sQ, volatile uint32_t* abort_flag) {
+    using C = tile::Cfg<D>;
+    const int row = w.q0 + r;
     if (ok) {
-      tc_fence_after();
       const float inv_l = l > 0.f ? 1.0f / l : 0.f;
       if (row < a.Nq)
         a.lse[static_cast<size_t>(bh) * a.Nq + row] = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
 #pragma unroll
       for (int ch = 0; ch < C::NCH; ++ch) {
         uint32_t o[2][32];
-        if (n > 0) {
+        if (w.n > 0) {
           tmem_ld32(tO + ch * 64, o[0]);
           tmem_ld32(tO + ch * 64 + 32, o[1]);
           tmem_wait_ld();
@@ -620,26 +454,21 @@ __global__ void __launch_bounds__(kTileThreads, 2) fwd_tile_kernel(const __grid_
           const uint32_t w1 = pack2<BF16>(__uint_as_float(o[h][b + 2]) * inv_l, __uint_as_float(o[h][b + 3]) * inv_l);
           const uint32_t w2 = pack2<BF16>(__uint_as_float(o[h][b + 4]) * inv_l, __uint_as_float(o[h][b + 5]) * inv_l);
           const uint32_t w3 = pack2<BF16>(__uint_as_float(o[h][b + 6]) * inv_l, __uint_as_float(o[h][b + 7]) * inv_l);
-          st_shared_v4(sQ + ch * kChunkBytes + sw128_offset(r, u), w0, w1, w2, w3);  // Q is dead
+          st_shared_v4(sQ + ch * tile::kChunkBytes + sw128_offset(r, u), w0, w1, w2, w3);
         }
       }
       fence_proxy_async_smem();
     }
     named_bar_sync(1, 128);
-    if (ok && r == 0 && q0 < a.Nq && !*abort_flag) {
-      for (int ch = 0; ch < C::NCH; ++ch) tma_store_4d(&a.tm_o, sQ + ch * kChunkBytes, ch * 64, q0, head, batch);
+    if (ok && r == 0 && w.q0 < a.Nq && !*abort_flag) {
+      for (int ch = 0; ch < C::NCH; ++ch)
+        tma_store_4d(&a.tm_o, sQ + ch * tile::kChunkBytes, ch * 64, w.q0, w.head, w.batch);
       tma_store_commit();
       tma_store_wait_all();
     }
-  }
-
-  // ------------------------------------------------------------ teardown
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 5) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 256);
-  }
+  };
+  tile::run<D, CAUSAL, BF16>(&a.tm_q, &a.tm_k, &a.tm_v, w, a.Nk, a.causal_off, a.scale, a.err_word, a.timeout_ns,
+                             epilogue);
 }
 
 template <int D, bool CAUSAL, bool BF16>
@@ -651,13 +480,13 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   // each K/V tile once for two query tiles, measured as fast or faster.)
   if constexpr (D == 64 && CAUSAL) {
     if (fwd_uses_tile_kernel(D, CAUSAL, a.Nk)) {
-      using T = TileCfg<D>;
+      using T = tile::Cfg<D>;
       auto kern = fwd_tile_kernel<D, CAUSAL, BF16>;
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_ALLOC);
       if (e != cudaSuccess) return e;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
       if (e != cudaSuccess) return e;
-      kern<<<dim3(a.bh_count, (a.Nq + kTileRows - 1) / kTileRows, 1), kTileThreads, T::SMEM_ALLOC, stream>>>(a);
+      kern<<<dim3(a.bh_count, (a.Nq + kTileRows - 1) / kTileRows, 1), tile::kThreads, T::SMEM_ALLOC, stream>>>(a);
       return cudaGetLastError();
     }
   }

@@ -23,6 +23,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "fwd_tile.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "softmax.cuh"
@@ -274,6 +275,56 @@ __global__ void __launch_bounds__(kSplitThreads, 1) fwd_split_kernel(const __gri
   }
 }
 
+// The slice kernel at d = 64: one query tile and one slice of its key tiles per CTA, two CTAs per SM
+// (fwd_tile.cuh), so two online-softmax chains run per SM where fwd_split_kernel runs one.  The same
+// slices, the same per-slice results (O normalised by the slice's own sum, base-2 LSE) and the same merge.
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(tile::kThreads, 2) fwd_split_tile_kernel(const __grid_constant__ SplitArgs a) {
+  const int bh = blockIdx.x;
+  const int split = blockIdx.z;
+  tile::Work w;
+  w.head = bh % a.heads;
+  w.batch = bh / a.heads;
+  w.q0 = blockIdx.y * kTileRows;
+  const int nkv = (a.Nk + kTileRows - 1) / kTileRows;
+  int nvis = nkv;  // key tiles this query tile sees
+  if (CAUSAL) {
+    const int last_key = w.q0 + kTileRows - 1 + a.causal_off;
+    nvis = last_key < 0 ? 0 : min(nkv, last_key / kTileRows + 1);
+  }
+  // this block's slice [j0, j0 + n): slices differ in length by at most one tile
+  w.j0 = static_cast<int>(static_cast<long long>(split) * nvis / a.splits);
+  w.n = static_cast<int>(static_cast<long long>(split + 1) * nvis / a.splits) - w.j0;
+  auto epilogue = [&](bool ok, float m, float l, int r, uint32_t tO, uint32_t, volatile uint32_t*) {
+    if (!ok) return;  // warp-uniform
+    const int row = w.q0 + r;
+    const size_t prow = (static_cast<size_t>(split) * a.bh_count + bh) * a.Nq + row;
+    const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+    if (row < a.Nq) a.l_part[prow] = l > 0.f ? m + __log2f(l) : -INFINITY;
+    float4* dst = reinterpret_cast<float4*>(a.o_part + prow * D);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      if (w.n > 0) {
+        tmem_ld32(tO + c * 32, o);  // warp-collective: every lane loads, only real rows store
+        tmem_wait_ld();
+        reg_fence32(o);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+      }
+      if (row < a.Nq) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          dst[c * 8 + e] = make_float4(__uint_as_float(o[4 * e]) * inv_l, __uint_as_float(o[4 * e + 1]) * inv_l,
+                                       __uint_as_float(o[4 * e + 2]) * inv_l, __uint_as_float(o[4 * e + 3]) * inv_l);
+      }
+    }
+  };
+  tile::run<D, CAUSAL, BF16>(&a.tm_q, &a.tm_k, &a.tm_v, w, a.Nk, a.causal_off, a.scale, a.err_word, a.timeout_ns,
+                             epilogue);
+}
+
 // Merge of the slices, one warp per query row: lane holds d/32 consecutive columns.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fwd_combine_kernel(const __grid_constant__ SplitArgs a) {
@@ -327,12 +378,23 @@ __global__ void __launch_bounds__(256) fwd_combine_kernel(const __grid_constant_
 
 template <int D, bool CAUSAL, bool BF16>
 cudaError_t launch_split_t(const SplitArgs& a, cudaStream_t stream) {
-  using C = SplitCfg<D>;
-  auto kern = fwd_split_kernel<D, CAUSAL, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
-  if (e != cudaSuccess) return e;
   dim3 grid(a.bh_count, (a.Nq + kTileRows - 1) / kTileRows, a.splits);
-  kern<<<grid, kSplitThreads, C::BYTES, stream>>>(a);
+  cudaError_t e;
+  if constexpr (D == 64) {  // two slice CTAs per SM (the library's slice count assumes as much at d = 64)
+    using T = tile::Cfg<D>;
+    auto kern = fwd_split_tile_kernel<D, CAUSAL, BF16>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_ALLOC)) != cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+      return e;
+    kern<<<grid, tile::kThreads, T::SMEM_ALLOC, stream>>>(a);
+  } else {
+    using C = SplitCfg<D>;
+    auto kern = fwd_split_kernel<D, CAUSAL, BF16>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES)) != cudaSuccess) return e;
+    kern<<<grid, kSplitThreads, C::BYTES, stream>>>(a);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long rows = static_cast<long long>(a.bh_count) * a.Nq;
   fwd_combine_kernel<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(a);

@@ -162,9 +162,9 @@ attn_status attn_fwd_splitkv_strided(const void* Q, attn_strides q_strides, cons
 /*
  * The number of slices attn_fwd_splitkv uses for num_splits = 0: 1 when the
  * B*H*ceil(Nq/128) query tiles alone fill sm_count SMs; otherwise the count
- * that minimises (waves of blocks over sm_count SMs, one resident block each)
- * x (key tiles per block + one tile of fixed cost), kept at 1 unless a split
- * wins by more than 2 %.  sm_count <= 0 asks the current device.  Returns 0
+ * that minimises (waves of blocks over sm_count SMs, with two resident blocks
+ * per SM at d = 64 and one at d = 128) x (key tiles per block + one tile of
+ * fixed cost), kept at 1 unless a split wins by more than 2 %.  sm_count <= 0 asks the current device.  Returns 0
  * for invalid sizes (or when no device answers for sm_count <= 0).  The
  * StreamKL summary names the split-K variant for small N_Q without a rule for
  * the number of slices; this one is the library's own.
@@ -204,10 +204,11 @@ attn_status attn_kl_fwd(const void* Q1, const void* K1, const void* Q2, const vo
  * slice's five running scalars and a second kernel merges them (maxima
  * combined, sums and the weighted logit difference rescaled to the common
  * maxima).  Same results as attn_kl_fwd up to fp32 rounding.  num_splits:
- * 1..256, or 0 for the library's choice (attn_fwd_splitkv_num_splits; when it
- * is 1 this is exactly attn_kl_fwd and needs no workspace).  workspace: at
- * least attn_kl_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, num_splits) bytes,
- * 256-byte aligned, contents on entry irrelevant.  Errors as attn_kl_fwd, plus
+ * 1..256, or 0 for the library's choice (the rule of
+ * attn_fwd_splitkv_num_splits with one resident block per SM at either d;
+ * when it is 1 this is exactly attn_kl_fwd and needs no workspace).
+ * workspace: at least attn_kl_fwd_splitkv_workspace_size(B, H, Nq, Nk, d,
+ * num_splits) bytes, 256-byte aligned, contents on entry irrelevant.  Errors as attn_kl_fwd, plus
  * ATTN_ERR_INVALID_ARG for num_splits outside [0, 256] and ATTN_ERR_WORKSPACE
  * for a missing or small workspace.
  */

@@ -148,6 +148,26 @@ def test_splitkv_heuristic(lib):
         s = exattn.splitkv_num_splits(*shape, sm_count=152)
         assert 1 < s <= 256
     assert exattn.splitkv_num_splits(0, 1, 1, 1, 64, sm_count=152) == 0
+
+    def documented_rule(B, H, Nq, Nk, d, sms):
+        """(waves over sms SMs with two resident blocks at d = 64, one at d = 128) x (tiles per block + 1),
+        a split kept only when it wins by more than 2 %; 1 once the query tiles alone fill the SMs."""
+        base, nkv = B * H * -(-Nq // 128), -(-Nk // 128)
+        if base >= sms:
+            return 1
+        slots = sms * (2 if d == 64 else 1)
+        best, best_cost = 1, None
+        for s in range(1, min(nkv, 256) + 1):
+            cost = -(-(base * s) // slots) * (-(-nkv // s) + 1)
+            if s == 1 or cost < best_cost * 0.98:
+                best, best_cost = s, cost
+        return best
+
+    for shape in [(4, 16, 64, 16384, 64), (8, 12, 1, 32768, 128), (2, 3, 100, 5000, 64), (1, 8, 1, 524288, 128),
+                  (1, 1, 1, 65536, 64)]:
+        assert exattn.splitkv_num_splits(*shape, sm_count=152) == documented_rule(*shape, 152), shape
+    # the 64-query chunk over a 16k cache (d = 64): two slice blocks per SM
+    assert exattn.splitkv_num_splits(4, 16, 64, 16384, 64, sm_count=152) == 9
     # workspace: fp32 O and LSE of every slice, each 256-byte aligned
     rows = 3 * 8 * 12 * 1
     assert lib.attn_fwd_splitkv_workspace_size(8, 12, 1, 32768, 128, 3) == \
