@@ -1,18 +1,19 @@
 // One 128-row query tile per CTA, two CTAs per SM: the body shared by the forward of short causal
 // sequences at d = 64 (attn_fwd.cu) and the split-KV forward at d = 64 (attn_splitkv.cu).
 //
-// A CTA holds one query tile in 256 TMEM columns (S, with P packed over it, then O) and 80 KB of shared
-// memory, so two CTAs share an SM: one's start (its first loads come from DRAM) and drain overlap the
-// other's products, and two online-softmax chains run per SM where one CTA of the split-KV forward runs
-// one.  The per-tile chain (S, online softmax, P V; the two-tile forward's softmax step) gives the
-// two-tile kernel's results (the same arithmetic in the same order).
+// A CTA holds one query tile (d = 64) in 256 TMEM columns -- S [0, 128), O [128, 192) and P, packed
+// 16-bit, [192, 256) -- and 80 KB of shared memory, so two CTAs share an SM: one's start (its first
+// loads come from DRAM) and drain overlap the other's products, and two online-softmax chains run per
+// SM where one CTA of the split-KV forward runs one.  The per-tile step is the two-tile forward's online
+// softmax (the same arithmetic in the same order, so the same results), with P in columns of its own.
 //
 // Warp roles (256 threads, two warpgroups): warps 0-3 softmax (thread = query row = TMEM lane), warp 4
 // TMA producer, warp 5 MMA issuer and TMEM owner, warps 6-7 idle (they complete the control
 // warpgroup).  Two CTAs of 256 threads launch with 128 registers a thread; setmaxnreg moves 80 of the
 // control warpgroup's to the softmax warpgroup (208 / 48), which holds a whole score row.  Issue order
-// S_0 | PV_0 S_1 | PV_1 S_2 ...: S_{i+1} overwrites P_i after PV_i has read it (one thread's MMAs run
-// in order), and when the softmax of tile i+1 starts, PV_i has completed, so O may be rescaled then.
+// S_0 | S_1 PV_0 | S_2 PV_1 ...: S_{i+1} is issued as soon as the softmax warps hold S_i in registers
+// (s_used), so it overlaps their exponentials; PV_i once P_i is in TMEM (p_full).  Before the softmax
+// of tile i+1 rescales O or writes P_{i+1}, it waits for PV_i (pv_done).
 #pragma once
 
 #include <cstdint>
@@ -38,8 +39,9 @@ struct Cfg {
   static constexpr uint32_t OFF_K = OFF_Q + TILE;
   static constexpr uint32_t OFF_V = OFF_K + NS * TILE;
   static constexpr uint32_t OFF_BAR = OFF_V + NS * TILE;
-  // q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full, p_full, o_full, mma_done
-  static constexpr int NBAR = 1 + 4 * NS + 4;
+  // q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full, p_full, o_full, mma_done, s_used,
+  // pv_done
+  static constexpr int NBAR = 1 + 4 * NS + 6;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (4 B) + abort flag (4 B)
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   // No alignment slack (two CTAs must fit an SM): the dynamic shared memory base is checked at entry.
@@ -59,6 +61,8 @@ struct Bars {
   __device__ uint32_t p_full() const { return base + 8 * (2 + 4 * ns); }
   __device__ uint32_t o_full() const { return base + 8 * (3 + 4 * ns); }
   __device__ uint32_t mma_done() const { return base + 8 * (4 + 4 * ns); }
+  __device__ uint32_t s_used() const { return base + 8 * (5 + 4 * ns); }   // S is in the softmax's registers
+  __device__ uint32_t pv_done() const { return base + 8 * (6 + 4 * ns); }  // the last P V product has completed
 };
 
 // What one CTA computes: query tile q0 of head (head, batch) against key tiles [j0, j0 + n).
@@ -76,6 +80,7 @@ template <int D, bool CAUSAL, bool BF16, typename Epilogue>
 __device__ __forceinline__ void run(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                     const Work& w, int Nk, int causal_off, float scale, uint32_t* err_word,
                                     uint64_t timeout_ns, Epilogue&& epilogue) {
+  static_assert(D == 64, "S, O and a separate P fill the 256 TMEM columns only at d = 64");
   using C = Cfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -103,6 +108,8 @@ __device__ __forceinline__ void run(const CUtensorMap* tm_q, const CUtensorMap* 
     mbar_init(bars.p_full(), kTileRows);
     mbar_init(bars.o_full(), 1);
     mbar_init(bars.mma_done(), 1);
+    mbar_init(bars.s_used(), kTileRows);
+    mbar_init(bars.pv_done(), 1);
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -171,19 +178,21 @@ __device__ __forceinline__ void run(const CUtensorMap* tm_q, const CUtensorMap* 
         if (!mbar_wait(bars.v_full(s), (i / NS) & 1, wc)) return false;
         if (!mbar_wait(bars.p_full(), i & 1, wc)) return false;
         tc_fence_after();
-        const uint32_t d = tmem + 128, b_lo = v_lo + s * kTileLo;
-        mma_ts_lo_rt(d, tmem, b_lo, idPV, i > 0 ? 1u : 0u);
+        const uint32_t d = tmem + 128, pa = tmem + 192, b_lo = v_lo + s * kTileLo;
+        mma_ts_lo_rt(d, pa, b_lo, idPV, i > 0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 1; k < kTileRows / 16; ++k) mma_ts_lo<true>(d, tmem + k * 8, b_lo + k * (2048 >> 4), idPV);
+        for (int k = 1; k < kTileRows / 16; ++k) mma_ts_lo<true>(d, pa + k * 8, b_lo + k * (2048 >> 4), idPV);
         mma_commit(bars.v_empty(s));
+        mma_commit(bars.pv_done());
         return true;
       };
       bool ok = mbar_wait(bars.q_full(), 0, wc);
       if (ok) ok = issue_S(0);
       for (int i = 0; ok && i < n; ++i) {
+        // S_{i+1} overwrites S_i once the softmax warps hold S_i in registers
+        if (i + 1 < n && !((ok = mbar_wait(bars.s_used(), i & 1, wc)) && (ok = issue_S(i + 1)))) break;
         if (!(ok = issue_PV(i))) break;
         if (i == n - 1) mma_commit(bars.o_full());
-        if (i + 1 < n && !(ok = issue_S(i + 1))) break;
       }
       // Every MMA issued above completes before TMEM can be released.
       mma_commit(bars.mma_done());
@@ -195,7 +204,7 @@ __device__ __forceinline__ void run(const CUtensorMap* tm_q, const CUtensorMap* 
     const int r = warp * 32 + lane;  // row inside the tile = TMEM lane
     const int row = w.q0 + r;        // query index inside the head
     const uint32_t lane_bits = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_bits, tO = tmem + 128 + lane_bits;
+    const uint32_t tS = tmem + lane_bits, tO = tmem + 128 + lane_bits, tP = tmem + 192 + lane_bits;
     const float c_log2 = scale * 1.4426950408889634f;
     const int coff = CAUSAL ? causal_off : 0;
     float m = -INFINITY, l = 0.f;
@@ -207,13 +216,23 @@ __device__ __forceinline__ void run(const CUtensorMap* tm_q, const CUtensorMap* 
       const int j = w.j0 + i;
       const bool need_mask = ((j + 1) * kTileRows > Nk) || (CAUSAL && j * kTileRows + kTileRows - 1 > w.q0 + coff);
       const int lim = need_mask ? (CAUSAL ? min(Nk, row + coff + 1) : Nk) - j * kTileRows : kTileRows;
+      const auto s_read = [&] {
+        tc_fence_before();
+        mbar_arrive(bars.s_used());  // S_{i+1} may overwrite S
+      };
+      // PV_{i-1} reads P and adds into O: it must have completed before O is rescaled or P rewritten.
+      const auto pv_finished = [&] {
+        if (i > 0 && !mbar_wait_warp(bars.pv_done(), (i - 1) & 1, wc)) ok = false;
+        tc_fence_after();
+      };
       if (need_mask)
-        softmax_tile<D, true, BF16>(tS, tO, lim, c_log2, i == 0, m, l, [] {});
+        softmax_tile_to<D, true, BF16>(tS, tP, tO, lim, c_log2, i == 0, m, l, s_read, pv_finished, pv_finished);
       else
-        softmax_tile<D, false, BF16>(tS, tO, lim, c_log2, i == 0, m, l, [] {});
+        softmax_tile_to<D, false, BF16>(tS, tP, tO, lim, c_log2, i == 0, m, l, s_read, pv_finished, pv_finished);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bars.p_full());
+      if (!ok) break;
     }
     if (ok && n > 0) ok = mbar_wait_warp(bars.o_full(), 0, wc);
     if (ok) tc_fence_after();

@@ -19,15 +19,22 @@ namespace exattn {
 // columns at or past `lim` count as -inf.  The exponent argument and the sums use paired fp32
 // instructions.  `before_rescale()` runs (warp-uniformly) before O is read for a rescale: a caller
 // whose previous P V product may still be in flight waits for it there.
-template <int D, bool MASKED, bool BF16, typename BeforeRescale>
-__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int lim, float c_log2, bool first, float& m,
-                                             float& l, BeforeRescale&& before_rescale) {
+//
+// softmax_tile_to is the same step with P written to its own 64 TMEM columns at tP instead of over S,
+// and two more warp-uniform hooks: `after_load()` once every score is in registers (S may then be
+// overwritten by the next score product), and `before_p()` before the first packed column of P is
+// written (a caller whose previous P V product may still read the P columns waits there).
+template <int D, bool MASKED, bool BF16, typename AfterLoad, typename BeforeRescale, typename BeforeP>
+__device__ __forceinline__ void softmax_tile_to(uint32_t tS, uint32_t tP, uint32_t tO, int lim, float c_log2,
+                                                bool first, float& m, float& l, AfterLoad&& after_load,
+                                                BeforeRescale&& before_rescale, BeforeP&& before_p) {
   uint32_t sr[4][32];
 #pragma unroll
   for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
   tmem_wait_ld();
 #pragma unroll
   for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
+  after_load();
   if constexpr (MASKED) {
 #pragma unroll
     for (int c = 0; c < 4; ++c)
@@ -63,6 +70,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int lim, 
       if (need) m = m_new;
     }
   }
+  before_p();
   const float ms = (m == -INFINITY) ? 0.f : m;
   const uint64_t c2 = f2_pack(c_log2, c_log2), nm2 = f2_pack(-ms, -ms);
   uint64_t acc[4];
@@ -82,13 +90,19 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int lim, 
       acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
       pk[i] = pack2<BF16>(p0, p1);
     }
-    tmem_st32(tS + h * 32, pk);
+    tmem_st32(tP + h * 32, pk);
   }
   float s0, s1, s2, s3;
   f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
   (void)s2;
   (void)s3;
   l += s0 + s1;
+}
+
+template <int D, bool MASKED, bool BF16, typename BeforeRescale>
+__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int lim, float c_log2, bool first, float& m,
+                                             float& l, BeforeRescale&& before_rescale) {
+  softmax_tile_to<D, MASKED, BF16>(tS, tS, tO, lim, c_log2, first, m, l, [] {}, before_rescale, [] {});
 }
 
 }  // namespace exattn
