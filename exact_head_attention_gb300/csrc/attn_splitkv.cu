@@ -10,8 +10,11 @@
 // slices of every query row:
 //     L = log2 sum_s 2^{L_s},  O = sum_s 2^{L_s - L} O_s,  LSE = L ln 2,
 // exact up to rounding (a slice that saw no key has L_s = -inf and weight 0).
+// The merge is a dependent launch: it starts while the last slice blocks run
+// and waits for the slice kernel before it reads anything.
 //
-// Warp roles of the slice kernel (192 threads):
+// At d = 64 the slices run on the one-tile body of fwd_tile.cuh (two slice
+// blocks per SM).  At d = 128, warp roles of the slice kernel (192 threads):
 //   warps 0-3  softmax warpgroup (thread = query row = TMEM lane)
 //   warp  4    TMA producer: Q once, then K_j / V_j into NS-deep rings
 //   warp  5    MMA issuer (one thread) and TMEM owner
@@ -68,6 +71,9 @@ struct SplitBars {
 
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(kSplitThreads, 1) fwd_split_kernel(const __grid_constant__ SplitArgs a) {
+  // The merge kernel is a dependent launch: it may start once every slice block is running, and waits
+  // for this kernel to finish before it reads the slices.
+  griddep_launch_dependents();
   using C = SplitCfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -280,6 +286,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) fwd_split_kernel(const __gri
 // slices, the same per-slice results (O normalised by the slice's own sum, base-2 LSE) and the same merge.
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(tile::kThreads, 2) fwd_split_tile_kernel(const __grid_constant__ SplitArgs a) {
+  griddep_launch_dependents();  // the merge kernel may start; it waits before it reads the slices
   const int bh = blockIdx.x;
   const int split = blockIdx.z;
   tile::Work w;
@@ -328,6 +335,7 @@ __global__ void __launch_bounds__(tile::kThreads, 2) fwd_split_tile_kernel(const
 // Merge of the slices, one warp per query row: lane holds d/32 consecutive columns.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fwd_combine_kernel(const __grid_constant__ SplitArgs a) {
+  griddep_wait();  // a dependent launch: the slices are complete once the slice kernel has finished
   constexpr int V = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long rows = static_cast<long long>(a.bh_count) * a.Nq;
@@ -396,9 +404,19 @@ cudaError_t launch_split_t(const SplitArgs& a, cudaStream_t stream) {
     kern<<<grid, kSplitThreads, C::BYTES, stream>>>(a);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // The merge as a dependent launch (programmatic stream serialisation): its launch overlaps the slice
+  // kernel's last blocks.
   const long long rows = static_cast<long long>(a.bh_count) * a.Nq;
-  fwd_combine_kernel<D, BF16><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fwd_combine_kernel<D, BF16>, a);
 }
 
 }  // namespace
