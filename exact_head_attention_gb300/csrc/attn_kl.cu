@@ -77,8 +77,8 @@ __device__ __forceinline__ float base_of(float m) { return m == -INFINITY ? 0.f 
 // student scores from TMEM twice (tile maxima, then sums), rescales l_a, acc (by the teacher's max
 // change) and l_b (the student's), and adds
 //     l_a += sum exp2(s_a c - m_a),  l_b += sum exp2(s_b c - m_b),  acc += sum exp2(s_a c - m_a) (s_a - s_b)
-// (c = scale log2 e; acc in raw score units).  With MASKED, columns at or past `lim` take no part.  The
-// two distributions' exponent arguments and sums travel as fp32 pairs.
+// (c = scale log2 e; acc in raw score units).  With MASKED, columns at or past `lim` take no part.
+// Neighbouring columns travel as fp32 pairs.
 template <bool MASKED>
 __device__ __forceinline__ void kl_tile(uint32_t tA, uint32_t tB, int lim, float c_log2, float& ma, float& mb,
                                         float& la, float& lb, float& acc) {
@@ -109,9 +109,12 @@ __device__ __forceinline__ void kl_tile(uint32_t tA, uint32_t tB, int lim, float
   lb *= alpha_b;
   ma = na;
   mb = nb;
-  const uint64_t c2 = f2_pack(c_log2, c_log2), nbase = f2_pack(-base_of(ma), -base_of(mb));
-  uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};  // (l_a, l_b) partial sums
-  float ac2[2] = {0.f, 0.f};
+  // Pairs of neighbouring columns of one distribution travel together: (s[2p], s[2p+1]) of the teacher
+  // and of the student each form one fp32 pair, so the exponent arguments, the two sums, the score
+  // difference and the weighted difference take one paired instruction per two columns.
+  const uint64_t c2 = f2_pack(c_log2, c_log2);
+  const uint64_t na2 = f2_pack(-base_of(ma), -base_of(ma)), nb2 = f2_pack(-base_of(mb), -base_of(mb));
+  uint64_t la2 = f2_pack(0.f, 0.f), lb2 = f2_pack(0.f, 0.f), ac2 = f2_pack(0.f, 0.f);
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
     uint32_t va[32], vb[32];
@@ -121,23 +124,37 @@ __device__ __forceinline__ void kl_tile(uint32_t tA, uint32_t tB, int lim, float
     reg_fence32(va);
     reg_fence32(vb);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float sa = __uint_as_float(va[i]), sb = __uint_as_float(vb[i]);
-      float xa2, xb2;
-      f2_unpack(f2_fma(f2_pack(sa, sb), c2, nbase), xa2, xb2);
-      float ea = ex2_approx(xa2), eb = ex2_approx(xb2), df = sa - sb;
+    for (int p = 0; p < 16; ++p) {
+      const uint64_t a2 = f2_pack(__uint_as_float(va[2 * p]), __uint_as_float(va[2 * p + 1]));
+      const uint64_t b2 = f2_pack(__uint_as_float(vb[2 * p]), __uint_as_float(vb[2 * p + 1]));
+      float xa0, xa1, xb0, xb1;
+      f2_unpack(f2_fma(a2, c2, na2), xa0, xa1);
+      f2_unpack(f2_fma(b2, c2, nb2), xb0, xb1);
+      float ea0 = ex2_approx(xa0), ea1 = ex2_approx(xa1), eb0 = ex2_approx(xb0), eb1 = ex2_approx(xb1);
+      uint64_t df2 = f2_sub(a2, b2);
       if constexpr (MASKED) {
-        if (c * 32 + i >= lim) ea = eb = df = 0.f;
+        const int col = c * 32 + 2 * p;
+        if (col >= lim || col + 1 >= lim) {  // masked columns take no part (their difference may be NaN)
+          float d0, d1;
+          f2_unpack(df2, d0, d1);
+          if (col >= lim) ea0 = eb0 = d0 = 0.f;
+          if (col + 1 >= lim) ea1 = eb1 = d1 = 0.f;
+          df2 = f2_pack(d0, d1);
+        }
       }
-      sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(ea, eb));
-      ac2[i & 1] = fmaf(ea, df, ac2[i & 1]);
+      const uint64_t e_a = f2_pack(ea0, ea1);
+      la2 = f2_add(la2, e_a);
+      lb2 = f2_add(lb2, f2_pack(eb0, eb1));
+      ac2 = f2_fma(e_a, df2, ac2);
     }
   }
-  float sa_, sb_;
-  f2_unpack(f2_add(sum2[0], sum2[1]), sa_, sb_);
-  la += sa_;
-  lb += sb_;
-  acc += ac2[0] + ac2[1];
+  float a0, a1, b0, b1, d0, d1;
+  f2_unpack(la2, a0, a1);
+  f2_unpack(lb2, b0, b1);
+  f2_unpack(ac2, d0, d1);
+  la += a0 + a1;
+  lb += b0 + b1;
+  acc += d0 + d1;
 }
 
 // SPLIT: the grid's z dimension divides the key tiles a query tile sees into a.splits contiguous
