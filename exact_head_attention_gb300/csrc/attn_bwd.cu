@@ -511,20 +511,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       reg_fence32(s[0]);
       reg_fence32(s[1]);
       // dS^T = P^T o (dP^T - D), into the half's last 32 columns of X and into the shared dS^T tile.
+      // Neighbouring query columns travel as fp32 pairs (the dP^T registers hold them side by side).
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
         const float4 d4 = *reinterpret_cast<const float4*>(dsum + c);
-        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-        float ds[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 4; e += 2) {
           const int col = c + e;
-          const float pv = (col & 1) ? unpack_hi<BF16>(pp[col >> 1]) : unpack_lo<BF16>(pp[col >> 1]);
-          ds[e] = pv * (__uint_as_float(s[col >> 5][col & 31]) - dv[e]);
+          const uint64_t dp2 = f2_pack(__uint_as_float(s[col >> 5][col & 31]), __uint_as_float(s[col >> 5][(col + 1) & 31]));
+          const uint64_t d2 = e ? f2_pack(d4.z, d4.w) : f2_pack(d4.x, d4.y);
+          const uint64_t p2 = f2_pack(unpack_lo<BF16>(pp[col >> 1]), unpack_hi<BF16>(pp[col >> 1]));
+          float ds0, ds1;
+          f2_unpack(f2_mul(p2, f2_sub(dp2, d2)), ds0, ds1);
+          pk[col >> 1] = pack2<BF16>(ds0, ds1);
         }
-        pk[c >> 1] = pack2<BF16>(ds[0], ds[1]);
-        pk[(c >> 1) + 1] = pack2<BF16>(ds[2], ds[3]);
       }
       mbar_arrive(bars.rowv_empty(rs));
       tmem_st32(tX + lane_bits + h * 64 + 32, pk);
