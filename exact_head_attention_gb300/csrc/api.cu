@@ -377,7 +377,7 @@ attn_status bwd_steps(const void* Q, const void* K, const void* V, const void* O
   a.sdo = vw.dout;
   a.sdq = vw.dq;
   a.dq_acc = reinterpret_cast<float*>(ws);
-  a.lse2 = reinterpret_cast<float*>(ws + align256(rows * d * sizeof(float)));
+  a.nlse2 = reinterpret_cast<float*>(ws + align256(rows * d * sizeof(float)));
   a.dsum = reinterpret_cast<float*>(ws + align256(rows * d * sizeof(float)) + align256(rows * sizeof(float)));
   a.err_word = ds->err_word;
   a.bh_count = bh;

@@ -1,9 +1,9 @@
 // Fused attention backward for sm_103a: three launches on one stream.
 //
 // 1. bwd_pre_kernel: D_q = rowsum(dO o O) in fp32 (SparkAttention Figure 9,
-//    "dPsum"), LSE converted to base 2 (padding rows get +inf so that their
-//    recomputed probabilities are exactly 0), and the fp32 dQ accumulator
-//    zeroed.
+//    "dPsum"), LSE converted to base 2 and stored negated, the additive term of
+//    the exponent (padding rows get -inf so that their recomputed
+//    probabilities are exactly 0), and the fp32 dQ accumulator zeroed.
 // 2. bwd_main_kernel: one CTA per 128-row key/value block of one (batch,
 //    head) -- the backward pass is parallel over blocks of columns of the
 //    attention matrix ("Fast Transformer training with long sequences",
@@ -79,7 +79,7 @@ struct BwdCfg {
   static constexpr uint32_t OFF_DS = OFF_V + TILE;
   static constexpr uint32_t OFF_RING = OFF_DS + PT;
   static constexpr uint32_t OFF_STAGE = OFF_RING + NR * TILE;
-  // two slots of the query tile's row vectors: 128 base-2 LSE then 128 D values (fp32)
+  // two slots of the query tile's row vectors: 128 negated base-2 LSE then 128 D values (fp32)
   static constexpr uint32_t OFF_ROWV = OFF_STAGE + STAGE_BYTES;
   static constexpr uint32_t ROWV_BYTES = 2 * 128 * 4;
   static constexpr uint32_t OFF_BAR = OFF_ROWV + 2 * ROWV_BYTES;
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
           if (!mbar_wait(bars.rowv_empty(rs), ((it >> 1) & 1) ^ 1, wc)) break;
           mbar_arrive_expect_tx(bars.rowv_full(rs), C::ROWV_BYTES);
           const size_t off = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows;
-          bulk_load(sRowv + rs * C::ROWV_BYTES, a.lse2 + off, 512, bars.rowv_full(rs));
+          bulk_load(sRowv + rs * C::ROWV_BYTES, a.nlse2 + off, 512, bars.rowv_full(rs));
           bulk_load(sRowv + rs * C::ROWV_BYTES + 512, a.dsum + off, 512, bars.rowv_full(rs));
           ++issued_rowv;
         }
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       const int qb = (i_start + it) * kTileRows + h * 64;  // first query column of this half
       const int rs = it & 1;                                // row-vector slot of this query tile
       const float* rowv = reinterpret_cast<const float*>(gbase + C::OFF_ROWV + rs * C::ROWV_BYTES);
-      const float* lse2 = rowv + h * 64;
+      const float* nlse2 = rowv + h * 64;  // -LSE2: the exponent's additive term
       const float* dsum = rowv + 128 + h * 64;
       wait(bars.s_full(), it & 1);
       tc_fence_after();
@@ -467,16 +467,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
 
       // P^T = exp2(S^T * scale*log2e - LSE2); masked entries are exactly 0.  Only query tiles the
       // causal diagonal crosses and a ragged last key block need the mask: columns below `lo` are zeroed.
+      // Neighbouring query columns travel as fp32 pairs (the workspace holds -LSE2, so one paired FMA
+      // forms two exponent arguments).
       const bool diag = CAUSAL && ((i_start + it) * kTileRows + coff < k0 + kTileRows - 1);
+      const uint64_t c2 = f2_pack(c_log2, c_log2);
       float p[64];
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + c);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 4; e += 2) {
           const int col = c + e;
-          p[col] = ex2_approx(fmaf(__uint_as_float(s[col >> 5][col & 31]), c_log2, -lv[e]));
+          const uint64_t s2 = f2_pack(__uint_as_float(s[col >> 5][col & 31]), __uint_as_float(s[col >> 5][(col + 1) & 31]));
+          float x0, x1;
+          f2_unpack(f2_fma(s2, c2, e ? f2_pack(l4.z, l4.w) : f2_pack(l4.x, l4.y)), x0, x1);
+          p[col] = ex2_approx(x0);
+          p[col + 1] = ex2_approx(x1);
         }
       }
       if (diag || ragged_kv) {
@@ -605,8 +611,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   }
 }
 
-// D = rowsum(dO o O), LSE2 = LSE * log2(e) (+inf on padding rows and on rows that see no key, so
-// that their recomputed probabilities are exactly 0), dQacc = 0.
+// D = rowsum(dO o O), -LSE2 = -LSE * log2(e) (-inf on padding rows and on rows that see no key, so
+// that their recomputed probabilities are exactly 0; stored negated, the exponent's additive term),
+// dQacc = 0.
 // TPR threads per row, 8 elements (16 bytes) per thread.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ BwdArgs a) {
@@ -648,10 +655,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
   if (sub == 0) {
     if (q < a.Nq) {
       const float lse = a.lse[static_cast<size_t>(bh) * a.Nq + q];
-      a.lse2[row] = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
+      a.nlse2[row] = lse == -INFINITY ? -INFINITY : -lse * 1.4426950408889634f;
       a.dsum[row] = acc;
     } else {
-      a.lse2[row] = INFINITY;
+      a.nlse2[row] = -INFINITY;
       a.dsum[row] = 0.f;
     }
   }

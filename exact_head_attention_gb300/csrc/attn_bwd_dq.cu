@@ -264,8 +264,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) pair_dq_kernel(const __grid_con
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int c0 = 2 * i, c1 = 2 * i + 1;  // columns inside this half
-          float ds0 = op(__uint_as_float(va[c0 >> 5][c0 & 31]), __uint_as_float(vb[c0 >> 5][c0 & 31]), c_log2, a.scale);
-          float ds1 = op(__uint_as_float(va[c1 >> 5][c1 & 31]), __uint_as_float(vb[c1 >> 5][c1 & 31]), c_log2, a.scale);
+          float ds0, ds1;
+          op.pair(__uint_as_float(va[c0 >> 5][c0 & 31]), __uint_as_float(va[c1 >> 5][c1 & 31]),
+                  __uint_as_float(vb[c0 >> 5][c0 & 31]), __uint_as_float(vb[c1 >> 5][c1 & 31]), c_log2, a.scale, ds0, ds1);
           if (need_mask) {
             if (h * 64 + c0 >= lim) ds0 = 0.f;
             if (h * 64 + c1 >= lim) ds1 = 0.f;
@@ -368,7 +369,7 @@ cudaError_t launch_bwd_dq(const BwdArgs& b, cudaStream_t stream) {
   a.tm_qb = b.tm_do;
   a.tm_kb = b.tm_v;
   a.tm_dq = b.tm_dq;
-  a.rv[0] = b.lse2;
+  a.rv[0] = b.nlse2;
   a.rv[1] = b.dsum;
   a.rv[2] = nullptr;
   a.rv[3] = nullptr;

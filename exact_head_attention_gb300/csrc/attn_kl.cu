@@ -558,8 +558,9 @@ __global__ void __launch_bounds__(kKlDkThreads, 1) kl_dk_kernel(const __grid_con
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int c0 = 2 * i, c1 = 2 * i + 1;
-          float d0 = op(__uint_as_float(va[c0 >> 5][c0 & 31]), __uint_as_float(vb[c0 >> 5][c0 & 31]), c_log2, a.scale);
-          float d1 = op(__uint_as_float(va[c1 >> 5][c1 & 31]), __uint_as_float(vb[c1 >> 5][c1 & 31]), c_log2, a.scale);
+          float d0, d1;
+          op.pair(__uint_as_float(va[c0 >> 5][c0 & 31]), __uint_as_float(va[c1 >> 5][c1 & 31]),
+                  __uint_as_float(vb[c0 >> 5][c0 & 31]), __uint_as_float(vb[c1 >> 5][c1 & 31]), c_log2, a.scale, d0, d1);
           if (need_mask) {
             if (h * 64 + c0 >= lim) d0 = 0.f;
             if (h * 64 + c1 >= lim) d1 = 0.f;

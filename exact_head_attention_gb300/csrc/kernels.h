@@ -46,7 +46,7 @@ struct BwdArgs {
   void* dq;            // [B][H][Nq][d] 16-bit, strides sdq
   RowStrides so, sdo, sdq;
   float* dq_acc;       // [B*H][Nq_pad][d] fp32 workspace (nullptr: deterministic dQ)
-  float* lse2;         // [B*H][Nq_pad] fp32 workspace: LSE * log2(e), +inf on padding rows
+  float* nlse2;        // [B*H][Nq_pad] fp32 workspace: -LSE * log2(e), -inf on padding rows and rows without keys
   float* dsum;         // [B*H][Nq_pad] fp32 workspace: rowsum(dO o O), 0 on padding rows
   uint32_t* err_word;
   int bh_count, heads, Nq, Nq_pad, Nk, d;

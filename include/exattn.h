@@ -276,7 +276,7 @@ attn_status attn_kl_bwd_ex(const void* Q1, const void* K1, const void* Q2, const
 /*
  * Bytes of device workspace attn_bwd needs for this shape: an fp32 dQ
  * accumulator [B,H,ceil(Nq/128)*128,d] plus two fp32 row vectors of the same
- * padded length (D = rowsum(dO o O) and the base-2 LSE).  Returns 0 for
+ * padded length (D = rowsum(dO o O) and the negated base-2 LSE).  Returns 0 for
  * invalid sizes.  The accumulator is the buffer that the thread blocks of
  * SparkAttention Figure 9 (and the column-block backward of "Fast Transformer
  * training with long sequences") add their dQ contributions into; D is that
@@ -436,7 +436,7 @@ attn_status attn_bwd_strided_ex(const void* Q, attn_strides q_strides, const voi
  * The three steps attn_bwd launches, callable one at a time (same arguments
  * and validation as attn_bwd; attn_bwd is exactly these three in this order on
  * `stream`, sharing `workspace`):
- *   attn_bwd_preprocess  D = rowsum(dO o O) and the base-2 LSE into the
+ *   attn_bwd_preprocess  D = rowsum(dO o O) and the negated base-2 LSE into the
  *                        workspace; zeroes the workspace's fp32 dQ accumulator
  *                        (SparkAttention Figure 9, the dPsum term).
  *   attn_bwd_kv_blocks   the fused pass over key/value blocks: writes dK and
