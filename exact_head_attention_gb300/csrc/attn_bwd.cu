@@ -70,6 +70,11 @@ struct BwdCfg {
   // Q/dO ring slots.  d = 128 gives one slot to the dQ staging tile: reducing dQ with the copy
   // engine from shared memory is far cheaper than per-thread atomics, which outweighs the shallower ring.
   static constexpr int NR = (D == 64) ? 6 : 3;
+  // A ring slot is freed by the completion of the query tile whose products last read it (one commit
+  // per tile, after dK, which follows dV).  NT tile barriers in turn: a slot's previous tile must not
+  // be NT tiles behind a tile that could already have completed (2 NT >= NR + 1).
+  static constexpr int NT = (NR == 3) ? 2 : 4;
+  static_assert(2 * NT >= NR + 1 && NT <= NR, "tile barriers");
   // fp32 dQ staging, 32 KB: d = 128, 64 query rows x 128 d in the accumulator's row-major layout (one
   // half per warpgroup in turn with the dS^T tile); d = 64, two [128 query][32 d] boxes (one per
   // warpgroup) in the 128-byte-swizzled layout of the accumulator's tensor map.
@@ -83,7 +88,7 @@ struct BwdCfg {
   static constexpr uint32_t OFF_ROWV = OFF_STAGE + STAGE_BYTES;
   static constexpr uint32_t ROWV_BYTES = 2 * 128 * 4;
   static constexpr uint32_t OFF_BAR = OFF_ROWV + 2 * ROWV_BYTES;
-  // kv_full, ring_full[NR], ring_empty[NR], s_full, s_used, dp_full, pd_ready, p_ready,
+  // kv_full, ring_full[NR], tile_free[NT] (NR reserved), s_full, s_used, dp_full, pd_ready, p_ready,
   // dq_full, dq_empty, done, mma_done, rowv_full[2], rowv_empty[2], dss_ready, dstile_free
   static constexpr int NBAR = 1 + 2 * NR + 15;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
@@ -99,7 +104,8 @@ struct BwdBars {
   int nr;
   __device__ uint32_t kv_full() const { return base; }
   __device__ uint32_t ring_full(int s) const { return base + 8 * (1 + s); }
-  __device__ uint32_t ring_empty(int s) const { return base + 8 * (1 + nr + s); }
+  // the Q_i/dO_i slots are free: query tile i's products have completed (its dK, and dV before it)
+  __device__ uint32_t tile_free(int k) const { return base + 8 * (1 + nr + k); }
   __device__ uint32_t at(int k) const { return base + 8 * (1 + 2 * nr + k); }
   __device__ uint32_t s_full() const { return at(0); }
   __device__ uint32_t s_used() const { return at(1); }
@@ -170,7 +176,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     mbar_init(bars.kv_full(), 1);
     for (int s = 0; s < NR; ++s) {
       mbar_init(bars.ring_full(s), 1);
-      mbar_init(bars.ring_empty(s), 1);
+      mbar_init(bars.tile_free(s), 1);
     }
     mbar_init(bars.s_full(), 1);
     mbar_init(bars.s_used(), 256);
@@ -232,7 +238,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
           bulk_load(sRowv + rs * C::ROWV_BYTES + 512, a.dsum + off, 512, bars.rowv_full(rs));
           ++issued_rowv;
         }
-        if (!mbar_wait(bars.ring_empty(s), ((L / NR) & 1) ^ 1, wc)) break;
+        if (L >= NR) {
+          const int tp = (L - NR) >> 1;  // the query tile whose products last read slot s
+          if (!mbar_wait(bars.tile_free(tp % C::NT), (tp / C::NT) & 1, wc)) break;
+        }
         mbar_arrive_expect_tx(bars.ring_full(s), C::TILE);
         const CUtensorMap* map = (L & 1) ? &a.tm_do : &a.tm_q;
         const int q_row = (i_start + (L >> 1)) * kTileRows;
@@ -311,14 +320,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         mma_ts_lo_rt(tdV, tY + p_col<D>(0), do_lo, idG, acc0);
 #pragma unroll
         for (int k = 1; k < 128 / 16; ++k) mma_ts_lo<true>(tdV, tY + p_col<D>(k), do_lo + k * (2048 >> 4), idG);
-        mma_commit(bars.ring_empty(slot_of(2 * it + 1)));
         if (!(ok = mbar_wait(bars.pd_ready(), it & 1, wc))) break;
         tc_fence_after();
         // dK += dS^T Q_i   (A: dS^T packed in TMEM X; B: Q_i [query][d] MN-major)
         mma_ts_lo_rt(tdK, tX + ds_col(0), q_lo, idG, acc0);
 #pragma unroll
         for (int k = 1; k < 128 / 16; ++k) mma_ts_lo<true>(tdK, tX + ds_col(k), q_lo + k * (2048 >> 4), idG);
-        mma_commit(bars.ring_empty(slot_of(2 * it)));
+        mma_commit(bars.tile_free(it % C::NT));  // both of tile i's ring slots
         // S^T_{i+1} overwrites X after dK_i has read it, and dQ_i overwrites Y after dV_i has read it
         // (MMAs of one thread run in order).
         if (it + 1 < n && !(ok = issue_S(it + 1))) break;
@@ -614,7 +622,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
 // D = rowsum(dO o O), -LSE2 = -LSE * log2(e) (-inf on padding rows and on rows that see no key, so
 // that their recomputed probabilities are exactly 0; stored negated, the exponent's additive term),
 // dQacc = 0.
-// TPR threads per row, 8 elements (16 bytes) per thread.
+// TPR threads per row, 8 elements (16 bytes) per thread; a block covers pre_rows<D>() consecutive rows of
+// one (batch, head), two per thread, with both rows' loads in flight before the first sum (one row per
+// thread measured the same or slower, four and eight slower).  The block's (batch, head) and row range
+// come from blockIdx.x by two 32-bit divisions.
+constexpr int kPreRowsPerThread = 2;
+template <int D>
+__host__ __device__ constexpr int pre_rows_per_pass() { return 256 / (D / 8); }
+template <int D>
+__host__ __device__ constexpr int pre_rows() { return kPreRowsPerThread * pre_rows_per_pass<D>(); }
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ BwdArgs a) {
   // O, dO and LSE may come from the kernels just before; the workspace may still be read by the
@@ -623,68 +640,101 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
   griddep_wait();
   griddep_launch_dependents();
   constexpr int TPR = D / 8;
-  constexpr int RPB = 256 / TPR;
-  const size_t row = static_cast<size_t>(blockIdx.x) * RPB + threadIdx.x / TPR;
+  constexpr int RPB = pre_rows_per_pass<D>();
+  constexpr int NP = kPreRowsPerThread;
+  const unsigned blocks_per_head = static_cast<unsigned>(a.Nq_pad) / pre_rows<D>();
+  const unsigned bh = blockIdx.x / blocks_per_head;
+  const int q0 = static_cast<int>(blockIdx.x - bh * blocks_per_head) * pre_rows<D>() + static_cast<int>(threadIdx.x) / TPR;
+  const unsigned batch = bh / static_cast<unsigned>(a.heads), head = bh - batch * static_cast<unsigned>(a.heads);
   const int sub = threadIdx.x % TPR;
-  const size_t total = static_cast<size_t>(a.bh_count) * a.Nq_pad;
-  const bool in_range = row < total;  // no early return: the whole warp takes part in the shuffles below
-  const int bh = in_range ? static_cast<int>(row / a.Nq_pad) : 0;
-  const int q = in_range ? static_cast<int>(row % a.Nq_pad) : a.Nq;
-  float acc = 0.f;
-  if (in_range && q < a.Nq) {
-    const long long b = bh / a.heads, h = bh % a.heads;
-    const long long so = b * a.so.b + h * a.so.h + q * a.so.n + sub * 8;
-    const long long sd = b * a.sdo.b + h * a.sdo.h + q * a.sdo.n + sub * 8;
-    const uint4 ov = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.o) + so));
-    const uint4 dv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.dout) + sd));
-    const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+  const uint16_t* o = static_cast<const uint16_t*>(a.o) + batch * a.so.b + head * a.so.h + sub * 8;
+  const uint16_t* dout = static_cast<const uint16_t*>(a.dout) + batch * a.sdo.b + head * a.sdo.h + sub * 8;
+  uint4 ov[NP], dv[NP];
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    const int q = q0 + p * RPB;
+    if (q < a.Nq) {
+      ov[p] = __ldg(reinterpret_cast<const uint4*>(o + q * a.so.n));
+      dv[p] = __ldg(reinterpret_cast<const uint4*>(dout + q * a.sdo.n));
+    } else {
+      ov[p] = dv[p] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  float acc[NP];
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    const uint32_t ow[4] = {ov[p].x, ov[p].y, ov[p].z, ov[p].w}, dw[4] = {dv[p].x, dv[p].y, dv[p].z, dv[p].w};
+    acc[p] = 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      acc = fmaf(unpack_lo<BF16>(ow[e]), unpack_lo<BF16>(dw[e]), acc);
-      acc = fmaf(unpack_hi<BF16>(ow[e]), unpack_hi<BF16>(dw[e]), acc);
+      acc[p] = fmaf(unpack_lo<BF16>(ow[e]), unpack_lo<BF16>(dw[e]), acc[p]);
+      acc[p] = fmaf(unpack_hi<BF16>(ow[e]), unpack_hi<BF16>(dw[e]), acc[p]);
     }
   }
 #pragma unroll
-  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (!in_range) return;
-  if (a.dq_acc != nullptr) {  // no accumulator in the deterministic mode
-    float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D + sub * 8);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  if (sub == 0) {
-    if (q < a.Nq) {
-      const float lse = a.lse[static_cast<size_t>(bh) * a.Nq + q];
-      a.nlse2[row] = lse == -INFINITY ? -INFINITY : -lse * 1.4426950408889634f;
-      a.dsum[row] = acc;
-    } else {
-      a.nlse2[row] = -INFINITY;
-      a.dsum[row] = 0.f;
+  for (int off = TPR / 2; off > 0; off >>= 1)
+#pragma unroll
+    for (int p = 0; p < NP; ++p) acc[p] += __shfl_xor_sync(0xffffffffu, acc[p], off);
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    const int q = q0 + p * RPB;
+    const size_t row = static_cast<size_t>(bh) * a.Nq_pad + q;
+    if (a.dq_acc != nullptr) {  // no accumulator in the deterministic mode
+      float4* z = reinterpret_cast<float4*>(a.dq_acc + row * D + sub * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (sub == 0) {
+      if (q < a.Nq) {
+        const float lse = a.lse[static_cast<size_t>(bh) * a.Nq + q];
+        a.nlse2[row] = lse == -INFINITY ? -INFINITY : -lse * 1.4426950408889634f;
+        a.dsum[row] = acc[p];
+      } else {
+        a.nlse2[row] = -INFINITY;
+        a.dsum[row] = 0.f;
+      }
     }
   }
 }
 
-// dQ = scale * dQacc, rounded to the input dtype; 8 elements per thread.
+// dQ = scale * dQacc, rounded to the input dtype.  A block covers 2 x 256 chunks of 8 elements of one
+// (batch, head); each thread loads both of its chunks before it converts either.  The accumulator's
+// rows of one head are contiguous, so a chunk's source is the head's base plus 8 x its index.
+constexpr int kConvChunks = 512;
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const __grid_constant__ BwdArgs a) {
   griddep_wait();  // the accumulator is complete once the main kernel has finished
-  const size_t e = (static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x) * 8;
-  const size_t total = static_cast<size_t>(a.bh_count) * a.Nq * D;
-  if (e >= total) return;
-  const size_t row = e / D;
-  const int col = static_cast<int>(e % D);
-  const size_t bh = row / a.Nq, q = row % a.Nq;
-  const float4* src = reinterpret_cast<const float4*>(a.dq_acc + (bh * a.Nq_pad + q) * D + col);
-  const long long b = static_cast<long long>(bh / a.heads), h = static_cast<long long>(bh % a.heads);
-  const long long dst = b * a.sdq.b + h * a.sdq.h + static_cast<long long>(q) * a.sdq.n + col;
-  const float4 x = src[0], y = src[1];
+  constexpr int CPR = D / 8;  // chunks per row
+  const int chunks = a.Nq * CPR;
+  const unsigned blocks_per_head = static_cast<unsigned>((chunks + kConvChunks - 1) / kConvChunks);
+  const unsigned bh = blockIdx.x / blocks_per_head;
+  const int c0 = static_cast<int>(blockIdx.x - bh * blocks_per_head) * kConvChunks + static_cast<int>(threadIdx.x);
+  const unsigned batch = bh / static_cast<unsigned>(a.heads), head = bh - batch * static_cast<unsigned>(a.heads);
+  const float* acc = a.dq_acc + static_cast<size_t>(bh) * a.Nq_pad * D;
+  uint16_t* dq = static_cast<uint16_t*>(a.dq) + batch * a.sdq.b + head * a.sdq.h;
+  float4 x[2], y[2];
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const int c = c0 + p * 256;
+    if (c < chunks) {
+      const float4* src = reinterpret_cast<const float4*>(acc + static_cast<size_t>(c) * 8);
+      x[p] = src[0];
+      y[p] = src[1];
+    }
+  }
   const float s = a.scale;
-  uint4 out;
-  out.x = pack2<BF16>(x.x * s, x.y * s);
-  out.y = pack2<BF16>(x.z * s, x.w * s);
-  out.z = pack2<BF16>(y.x * s, y.y * s);
-  out.w = pack2<BF16>(y.z * s, y.w * s);
-  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dq) + dst) = out;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const int c = c0 + p * 256;
+    if (c >= chunks) continue;
+    uint4 out;
+    out.x = pack2<BF16>(x[p].x * s, x[p].y * s);
+    out.y = pack2<BF16>(x[p].z * s, x[p].w * s);
+    out.z = pack2<BF16>(y[p].x * s, y[p].y * s);
+    out.w = pack2<BF16>(y[p].z * s, y[p].w * s);
+    const int q = c / CPR, col = (c % CPR) * 8;
+    *reinterpret_cast<uint4*>(dq + static_cast<long long>(q) * a.sdq.n + col) = out;
+  }
 }
 
 // Launches `kern` with programmatic stream serialisation: it may start before the previous kernel on
@@ -710,10 +760,9 @@ template <int D, bool CAUSAL, bool BF16>
 cudaError_t launch_bwd_t(const BwdArgs& a, int steps, cudaStream_t stream) {
   using C = BwdCfg<D>;
   if (steps & kBwdPre) {
-    constexpr int RPB = 256 / (D / 8);
-    const size_t rows = static_cast<size_t>(a.bh_count) * a.Nq_pad;
-    cudaError_t e = launch_dependent(bwd_pre_kernel<D, BF16>, dim3(static_cast<unsigned>((rows + RPB - 1) / RPB)), 256, 0,
-                                     stream, a);
+    static_assert(kTileRows % pre_rows<D>() == 0, "a block's rows lie inside one head's padded rows");
+    const size_t blocks = static_cast<size_t>(a.bh_count) * (a.Nq_pad / pre_rows<D>());
+    cudaError_t e = launch_dependent(bwd_pre_kernel<D, BF16>, dim3(static_cast<unsigned>(blocks)), 256, 0, stream, a);
     if (e != cudaSuccess) return e;
   }
   if (steps & kBwdMain) {
@@ -726,9 +775,9 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int steps, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   if ((steps & kBwdConvert) && a.dq_acc) {
-    const size_t total = static_cast<size_t>(a.bh_count) * a.Nq * D / 8;
-    cudaError_t e = launch_dependent(bwd_dq_convert_kernel<D, BF16>, dim3(static_cast<unsigned>((total + 255) / 256)), 256, 0,
-                                     stream, a);
+    const size_t per_head = (static_cast<size_t>(a.Nq) * (D / 8) + kConvChunks - 1) / kConvChunks;
+    cudaError_t e = launch_dependent(bwd_dq_convert_kernel<D, BF16>, dim3(static_cast<unsigned>(a.bh_count * per_head)), 256,
+                                     0, stream, a);
     if (e != cudaSuccess) return e;
   }
   if (steps & kBwdDq) return launch_bwd_dq(a, stream);
