@@ -349,7 +349,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
 #pragma unroll
           for (int k = 1; k < 128 / 16; ++k) mma_ss_lo<true>(tY, ds_mn + k * (2048 >> 4), k_mn + k * (2048 >> 4), idQ);
         }
-        mma_commit(bars.dq_full());  // also frees the dS^T tile (ds_empty)
+        // dq_full also frees the dS^T tile (ds_empty).  At d = 64 the compute warps read dQ_i only after
+        // dP_{i+1} has landed, whose commit covers dQ_i too: only the last tile's dQ needs its own.
+        if (D == 128 || it + 1 == n) mma_commit(bars.dq_full());
         if (it + 1 < n && !(ok = issue_dP(it + 1))) break;
       }
       if (ok) mma_commit(bars.done());
@@ -428,8 +430,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         const uint32_t none[32] = {};
         drain128(it, false, none);
       } else {
-        wait(bars.dq_full(), it & 1);
-        tc_fence_after();
+        // dQ_i is complete: for i < n - 1 the dP^T_{i+1} wait of this iteration showed it (dQ_i was
+        // issued before dP_{i+1}); the last tile's dQ has a commit of its own.
+        if (it + 1 == n) {
+          wait(bars.dq_full(), 0);
+          tc_fence_after();
+        }
         // dQ_i: lane = query row; this warpgroup reduces d columns [32h, 32h + 32).  Its box [128
         // query][32 d] (128 bytes per row) goes into its half of the staging tile with the 128-byte
         // swizzle of the accumulator's tensor map (a thread writes one row: no bank conflicts), and one
@@ -547,7 +553,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       tc_fence_before();
       mbar_arrive(bars.pd_ready());  // dK_i and S_{i+1} may go
       if constexpr (!DQ) continue;
-      if (it > 0) wait(bars.ds_empty(), (it - 1) & 1);
+      // The dQ_{i-1} MMA has read the dS^T tile.  At d = 64 the dP^T_i wait above showed that already.
+      if (D == 128 && it > 0) wait(bars.ds_empty(), (it - 1) & 1);
       if constexpr (D == 128) {
         // The dS^T tile held warpgroup 1's dQ_{i-1} rows; the copy engine must have read them.
         if (it > 0 && h == 1) {

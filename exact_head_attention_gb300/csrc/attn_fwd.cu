@@ -60,6 +60,11 @@ struct FwdCfg {
   static constexpr int NCH = D / 64;                      // 128-byte chunks per row
   static constexpr uint32_t TILE = kTileRows * D * 2;     // one 128-row 16-bit tile
   static constexpr int NS = (D == 64) ? 4 : 2;            // K and V ring depth
+  // NS = 2: the ring slots are freed by the score commits of query tile 1 (S_1[j] completes after K_j's
+  // last read, and after the P V_{j-1} products), so no commit of their own.  A deeper ring could let the
+  // producer fall two of those commits behind, where a parity wait cannot tell them apart: it keeps
+  // its own empty barriers.
+  static constexpr bool FREE_BY_S1 = (NS == 2);
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE;
   static constexpr uint32_t OFF_V = OFF_K + NS * TILE;
@@ -218,12 +223,19 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a, const uint32_t* units
         for (int j = 0; j < ntile1; ++j) {
           const int s = j % NS;
           const uint32_t ph = (j / NS) & 1;
-          if (!mbar_wait(bars.k_empty(s), ph ^ 1, wc)) break;
+          // K_{j-NS} is free once S_1[j-NS] has completed; V_{j-NS} once S_1[j-NS+1] has (it follows
+          // P_1 V_{j-NS}).  The producer is at most one of these commits behind: S_1[j-NS+2] = S_1[j]
+          // needs the K_j it is about to load.
+          if (C::FREE_BY_S1 ? (j >= NS && !mbar_wait(bars.s_full(1), (j - NS) & 1, wc))
+                            : !mbar_wait(bars.k_empty(s), ph ^ 1, wc))
+            break;
           mbar_arrive_expect_tx(bars.k_full(s), C::TILE);
           for (int c = 0; c < C::NCH; ++c)
             tma_load_4d(sK + s * C::TILE + c * kChunkBytes, &a.tm_k, c * 64, j * kTileRows, head, batch, bars.k_full(s));
           ++issued_k;
-          if (!mbar_wait(bars.v_empty(s), ph ^ 1, wc)) break;
+          if (C::FREE_BY_S1 ? (j >= NS && !mbar_wait(bars.s_full(1), (j - NS + 1) & 1, wc))
+                            : !mbar_wait(bars.v_empty(s), ph ^ 1, wc))
+            break;
           mbar_arrive_expect_tx(bars.v_full(s), C::TILE);
           for (int c = 0; c < C::NCH; ++c)
             tma_load_4d(sV + s * C::TILE + c * kChunkBytes, &a.tm_v, c * 64, j * kTileRows, head, batch, bars.v_full(s));
@@ -234,9 +246,10 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a, const uint32_t* units
           for (int j = max(0, issued_k - NS); j < issued_k; ++j) mbar_drain(bars.k_full(j % NS), (j / NS) & 1, a.timeout_ns);
           for (int j = max(0, issued_v - NS); j < issued_v; ++j) mbar_drain(bars.v_full(j % NS), (j / NS) & 1, a.timeout_ns);
           mbar_drain(bars.q_full(), 0, a.timeout_ns);
-        } else if (MULTI && nunits > 1) {
+        } else if (!C::FREE_BY_S1 && MULTI && nunits > 1) {
           // Before the next block re-arms the barriers, the commits that free the ring slots (the last
-          // ones are never waited for otherwise) must all have arrived.
+          // ones are never waited for otherwise) must all have arrived.  (With FREE_BY_S1 they are the
+          // score commits, each of which softmax warpgroup 1 waits for.)
           for (int j = ntile1; j < ntile1 + NS; ++j) {
             if (!mbar_wait(bars.k_empty(j % NS), ((j / NS) & 1) ^ 1, wc)) break;
             if (!mbar_wait(bars.v_empty(j % NS), ((j / NS) & 1) ^ 1, wc)) break;
@@ -280,7 +293,7 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a, const uint32_t* units
 
         if (ok && ntile0 > 0) ok = issue_S(0, 0);
         if (ok) ok = issue_S(1, 0);
-        if (ok) mma_commit(bars.k_empty(0));
+        if (ok && !C::FREE_BY_S1) mma_commit(bars.k_empty(0));
         for (int j = 0; ok && j < ntile1; ++j) {
           if (j < ntile0) {
             if (!(ok = issue_PV(0, j))) break;
@@ -288,11 +301,11 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a, const uint32_t* units
             if (j + 1 < ntile0 && !(ok = issue_S(0, j + 1))) break;
           }
           if (!(ok = issue_PV(1, j))) break;
-          mma_commit(bars.v_empty(j % NS));
+          if (!C::FREE_BY_S1) mma_commit(bars.v_empty(j % NS));
           if (j == ntile1 - 1) mma_commit(bars.o_full(1));
           if (j + 1 < ntile1) {
             if (!(ok = issue_S(1, j + 1))) break;
-            mma_commit(bars.k_empty((j + 1) % NS));
+            if (!C::FREE_BY_S1) mma_commit(bars.k_empty((j + 1) % NS));
           }
         }
         // Every MMA issued above completes before TMEM can be released.
