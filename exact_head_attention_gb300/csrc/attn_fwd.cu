@@ -61,16 +61,20 @@ struct FwdCfg {
   static constexpr uint32_t TILE = kTileRows * D * 2;     // one 128-row 16-bit tile
   static constexpr int NS = (D == 64) ? 4 : 2;            // K and V ring depth
   // NS = 2: the ring slots are freed by the score commits of query tile 1 (S_1[j] completes after K_j's
-  // last read, and after the P V_{j-1} products), so no commit of their own.  A deeper ring could let the
-  // producer fall two of those commits behind, where a parity wait cannot tell them apart: it keeps
-  // its own empty barriers.
+  // last read, and after the P V_{j-1} products), so no commit of their own.  Those commits alternate
+  // between two barriers by the key tile's parity.  A parity wait finds the completion it means only if
+  // the waiter has seen the barrier's previous completion and the next one cannot have happened yet.
+  // Before loading K_j and V_j the producer waits for S_1[j-2] and S_1[j-1]: every completion of both
+  // barriers in turn, and on each barrier the completion after the awaited one is S_1[j] or S_1[j+1],
+  // which needs the K_j or K_{j+1} it has yet to load.  A deeper ring keeps its own empty barriers.
   static constexpr bool FREE_BY_S1 = (NS == 2);
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE;
   static constexpr uint32_t OFF_V = OFF_K + NS * TILE;
   static constexpr uint32_t OFF_BAR = OFF_V + NS * TILE;
-  // barriers: q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[2], p_full[2], o_full[2], mma_done
-  static constexpr int NBAR = 1 + 4 * NS + 7;
+  // barriers: q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[2], p_full[2], o_full[2], mma_done,
+  // s_full of query tile 1's odd key tiles (FREE_BY_S1)
+  static constexpr int NBAR = 1 + 4 * NS + 8;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (4 B) + abort flag (4 B)
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   static constexpr uint32_t SMEM_ALLOC = BYTES + 1024;      // slack for 1024-byte alignment
@@ -85,6 +89,7 @@ struct FwdBars {
   __device__ uint32_t v_full(int s) const { return base + 8 * (1 + 2 * ns + s); }
   __device__ uint32_t v_empty(int s) const { return base + 8 * (1 + 3 * ns + s); }
   __device__ uint32_t s_full(int t) const { return base + 8 * (1 + 4 * ns + t); }
+  __device__ uint32_t s_full_odd1() const { return base + 8 * (8 + 4 * ns); }
   __device__ uint32_t p_full(int t) const { return base + 8 * (3 + 4 * ns + t); }
   __device__ uint32_t o_full(int t) const { return base + 8 * (5 + 4 * ns + t); }
   __device__ uint32_t mma_done() const { return base + 8 * (7 + 4 * ns); }
@@ -117,6 +122,11 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a, const uint32_t* units
   const int nkv = (a.Nk + kTileRows - 1) / kTileRows;
   const int coff = CAUSAL ? a.causal_off : 0;
 
+  // Query tile t's score commit for key tile j, and the parity of a wait for it (FREE_BY_S1: tile 1's
+  // commits alternate between two barriers).
+  auto score_bar = [&](int t, int j) { return (C::FREE_BY_S1 && t == 1 && (j & 1)) ? bars.s_full_odd1() : bars.s_full(t); };
+  auto score_parity = [&](int t, int j) -> uint32_t { return (C::FREE_BY_S1 && t == 1) ? (j >> 1) & 1 : j & 1; };
+
   auto init_bars = [&] {
     mbar_init(bars.q_full(), 1);
     for (int s = 0; s < NS; ++s) {
@@ -130,6 +140,7 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a, const uint32_t* units
       mbar_init(bars.p_full(t), kTileRows);
       mbar_init(bars.o_full(t), 1);
     }
+    mbar_init(bars.s_full_odd1(), 1);
     mbar_init(bars.mma_done(), 1);
     fence_mbar_init();
   };
@@ -166,6 +177,7 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a, const uint32_t* units
         mbar_inval(bars.p_full(t));
         mbar_inval(bars.o_full(t));
       }
+      mbar_inval(bars.s_full_odd1());
       mbar_inval(bars.mma_done());
       init_bars();
     }
@@ -224,16 +236,15 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a, const uint32_t* units
           const int s = j % NS;
           const uint32_t ph = (j / NS) & 1;
           // K_{j-NS} is free once S_1[j-NS] has completed; V_{j-NS} once S_1[j-NS+1] has (it follows
-          // P_1 V_{j-NS}).  The producer is at most one of these commits behind: S_1[j-NS+2] = S_1[j]
-          // needs the K_j it is about to load.
-          if (C::FREE_BY_S1 ? (j >= NS && !mbar_wait(bars.s_full(1), (j - NS) & 1, wc))
+          // P_1 V_{j-NS}).
+          if (C::FREE_BY_S1 ? (j >= NS && !mbar_wait(score_bar(1, j - NS), score_parity(1, j - NS), wc))
                             : !mbar_wait(bars.k_empty(s), ph ^ 1, wc))
             break;
           mbar_arrive_expect_tx(bars.k_full(s), C::TILE);
           for (int c = 0; c < C::NCH; ++c)
             tma_load_4d(sK + s * C::TILE + c * kChunkBytes, &a.tm_k, c * 64, j * kTileRows, head, batch, bars.k_full(s));
           ++issued_k;
-          if (C::FREE_BY_S1 ? (j >= NS && !mbar_wait(bars.s_full(1), (j - NS + 1) & 1, wc))
+          if (C::FREE_BY_S1 ? (j >= NS && !mbar_wait(score_bar(1, j - NS + 1), score_parity(1, j - NS + 1), wc))
                             : !mbar_wait(bars.v_empty(s), ph ^ 1, wc))
             break;
           mbar_arrive_expect_tx(bars.v_full(s), C::TILE);
@@ -276,7 +287,7 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a, const uint32_t* units
             const uint32_t off = ((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4;
             mma_ss_lo<true>(d, a_lo + off, b_lo + off, idS);
           }
-          mma_commit(bars.s_full(t));
+          mma_commit(score_bar(t, j));
           return true;
         };
         auto issue_PV = [&](int t, int j) -> bool {
@@ -334,7 +345,7 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a, const uint32_t* units
       bool ok = true;
 
       for (int j = 0; j < n; ++j) {
-        if (!(ok = mbar_wait_warp(bars.s_full(t), j & 1, wc))) break;
+        if (!(ok = mbar_wait_warp(score_bar(t, j), score_parity(t, j), wc))) break;
         tc_fence_after();
         // Columns at or past `lim` are masked (ragged last key tile, causal diagonal tile).
         const bool need_mask =
