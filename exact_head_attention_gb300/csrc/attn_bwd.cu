@@ -31,7 +31,7 @@
 //   warps 0-3   compute, query columns [0, 64) of each tile (thread = key row),
 //               and query rows [0, 64) of the dQ drain
 //   warps 4-7   compute, query columns [64, 128), dQ query rows [64, 128)
-//   warp  8     TMA producer: K_j, V_j once; Q_i, dO_i through an NR-slot ring,
+//   warp  8     TMA producer: K_j, V_j once; Q_i and dO_i through two rings,
 //               LSE2_i and D_i through a 2-slot ring
 //   warp  9     MMA issuer (one thread) and TMEM owner
 // Tensor memory (512 columns):
@@ -70,11 +70,14 @@ struct BwdCfg {
   // Q/dO ring slots.  d = 128 gives one slot to the dQ staging tile: reducing dQ with the copy
   // engine from shared memory is far cheaper than per-thread atomics, which outweighs the shallower ring.
   static constexpr int NR = (D == 64) ? 6 : 3;
-  // A ring slot is freed by the completion of the query tile whose products last read it (one commit
-  // per tile, after dK, which follows dV).  NT tile barriers in turn: a slot's previous tile must not
-  // be NT tiles behind a tile that could already have completed (2 NT >= NR + 1).
-  static constexpr int NT = (NR == 3) ? 2 : 4;
-  static_assert(2 * NT >= NR + 1 && NT <= NR, "tile barriers");
+  // The ring is two: NQ slots take Q_i, freed by dK_i (its last reader), and NO slots take dO_i.  At
+  // d = 128 the one dO slot is freed by dV_i, a product before dK_i, so the load of dO_{i+1} (needed by
+  // dP_{i+1}, three products after dV_i) starts as early as it can.  At d = 64 the rings are deep enough
+  // for dO_i's slot to be freed with Q_i's, by one commit per tile.
+  static constexpr int NQ = (D == 64) ? 3 : 2;
+  static constexpr int NO = NR - NQ;
+  static constexpr bool DO_OWN_FREE = (D == 128);
+  static_assert(DO_OWN_FREE || NO == NQ, "dO slots freed with the Q slots of the same tile");
   // fp32 dQ staging, 32 KB: d = 128, 64 query rows x 128 d in the accumulator's row-major layout (one
   // half per warpgroup in turn with the dS^T tile); d = 64, two [128 query][32 d] boxes (one per
   // warpgroup) in the 128-byte-swizzled layout of the accumulator's tensor map.
@@ -88,7 +91,7 @@ struct BwdCfg {
   static constexpr uint32_t OFF_ROWV = OFF_STAGE + STAGE_BYTES;
   static constexpr uint32_t ROWV_BYTES = 2 * 128 * 4;
   static constexpr uint32_t OFF_BAR = OFF_ROWV + 2 * ROWV_BYTES;
-  // kv_full, ring_full[NR], tile_free[NT] (NR reserved), s_full, s_used, dp_full, pd_ready, p_ready,
+  // kv_full, q_full[NQ], do_full[NO], q_free[NQ], do_free[NO], s_full, s_used, dp_full, pd_ready, p_ready,
   // dq_full, dq_empty, done, mma_done, rowv_full[2], rowv_empty[2], dss_ready, dstile_free
   static constexpr int NBAR = 1 + 2 * NR + 15;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
@@ -101,11 +104,12 @@ struct BwdCfg {
 
 struct BwdBars {
   uint32_t base;
-  int nr;
+  int nr, nq;
   __device__ uint32_t kv_full() const { return base; }
-  __device__ uint32_t ring_full(int s) const { return base + 8 * (1 + s); }
-  // the Q_i/dO_i slots are free: query tile i's products have completed (its dK, and dV before it)
-  __device__ uint32_t tile_free(int k) const { return base + 8 * (1 + nr + k); }
+  __device__ uint32_t q_full(int s) const { return base + 8 * (1 + s); }
+  __device__ uint32_t do_full(int s) const { return base + 8 * (1 + nq + s); }
+  __device__ uint32_t q_free(int s) const { return base + 8 * (1 + nr + s); }        // dK of the slot's tile done
+  __device__ uint32_t do_free(int s) const { return base + 8 * (1 + nr + nq + s); }  // dV of the slot's tile done
   __device__ uint32_t at(int k) const { return base + 8 * (1 + 2 * nr + k); }
   __device__ uint32_t s_full() const { return at(0); }
   __device__ uint32_t s_used() const { return at(1); }
@@ -153,7 +157,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sDS = sbase + C::OFF_DS;
   const uint32_t sRing = sbase + C::OFF_RING;
   const uint32_t sRowv = sbase + C::OFF_ROWV;
-  const BwdBars bars{sbase + C::OFF_BAR, NR};
+  const BwdBars bars{sbase + C::OFF_BAR, NR, C::NQ};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + C::OFF_MISC + 4);
   const WaitCtx wc{abort_flag, a.err_word, a.timeout_ns};
@@ -174,9 +178,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
     mbar_init(bars.kv_full(), 1);
-    for (int s = 0; s < NR; ++s) {
-      mbar_init(bars.ring_full(s), 1);
-      mbar_init(bars.tile_free(s), 1);
+    for (int s = 0; s < C::NQ; ++s) {
+      mbar_init(bars.q_full(s), 1);
+      mbar_init(bars.q_free(s), 1);
+    }
+    for (int s = 0; s < C::NO; ++s) {
+      mbar_init(bars.do_full(s), 1);
+      mbar_init(bars.do_free(s), 1);
     }
     mbar_init(bars.s_full(), 1);
     mbar_init(bars.s_used(), 256);
@@ -225,32 +233,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     griddep_wait();
     griddep_launch_dependents();
     if (lane == 0 && n > 0) {
-      int issued = 0, issued_rowv = 0;
-      for (int L = 0; L < 2 * n; ++L) {
-        const int s = L % NR;
-        if ((L & 1) == 0) {
-          // LSE2 and D of query tile it = L/2 into row-vector slot it % 2
-          const int it = L >> 1, rs = it & 1;
-          if (!mbar_wait(bars.rowv_empty(rs), ((it >> 1) & 1) ^ 1, wc)) break;
-          mbar_arrive_expect_tx(bars.rowv_full(rs), C::ROWV_BYTES);
-          const size_t off = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows;
-          bulk_load(sRowv + rs * C::ROWV_BYTES, a.nlse2 + off, 512, bars.rowv_full(rs));
-          bulk_load(sRowv + rs * C::ROWV_BYTES + 512, a.dsum + off, 512, bars.rowv_full(rs));
-          ++issued_rowv;
-        }
-        if (L >= NR) {
-          const int tp = (L - NR) >> 1;  // the query tile whose products last read slot s
-          if (!mbar_wait(bars.tile_free(tp % C::NT), (tp / C::NT) & 1, wc)) break;
-        }
-        mbar_arrive_expect_tx(bars.ring_full(s), C::TILE);
-        const CUtensorMap* map = (L & 1) ? &a.tm_do : &a.tm_q;
-        const int q_row = (i_start + (L >> 1)) * kTileRows;
+      int issued_q = 0, issued_do = 0, issued_rowv = 0;
+      for (int it = 0; it < n; ++it) {
+        // LSE2 and D of query tile it into row-vector slot it % 2
+        const int rs = it & 1;
+        if (!mbar_wait(bars.rowv_empty(rs), ((it >> 1) & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(bars.rowv_full(rs), C::ROWV_BYTES);
+        const size_t off = static_cast<size_t>(bh) * a.Nq_pad + (i_start + it) * kTileRows;
+        bulk_load(sRowv + rs * C::ROWV_BYTES, a.nlse2 + off, 512, bars.rowv_full(rs));
+        bulk_load(sRowv + rs * C::ROWV_BYTES + 512, a.dsum + off, 512, bars.rowv_full(rs));
+        ++issued_rowv;
+        const int q_row = (i_start + it) * kTileRows;
+        // Q_it into slot it % NQ, once tile it - NQ's dK has completed (which also frees dO slot it % NO
+        // when the dO slots are freed with the Q ones)
+        const int sq = it % C::NQ;
+        if (!mbar_wait(bars.q_free(sq), ((it / C::NQ) & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(bars.q_full(sq), C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(sRing + s * C::TILE + c * kChunkBytes, map, c * 64, q_row, head, batch, bars.ring_full(s));
-        ++issued;
+          tma_load_4d(sRing + sq * C::TILE + c * kChunkBytes, &a.tm_q, c * 64, q_row, head, batch, bars.q_full(sq));
+        ++issued_q;
+        // dO_it into slot it % NO, once tile it - NO's dV has completed
+        const int so = it % C::NO;
+        if (C::DO_OWN_FREE && !mbar_wait(bars.do_free(so), ((it / C::NO) & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(bars.do_full(so), C::TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_4d(sRing + (C::NQ + so) * C::TILE + c * kChunkBytes, &a.tm_do, c * 64, q_row, head, batch,
+                      bars.do_full(so));
+        ++issued_do;
       }
       if (*abort_flag) {
-        for (int L = max(0, issued - NR); L < issued; ++L) mbar_drain(bars.ring_full(L % NR), (L / NR) & 1, a.timeout_ns);
+        for (int it = max(0, issued_q - C::NQ); it < issued_q; ++it)
+          mbar_drain(bars.q_full(it % C::NQ), (it / C::NQ) & 1, a.timeout_ns);
+        for (int it = max(0, issued_do - C::NO); it < issued_do; ++it)
+          mbar_drain(bars.do_full(it % C::NO), (it / C::NO) & 1, a.timeout_ns);
         for (int it = max(0, issued_rowv - 2); it < issued_rowv; ++it)
           mbar_drain(bars.rowv_full(it & 1), (it >> 1) & 1, a.timeout_ns);
         mbar_drain(bars.kv_full(), 0, a.timeout_ns);
@@ -264,8 +279,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       constexpr uint32_t idG = idesc_f16(128, D, BF16, false, true);      // dV, dK: A (TMEM) K-major, B MN-major
       constexpr uint32_t idQ = idesc_f16(128, D, BF16, true, true);       // dQ: A = dS MN-major, B = K MN-major
       constexpr uint32_t idQT = idesc_f16(D, 128, BF16, true, true);      // dQ^T: A = K^T MN-major, B = dS^T MN-major
-      auto slot_of = [](int L) { return L % NR; };
-      auto phase_of = [](int L) { return static_cast<uint32_t>((L / NR) & 1); };
+      // ring slot (in tiles from the ring's start) of Q_it and of dO_it
+      auto q_slot = [](int it) { return it % C::NQ; };
+      auto do_slot = [](int it) { return C::NQ + it % C::NO; };
       // Descriptor low words of the operand bases (K-major: leading offset unused; MN-major: the
       // 64-column chunk stride).  A K step adds a constant, so one thread keeps up with the tensor core.
       constexpr uint32_t kTileLo = C::TILE >> 4;
@@ -275,10 +291,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
 
       // S^T_i = K Q_i^T into X
       auto issue_S = [&](int it) -> bool {
-        const int L = 2 * it;
-        if (!mbar_wait(bars.ring_full(slot_of(L)), phase_of(L), wc)) return false;
+        if (!mbar_wait(bars.q_full(it % C::NQ), (it / C::NQ) & 1, wc)) return false;
         tc_fence_after();
-        const uint32_t b_lo = ring_kmaj + slot_of(L) * kTileLo;
+        const uint32_t b_lo = ring_kmaj + q_slot(it) * kTileLo;
         mma_ss_lo<false>(tX, k_kmaj, b_lo, idS);
 #pragma unroll
         for (int k = 1; k < D / 16; ++k) {
@@ -290,11 +305,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       };
       // dP^T_i = V dO_i^T into X (after the compute warps have read S^T_i)
       auto issue_dP = [&](int it) -> bool {
-        const int L = 2 * it + 1;
-        if (!mbar_wait(bars.ring_full(slot_of(L)), phase_of(L), wc)) return false;
+        if (!mbar_wait(bars.do_full(it % C::NO), (it / C::NO) & 1, wc)) return false;
         if (!mbar_wait(bars.s_used(), it & 1, wc)) return false;
         tc_fence_after();
-        const uint32_t b_lo = ring_kmaj + slot_of(L) * kTileLo;
+        const uint32_t b_lo = ring_kmaj + do_slot(it) * kTileLo;
         mma_ss_lo<false>(tX, v_kmaj, b_lo, idS);
 #pragma unroll
         for (int k = 1; k < D / 16; ++k) {
@@ -313,20 +327,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         // the compute warps form dS^T.
         if (!(ok = mbar_wait(bars.p_ready(), it & 1, wc))) break;
         tc_fence_after();
-        const uint32_t q_lo = ring_mn + slot_of(2 * it) * kTileLo;
-        const uint32_t do_lo = ring_mn + slot_of(2 * it + 1) * kTileLo;
+        const uint32_t q_lo = ring_mn + q_slot(it) * kTileLo;
+        const uint32_t do_lo = ring_mn + do_slot(it) * kTileLo;
         const uint32_t acc0 = it > 0 ? 1u : 0u;
         // dV += P^T dO_i   (A: P^T packed in TMEM Y; B: dO_i [query][d] MN-major, 16 query rows per K step)
         mma_ts_lo_rt(tdV, tY + p_col<D>(0), do_lo, idG, acc0);
 #pragma unroll
         for (int k = 1; k < 128 / 16; ++k) mma_ts_lo<true>(tdV, tY + p_col<D>(k), do_lo + k * (2048 >> 4), idG);
+        if (C::DO_OWN_FREE) mma_commit(bars.do_free(it % C::NO));  // dO_i's last reader
         if (!(ok = mbar_wait(bars.pd_ready(), it & 1, wc))) break;
         tc_fence_after();
         // dK += dS^T Q_i   (A: dS^T packed in TMEM X; B: Q_i [query][d] MN-major)
         mma_ts_lo_rt(tdK, tX + ds_col(0), q_lo, idG, acc0);
 #pragma unroll
         for (int k = 1; k < 128 / 16; ++k) mma_ts_lo<true>(tdK, tX + ds_col(k), q_lo + k * (2048 >> 4), idG);
-        mma_commit(bars.tile_free(it % C::NT));  // both of tile i's ring slots
+        mma_commit(bars.q_free(it % C::NQ));  // Q_i's last reader (and dO_i's, before it)
         // S^T_{i+1} overwrites X after dK_i has read it, and dQ_i overwrites Y after dV_i has read it
         // (MMAs of one thread run in order).
         if (it + 1 < n && !(ok = issue_S(it + 1))) break;
