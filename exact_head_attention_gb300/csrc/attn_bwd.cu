@@ -91,9 +91,9 @@ struct BwdCfg {
   static constexpr uint32_t OFF_ROWV = OFF_STAGE + STAGE_BYTES;
   static constexpr uint32_t ROWV_BYTES = 2 * 128 * 4;
   static constexpr uint32_t OFF_BAR = OFF_ROWV + 2 * ROWV_BYTES;
-  // kv_full, q_full[NQ], do_full[NO], q_free[NQ], do_free[NO], s_full, s_used, dp_full, pd_ready, p_ready,
-  // dq_full, dq_empty, done, mma_done, rowv_full[2], rowv_empty[2], dss_ready, dstile_free
-  static constexpr int NBAR = 1 + 2 * NR + 15;
+  // kv_full, q_full[NQ], do_full[NO], q_free[NQ], do_free[NO], s_full, s_used, dp_full, pd_ready[0], p_ready,
+  // dq_full, dq_empty, done, mma_done, rowv_full[2], rowv_empty[2], dss_ready, dstile_free, pd_ready[1]
+  static constexpr int NBAR = 1 + 2 * NR + 16;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16;
   // The operand tiles need 1024-byte alignment; the dynamic shared memory base is checked at entry
@@ -114,7 +114,9 @@ struct BwdBars {
   __device__ uint32_t s_full() const { return at(0); }
   __device__ uint32_t s_used() const { return at(1); }
   __device__ uint32_t dp_full() const { return at(2); }
-  __device__ uint32_t pd_ready() const { return at(3); }   // P^T, dS^T packed in TMEM X
+  // compute warpgroup h has packed its half of dS^T into TMEM X (the query columns [64h, 64h + 64): dK's
+  // K steps 4h .. 4h + 3); at d = 64 pd_ready(0) stands for both warpgroups
+  __device__ uint32_t pd_ready(int h) const { return h ? at(15) : at(3); }
   __device__ uint32_t dss_ready() const { return at(13); } // dS^T in shared memory
   // d = 128: the copy engine has read warpgroup 1's dQ rows out of the dS^T tile
   __device__ uint32_t dstile_free() const { return at(14); }
@@ -189,7 +191,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     mbar_init(bars.s_full(), 1);
     mbar_init(bars.s_used(), 256);
     mbar_init(bars.dp_full(), 1);
-    mbar_init(bars.pd_ready(), 256);
+    // d = 64: one hand-over for both warpgroups (pd_ready(0), 256 arrivals); d = 128: one each
+    mbar_init(bars.pd_ready(0), D == 128 ? 128 : 256);
+    mbar_init(bars.pd_ready(1), 128);
     mbar_init(bars.p_ready(), 256);
     mbar_init(bars.dss_ready(), 256);
     mbar_init(bars.dstile_free(), 1);
@@ -335,12 +339,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
 #pragma unroll
         for (int k = 1; k < 128 / 16; ++k) mma_ts_lo<true>(tdV, tY + p_col<D>(k), do_lo + k * (2048 >> 4), idG);
         if (C::DO_OWN_FREE) mma_commit(bars.do_free(it % C::NO));  // dO_i's last reader
-        if (!(ok = mbar_wait(bars.pd_ready(), it & 1, wc))) break;
+        // dK += dS^T Q_i   (A: dS^T packed in TMEM X; B: Q_i [query][d] MN-major).  At d = 128 in the two
+        // halves of its query (K) dimension, as the two compute warpgroups hand them over: warpgroup 0
+        // hands over first (it stages part of its dQ later).  At d = 64 the warpgroups finish together and
+        // a wait between the halves only cost time.
+        if (!(ok = mbar_wait(bars.pd_ready(0), it & 1, wc))) break;
         tc_fence_after();
-        // dK += dS^T Q_i   (A: dS^T packed in TMEM X; B: Q_i [query][d] MN-major)
         mma_ts_lo_rt(tdK, tX + ds_col(0), q_lo, idG, acc0);
 #pragma unroll
-        for (int k = 1; k < 128 / 16; ++k) mma_ts_lo<true>(tdK, tX + ds_col(k), q_lo + k * (2048 >> 4), idG);
+        for (int k = 1; k < 4; ++k) mma_ts_lo<true>(tdK, tX + ds_col(k), q_lo + k * (2048 >> 4), idG);
+        if (D == 128) {
+          if (!(ok = mbar_wait(bars.pd_ready(1), it & 1, wc))) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int k = 4; k < 128 / 16; ++k) mma_ts_lo<true>(tdK, tX + ds_col(k), q_lo + k * (2048 >> 4), idG);
         mma_commit(bars.q_free(it % C::NQ));  // Q_i's last reader (and dO_i's, before it)
         // S^T_{i+1} overwrites X after dK_i has read it, and dQ_i overwrites Y after dV_i has read it
         // (MMAs of one thread run in order).
@@ -404,7 +417,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     // ago); warpgroup 1 uses the dS^T tile, free from the end of the dQ_i MMA until the next dS^T store,
     // which waits for this reduction's read (see dstile_free).  The rows come out of TMEM 32 at a time;
     // with `pp`, this warpgroup's P^T of the next tile goes into the first 32 columns once they are read.
-    auto drain128 = [&](int it, bool with_p, const uint32_t (&pp)[32]) {
+    // Part a stages the first 32 rows, part b the other 32 and hands the block to the copy engine.
+    // Warpgroup 0 runs part b of dQ_{i-1} only after it has handed over its half of dS^T_i (its staging
+    // tile is its own), so the dK half it feeds can start while warpgroup 1 still drains.
+    const uint32_t buf_off = h ? C::OFF_DS : C::OFF_STAGE;
+    float* const buf = reinterpret_cast<float*>(gbase + buf_off);
+    auto drain128_a = [&](int it, bool with_p, const uint32_t (&pp)[32]) {
       wait(bars.dq_full(), it & 1);
       tc_fence_after();
       uint32_t v[32];
@@ -417,14 +435,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         tc_fence_before();
         mbar_arrive(bars.p_ready());  // dV of the next tile may go
       }
-      const uint32_t buf_off = h ? C::OFF_DS : C::OFF_STAGE;
       if (h == 0) {
         if (r == 0) tma_store_wait_read_all();  // the previous reduction from the staging tile
         named_bar_sync(1, 128);
       }
-      float* buf = reinterpret_cast<float*>(gbase + buf_off);
 #pragma unroll
       for (int c = 0; c < 32; ++c) buf[c * D + r] = __uint_as_float(v[c]);
+    };
+    auto drain128_b = [&](int it) {
+      uint32_t v[32];
       tmem_ld32(tY + lane_bits + h * 64 + 32, v);
       tmem_wait_ld();
       reg_fence32(v);
@@ -443,7 +462,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     auto drain_dq = [&](int it) {
       if constexpr (D == 128) {
         const uint32_t none[32] = {};
-        drain128(it, false, none);
+        drain128_a(it, false, none);
+        drain128_b(it);
       } else {
         // dQ_i is complete: for i < n - 1 the dP^T_{i+1} wait of this iteration showed it (dQ_i was
         // issued before dP_{i+1}); the last tile's dQ has a commit of its own.
@@ -530,7 +550,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       // half of Y (dQ_{i-1} runs just before dP^T_i), at d = 64 straight away.  dV_i then queues behind
       // dP^T_i.  Staging dQ_{i-1} for the copy engine fits before dP^T_i lands.
       if (DQ && D == 128 && it > 0) {
-        drain128(it - 1, true, pp);
+        drain128_a(it - 1, true, pp);
+        if (h == 1) drain128_b(it - 1);
       } else {
         tmem_st32(tY + lane_bits + p_base<D>() + h * p_stride<D>(), pp);
         tmem_wait_st();
@@ -566,7 +587,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       tmem_st32(tX + lane_bits + h * 64 + 32, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bars.pd_ready());  // dK_i and S_{i+1} may go
+      mbar_arrive(bars.pd_ready(D == 128 ? h : 0));  // dK_i (at d = 128 this half of it) may go
       if constexpr (!DQ) continue;
       // The dQ_{i-1} MMA has read the dS^T tile.  At d = 64 the dP^T_i wait above showed that already.
       if (D == 128 && it > 0) wait(bars.ds_empty(), (it - 1) & 1);
@@ -585,7 +606,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
       fence_proxy_async_smem();
       mbar_arrive(bars.dss_ready());  // dQ_i may go
 
-      // d = 64: the previous tile's dQ is staged and handed to the copy engine after this tile is handed over.
+      // The previous tile's dQ is staged and handed to the copy engine after this tile is handed over:
+      // at d = 128 warpgroup 0's second half, at d = 64 all of it.
+      if (DQ && D == 128 && it > 0 && h == 0) drain128_b(it - 1);
       if (DQ && D == 64 && it > 0) drain_dq(it - 1);
     }
     if (DQ && n > 0) drain_dq(n - 1);
